@@ -1,0 +1,316 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each ``check_*`` takes the oracle module (or a deliberately broken copy of it)
+and raises AssertionError when the oracle disagrees with the pin.  The pins are
+library routines computing the same quantity another way (torch's fp64
+scaled-dot-product attention with an explicit mask), counting formulations of
+the rank rules, brute force with scalar loops, closed forms and invariants.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+import torch
+
+
+def rand(gen, *shape):
+    return torch.randn(*shape, generator=gen, dtype=torch.float64).numpy()
+
+
+def sdpa(q, k, v, mask=None, scale=None):
+    """torch fp64 SDPA on [L, D] x [S, D] -> [L, D]; mask True = attend."""
+    qt, kt, vt = (torch.from_numpy(np.ascontiguousarray(x))[None, None] for x in (q, k, v))
+    mt = None if mask is None else torch.from_numpy(mask)[None, None]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mt, scale=scale)
+    return o[0, 0].numpy()
+
+
+# ----------------------------------------------------------- chunk attention --
+
+def check_chunk_attention(orc, seed=1, n=3, c=6, hq=4, hkv=2, d=8):
+    """Chunked prefill == dense attention over the whole prefix with a
+    block-diagonal mask (torch SDPA), head by head."""
+    gen = torch.Generator().manual_seed(seed)
+    rows = n * (c + 1)
+    q, k, v = rand(gen, rows, hq, d), rand(gen, rows, hkv, d), rand(gen, rows, hkv, d)
+    scale = 0.37
+    got = orc.chunk_attention(q, k, v, n, c, scale)
+    blk = np.arange(rows) // (c + 1)
+    mask = blk[:, None] == blk[None, :]
+    for h in range(hq):
+        g = h // (hq // hkv)
+        want = sdpa(q[:, h], k[:, g], v[:, g], mask, scale)
+        assert np.max(np.abs(got[:, h] - want)) < 1e-12, "chunk attention != masked dense SDPA"
+
+
+# ------------------------------------------------------------ window scores --
+
+def check_scores_vs_sdpa(orc, seed=2, n=3, c=5, w=4, hq=6, hkv=2, d=8):
+    """Attention with V = identity returns the probability matrix itself;
+    its column sums over window rows and heads are the scores."""
+    gen = torch.Generator().manual_seed(seed)
+    rows = n * (c + 1)
+    k = rand(gen, rows, hkv, d)
+    q_win = rand(gen, w, hq, d)
+    scale = 0.41
+    got = orc.window_scores(q_win, k, n, c, scale)
+    assert got.shape == (n, c + 1)
+    eye = np.eye(c + 1)
+    for j in range(n):
+        want = np.zeros(c + 1)
+        for h in range(hq):
+            g = h // (hq // hkv)
+            p = sdpa(q_win[:, h], k[j * (c + 1):(j + 1) * (c + 1), g], eye, None, scale)
+            want += p.sum(axis=0)
+        assert np.max(np.abs(got[j] - want)) < 1e-12, "scores != column sums of SDPA probabilities"
+
+
+def check_scores_brute_force(orc, seed=3):
+    """Scalar loops with math.exp on a tiny case."""
+    gen = torch.Generator().manual_seed(seed)
+    n, c, w, hq, hkv, d = 2, 3, 2, 2, 1, 3
+    rows = n * (c + 1)
+    k = rand(gen, rows, hkv, d)
+    q_win = rand(gen, w, hq, d)
+    scale = 0.9
+    got = orc.window_scores(q_win, k, n, c, scale)
+    for j in range(n):
+        for t in range(c + 1):
+            total = 0.0
+            for ww in range(w):
+                for h in range(hq):
+                    x = [scale * sum(q_win[ww, h, e] * k[j * (c + 1) + u, 0, e] for e in range(d))
+                         for u in range(c + 1)]
+                    total += math.exp(x[t]) / sum(math.exp(xu) for xu in x)
+            assert abs(got[j, t] - total) < 1e-12, "scores != scalar brute force"
+
+
+def check_scores_invariants(orc, seed=4):
+    """Each window row's probabilities sum to one, so every chunk's scores sum
+    to W * Hq; equal keys share the mass uniformly; one dominant key takes it."""
+    gen = torch.Generator().manual_seed(seed)
+    n, c, w, hq, hkv, d = 4, 9, 3, 4, 2, 8
+    rows = n * (c + 1)
+    k = rand(gen, rows, hkv, d)
+    q_win = rand(gen, w, hq, d)
+    got = orc.window_scores(q_win, k, n, c, 0.3)
+    assert np.max(np.abs(got.sum(axis=1) - w * hq)) < 1e-10, "scores do not sum to W*Hq"
+    k_eq = np.repeat(k[:1], rows, axis=0)
+    got = orc.window_scores(q_win, k_eq, n, c, 0.3)
+    assert np.max(np.abs(got - w * hq / (c + 1))) < 1e-12, "equal keys must split the mass evenly"
+    q1 = np.ones((1, 1, 4))
+    k1 = np.zeros((c + 1, 1, 4))
+    k1[5] = 100.0
+    got = orc.window_scores(q1, k1, 1, c, 1.0)
+    assert abs(got[0, 5] - 1.0) < 1e-12 and got[0, :5].max() < 1e-100, "dominant key must take all mass"
+
+
+def check_scores_single_row(orc, seed=5):
+    """W = 1, Hq = 1: the score row is one softmax row (torch.softmax)."""
+    gen = torch.Generator().manual_seed(seed)
+    c, d = 11, 16
+    k = rand(gen, c + 1, 1, d)
+    q_win = rand(gen, 1, 1, d)
+    got = orc.window_scores(q_win, k, 1, c, 0.25)
+    logits = torch.from_numpy(0.25 * (q_win[0, 0] @ k[:, 0].T))
+    want = torch.softmax(logits, dim=0).numpy()
+    assert np.max(np.abs(got[0] - want)) < 1e-14, "single-row scores != softmax"
+
+
+# ----------------------------------------------------------------- ranking --
+
+def beats(a_val, a_idx, b_val, b_idx):
+    """True when (a_val, a_idx) ranks strictly before (b_val, b_idx):
+    larger value first, -0 == +0, NaN last, ties to the lower index."""
+    a_nan, b_nan = math.isnan(a_val), math.isnan(b_val)
+    if a_nan != b_nan:
+        return b_nan
+    if not a_nan and a_val != b_val:
+        return a_val > b_val
+    return a_idx < b_idx
+
+
+def kept_by_counting(values, n_keep):
+    """Index t is kept iff fewer than n_keep indices beat it (O(n^2))."""
+    vals = [float(x) for x in values]
+    kept = []
+    for t, vt in enumerate(vals):
+        n_beat = sum(1 for u, vu in enumerate(vals) if u != t and beats(vu, u, vt, t))
+        if n_beat < n_keep:
+            kept.append(t)
+    return kept
+
+
+def ranked_by_counting(values, n_take):
+    """The first n_take indices in rank order, by counting who beats whom."""
+    vals = [float(x) for x in values]
+    rank = {}
+    for t, vt in enumerate(vals):
+        rank[t] = sum(1 for u, vu in enumerate(vals) if u != t and beats(vu, u, vt, t))
+    return [t for t, _ in sorted(rank.items(), key=lambda kv: kv[1])][:n_take]
+
+
+def top_b_cases():
+    gen = np.random.default_rng(7)
+    cases = []
+    cases.append(gen.standard_normal((5, 17)))
+    cases.append(np.round(gen.standard_normal((4, 21)) * 2) / 2)           # many exact ties
+    z = np.zeros((2, 9))
+    z[0, 3], z[1, 2] = -0.0, -0.0
+    z[0, 5] = 1.0
+    cases.append(z)                                                        # +/-0 ties
+    cases.append(np.full((3, 12), 0.25))                                   # all equal
+    base = np.ones((1, 7))
+    base[0, 4] = 1.0 + 1e-12                                              # equal after fp32 rounding
+    cases.append(base)
+    return cases
+
+
+def check_top_b(orc):
+    for scores in top_b_cases():
+        n, rows = scores.shape
+        for n_keep in sorted({0, 1, 3, rows - 2, rows - 1}):
+            if n_keep > rows - 1:
+                continue
+            got = orc.top_b(scores, n_keep)
+            assert got.shape == (n, n_keep)
+            for j in range(n):
+                want = kept_by_counting(scores[j, 1:].astype(np.float32), n_keep)
+                assert list(got[j]) == want, f"top_b mismatch on row {j}, B={n_keep}"
+
+
+def check_select(orc):
+    gen = np.random.default_rng(11)
+    cases = [
+        (gen.standard_normal(13).astype(np.float32), gen.standard_normal(13).astype(np.float32)),
+        (np.round(gen.standard_normal(16)).astype(np.float32), np.zeros(16, np.float32)),
+        (np.array([0.0, -0.0, 1.0, 0.0], np.float32), np.array([-0.0, 0.0, -1.0, -0.0], np.float32)),
+        # 1 + 2^-25 rounds to 1 in fp32: chunk 2 ties chunk 0 and loses on index
+        (np.array([1.0, 0.5, 1.0, 0.75], np.float32),
+         np.array([0.0, 0.0, 2.0 ** -25, 0.0], np.float32)),
+        (np.full(9, 0.5, np.float32), np.full(9, 0.25, np.float32)),
+    ]
+    for s_i, s_p in cases:
+        n = s_i.shape[0]
+        s_want = [float(np.float32(np.float32(a) + np.float32(b))) for a, b in zip(s_i, s_p)]
+        for k_sel in sorted({1, 2, n // 2, n}):
+            sel, s = orc.select_chunks(s_i, s_p, k_sel)
+            assert [float(x) for x in s] == s_want, "s must be the fp32 sum"
+            assert list(sel) == ranked_by_counting(s_want, k_sel), "select order mismatch"
+
+
+# ------------------------------------------------------------------ decode --
+
+def check_split_equals_concat(orc, seed=8):
+    """Split per chunk + LSE merge == one softmax over the concatenation."""
+    gen = torch.Generator().manual_seed(seed)
+    hq, hkv, d, lq = 6, 2, 16, 9
+    pool_rows = 40
+    pool_k, pool_v = rand(gen, pool_rows, hkv, d), rand(gen, pool_rows, hkv, d)
+    table = np.array([[0, 5], [7, 9], [20, 1], [25, 15]], dtype=np.int32)
+    sel = np.array([3, 0, 2], dtype=np.int32)
+    q, ks, vs = rand(gen, lq, hq, d), rand(gen, lq, hkv, d), rand(gen, lq, hkv, d)
+    out1, lse1 = orc.decode_attention(q, ks, vs, pool_k, pool_v, table, sel, 0.3)
+    out2, lse2 = orc.decode_attention_split(q, ks, vs, pool_k, pool_v, table, sel, 0.3)
+    assert np.max(np.abs(out1 - out2)) < 1e-12 and np.max(np.abs(lse1 - lse2)) < 1e-12
+
+
+def check_decode_vs_sdpa(orc, seed=9):
+    """Decode == SDPA over [selected rows ; live rows]; lse == logsumexp."""
+    gen = torch.Generator().manual_seed(seed)
+    hq, hkv, d, lq = 4, 2, 8, 5
+    pool_k, pool_v = rand(gen, 30, hkv, d), rand(gen, 30, hkv, d)
+    table = np.array([[2, 6], [10, 4], [16, 11]], dtype=np.int32)
+    sel = np.array([2, 1], dtype=np.int32)
+    q, ks, vs = rand(gen, lq, hq, d), rand(gen, lq, hkv, d), rand(gen, lq, hkv, d)
+    out, lse = orc.decode_attention(q, ks, vs, pool_k, pool_v, table, sel, 0.5)
+    rows = list(range(16, 27)) + list(range(10, 14))
+    kk = np.concatenate([pool_k[rows], ks], axis=0)
+    vv = np.concatenate([pool_v[rows], vs], axis=0)
+    for h in range(hq):
+        g = h // 2
+        want = sdpa(q[:, h], kk[:, g], vv[:, g], None, 0.5)
+        assert np.max(np.abs(out[:, h] - want)) < 1e-12, "decode != SDPA"
+        lg = torch.from_numpy(0.5 * q[:, h] @ kk[:, g].T)
+        assert np.max(np.abs(lse[:, h] - torch.logsumexp(lg, dim=1).numpy())) < 1e-12
+
+
+def check_dense_equivalence(orc, seed=10):
+    """K = N and B = C: the whole sparse path (scores, top-B, compaction,
+    selection, decode) equals dense attention of the live rows over every
+    prefix row (BOS rows included) and the live rows (torch SDPA)."""
+    gen = torch.Generator().manual_seed(seed)
+    n, c, w, hq, hkv, d, lq = 3, 6, 2, 4, 2, 8, 5
+    rows = n * (c + 1)
+    k, v = rand(gen, rows, hkv, d), rand(gen, rows, hkv, d)
+    q_win = rand(gen, w, hq, d)
+    scale = 0.35
+    scores = orc.window_scores(q_win, k, n, c, scale)
+    kept = orc.top_b(scores, c)
+    slot = np.array([2 * (c + 1), 0, c + 1], dtype=np.int32)       # permuted slots
+    pool_k, pool_v = np.zeros((rows, hkv, d)), np.zeros((rows, hkv, d))
+    table = orc.compact(k, v, kept, slot, c, pool_k, pool_v)
+    sel, _ = orc.select_chunks(rand(gen, n).astype(np.float32), np.zeros(n, np.float32), n)
+    q, ks, vs = rand(gen, lq, hq, d), rand(gen, lq, hkv, d), rand(gen, lq, hkv, d)
+    out, _ = orc.decode_attention(q, ks, vs, pool_k, pool_v, table, sel, scale)
+    kk = np.concatenate([k, ks], axis=0)
+    vv = np.concatenate([v, vs], axis=0)
+    for h in range(hq):
+        g = h // 2
+        want = sdpa(q[:, h], kk[:, g], vv[:, g], None, scale)
+        assert np.max(np.abs(out[:, h] - want)) < 1e-12, "K=N, B=C path != dense attention"
+
+
+def check_compact(orc, seed=12):
+    gen = torch.Generator().manual_seed(seed)
+    n, c, hkv, d, b = 3, 5, 2, 4, 2
+    rows = n * (c + 1)
+    k, v = rand(gen, rows, hkv, d), rand(gen, rows, hkv, d)
+    kept = np.array([[0, 4], [1, 2], [3, 4]], dtype=np.int32)
+    slot = np.array([6, 0, 3], dtype=np.int32)
+    pk, pv = np.full((9, hkv, d), np.nan), np.full((9, hkv, d), np.nan)
+    table = orc.compact(k, v, kept, slot, c, pk, pv)
+    assert table.tolist() == [[6, 3], [0, 3], [3, 3]]
+    for j in range(n):
+        src = [j * (c + 1)] + [j * (c + 1) + 1 + t for t in kept[j]]
+        assert np.array_equal(pk[slot[j]:slot[j] + b + 1], k[src])
+        assert np.array_equal(pv[slot[j]:slot[j] + b + 1], v[src])
+
+
+# -------------------------------------------------------------- cost model --
+
+def check_cost_model(orc):
+    """The oracle's MAC counts equal the closed forms, and they scale as the
+    per-step complexity O(N C^2 + (L_d^2 + K C) T) says: prefill linear in N
+    and quadratic in C; decode independent of N at fixed K, B, Lq."""
+    gen = torch.Generator().manual_seed(13)
+    hq, hkv, d = 4, 2, 8
+    for n, c, w in itertools.product((2, 3), (4, 7), (0, 3)):
+        rows = n * (c + 1)
+        q, k, v = rand(gen, rows, hq, d), rand(gen, rows, hkv, d), rand(gen, rows, hkv, d)
+        cnt = orc.MacCounter()
+        orc.chunk_attention(q, k, v, n, c, 0.3, counter=cnt)
+        orc.window_scores(rand(gen, w, hq, d), k, n, c, 0.3, counter=cnt)
+        assert cnt.macs == orc.prefill_macs(n, c, w, hq, d)
+        assert cnt.macs == 2 * hq * n * (c + 1) ** 2 * d + hq * n * w * (c + 1) * d
+    macs = []
+    for n in (4, 8):
+        pool_k, pool_v = rand(gen, n * 3, hkv, d), rand(gen, n * 3, hkv, d)
+        table = np.array([[3 * j, 3] for j in range(n)], dtype=np.int32)
+        sel = np.array([1, 3], dtype=np.int32)
+        lq = 5
+        q, ks, vs = rand(gen, lq, hq, d), rand(gen, lq, hkv, d), rand(gen, lq, hkv, d)
+        cnt = orc.MacCounter()
+        orc.decode_attention(q, ks, vs, pool_k, pool_v, table, sel, 0.3, counter=cnt)
+        assert cnt.macs == orc.decode_step_macs(lq, 6, hq, d) == 2 * hq * lq * (6 + lq) * d
+        macs.append(cnt.macs)
+    assert macs[0] == macs[1], "decode cost must not depend on N"
+
+
+ALL_CHECKS = [
+    check_chunk_attention, check_scores_vs_sdpa, check_scores_brute_force, check_scores_invariants,
+    check_scores_single_row, check_top_b, check_select, check_split_equals_concat,
+    check_decode_vs_sdpa, check_dense_equivalence, check_compact, check_cost_model,
+]

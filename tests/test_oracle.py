@@ -1,0 +1,131 @@
+"""CPU tests: the oracle against its pins, and planted mistakes against the pins."""
+import numpy as np
+import pytest
+
+from oracle import pfd_oracle as orc
+from tests import oracle_pins as pins
+
+
+@pytest.mark.parametrize("check", pins.ALL_CHECKS, ids=lambda f: f.__name__)
+def test_oracle_pin(check):
+    check(orc)
+
+
+class Mutant:
+    """The oracle with some functions replaced by broken versions."""
+
+    def __init__(self, **overrides):
+        self.__dict__.update(overrides)
+
+    def __getattr__(self, name):
+        return getattr(orc, name)
+
+
+def _chunk_attention_global(q, k, v, n, c, scale, counter=None):
+    # mistake: attends across chunk boundaries (no block-diagonal mask)
+    out = np.empty(q.shape)
+    g = q.shape[1] // k.shape[1]
+    for h in range(q.shape[1]):
+        p = orc.softmax_rows(scale * q[:, h] @ k[:, h // g].T)
+        out[:, h] = p @ v[:, h // g]
+    return out
+
+
+def _chunk_attention_bad_gqa(q, k, v, n, c, scale, counter=None):
+    # mistake: query head h reads KV head h % Hkv instead of h // G
+    hkv = k.shape[1]
+    out = np.empty(q.shape)
+    rows = c + 1
+    for j in range(n):
+        sl = slice(j * rows, (j + 1) * rows)
+        for h in range(q.shape[1]):
+            p = orc.softmax_rows(scale * q[sl, h] @ k[sl, h % hkv].T)
+            out[sl, h] = p @ v[sl, h % hkv]
+    return out
+
+
+def _scores_wrong_axis(q_win, k, n, c, scale, counter=None):
+    # mistake: normalises over the window rows instead of over the keys
+    rows = c + 1
+    g = q_win.shape[1] // k.shape[1]
+    out = np.zeros((n, rows))
+    for j in range(n):
+        for h in range(q_win.shape[1]):
+            x = scale * q_win[:, h] @ k[j * rows:(j + 1) * rows, h // g].T
+            out[j] += orc.softmax_rows(x.T).T.sum(axis=0)
+    return out
+
+
+def _scores_no_scale(q_win, k, n, c, scale, counter=None):
+    return orc.window_scores(q_win, k, n, c, 1.0)
+
+
+def _scores_drops_last_head(q_win, k, n, c, scale, counter=None):
+    # mistake: the sum over query heads stops one head short
+    rows = c + 1
+    g = q_win.shape[1] // k.shape[1]
+    out = np.zeros((n, rows))
+    for j in range(n):
+        for h in range(q_win.shape[1] - 1):
+            x = scale * q_win[:, h] @ k[j * rows:(j + 1) * rows, h // g].T
+            out[j] += orc.softmax_rows(x).sum(axis=0)
+    return out
+
+
+def _top_b_high_index_ties(scores, n_keep):
+    content = scores[:, 1:].astype(np.float32)
+    kept = np.empty((scores.shape[0], n_keep), np.int32)
+    for j in range(scores.shape[0]):
+        order = sorted(range(content.shape[1]), key=lambda t: (-float(content[j, t]), -t))
+        kept[j] = sorted(order[:n_keep])
+    return kept
+
+
+def _top_b_with_bos(scores, n_keep):
+    kept = np.empty((scores.shape[0], n_keep), np.int32)
+    for j in range(scores.shape[0]):
+        order = sorted(range(scores.shape[1]), key=lambda t: (-float(np.float32(scores[j, t])), t))
+        kept[j] = sorted(order[:n_keep])
+    return kept
+
+
+def _select_fp64(s_i, s_p, n_select):
+    s = s_i.astype(np.float64) + s_p.astype(np.float64)
+    order = sorted(range(s.shape[0]), key=lambda j: (-s[j], j))
+    return np.array(order[:n_select], np.int32), s.astype(np.float32)
+
+
+def _decode_no_self(q, ks, vs, pk, pv, table, sel, scale, counter=None):
+    return orc.decode_attention(q, ks[:0], vs[:0], pk, pv, table, sel, scale)
+
+
+def _decode_split_no_rescale(q, ks, vs, pk, pv, table, sel, scale):
+    group = q.shape[1] // ks.shape[1]
+    parts = [orc.split_partials(q, pk[t[0]:t[0] + t[1]], pv[t[0]:t[0] + t[1]], group, scale)
+             for t in (table[c] for c in sel)]
+    parts.append(orc.split_partials(q, ks, vs, group, scale))
+    l = sum(p[1] for p in parts)
+    acc = sum(p[2] for p in parts)
+    return acc / l[..., None], np.log(l)
+
+
+MUTANTS = {
+    "cross_chunk_attention": (Mutant(chunk_attention=_chunk_attention_global), pins.check_chunk_attention),
+    "gqa_mapping": (Mutant(chunk_attention=_chunk_attention_bad_gqa), pins.check_chunk_attention),
+    "scores_softmax_axis": (Mutant(window_scores=_scores_wrong_axis), pins.check_scores_vs_sdpa),
+    "scores_scale_dropped": (Mutant(window_scores=_scores_no_scale), pins.check_scores_brute_force),
+    "scores_one_head": (Mutant(window_scores=_scores_drops_last_head), pins.check_scores_vs_sdpa),
+    "topb_tie_high_index": (Mutant(top_b=_top_b_high_index_ties), pins.check_top_b),
+    "topb_ranks_bos": (Mutant(top_b=_top_b_with_bos), pins.check_top_b),
+    "select_in_fp64": (Mutant(select_chunks=_select_fp64), pins.check_select),
+    "decode_drops_self_block": (Mutant(decode_attention=_decode_no_self), pins.check_decode_vs_sdpa),
+    "merge_without_rescale": (Mutant(decode_attention_split=_decode_split_no_rescale),
+                              pins.check_split_equals_concat),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name):
+    mutant, check = MUTANTS[name]
+    with pytest.raises(AssertionError):
+        check(mutant)
