@@ -1,0 +1,210 @@
+/*
+ * pfd.h -- C ABI of libpfd: sparse chunked-KV prefill and static-KV decode
+ * attention for diffusion language models, on one NVIDIA GB300 (sm_103a).
+ *
+ * The method is the one of "Prefilling-dLLM: Predictive Prefilling for
+ * Long-Context Inference in Diffusion Language Models" (technical summary):
+ *   Methodology 1, "Chunked Prefill and KV Caching"   -> pfd_chunk_prefill,
+ *                                                        pfd_select_chunks
+ *   Methodology 2, "Two-Level Sparsity"                -> the top-B inside
+ *                                                        pfd_chunk_prefill and
+ *                                                        the top-K selection
+ *   Methodology 3, "Decoding with Static KV Reuse" and
+ *   "Attention Kernel Optimization" (split-KV, LSE merge) -> pfd_decode_attention
+ *
+ * Conventions shared by every call:
+ *   - Tensors are token-major and contiguous: a [rows, heads, D] tensor keeps
+ *     the D values of one (row, head) together, heads of a row together.
+ *   - bf16 values are passed as raw 16-bit patterns (pfd_bf16).
+ *   - Every pointer named as device memory must be CUDA device memory on the
+ *     current device; the caller owns all memory.  The library allocates
+ *     nothing and keeps no state between calls other than process-wide,
+ *     read-only caches (the device's SM count, the TMA encoder entry point).
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream).  The return value reports only what the host can check:
+ *     invalid arguments (PFD_ERR_INVALID_ARG), shapes outside the supported
+ *     set (PFD_ERR_UNSUPPORTED) and launch failures (PFD_ERR_CUDA).  Nothing
+ *     is launched when the return value is not PFD_OK.
+ *   - Errors found in device-resident data (a chunk-table entry, a selected
+ *     index or a pool slot out of range) never trap: the offending item is
+ *     skipped and a PFD_DEVERR_* bit is OR-ed into *dev_err when dev_err is
+ *     not NULL.  The kernels wait on nothing outside their own thread block,
+ *     and every internal pipeline wait is bounded (PFD_DEVERR_TIMEOUT).
+ *   - Calls are thread-safe; calls on one stream run in order.
+ */
+#ifndef PFD_H_
+#define PFD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PFD_ABI_VERSION 1
+
+typedef enum {
+  PFD_OK = 0,
+  PFD_ERR_INVALID_ARG = 1,
+  PFD_ERR_UNSUPPORTED = 2,
+  PFD_ERR_CUDA = 3
+} pfd_status;
+
+/* Device-side error bits (OR-ed into *dev_err). */
+#define PFD_DEVERR_TABLE 1   /* chunk-table entry outside [0, pool_rows]      */
+#define PFD_DEVERR_SEL 2     /* selected chunk index outside [0, table_len)   */
+#define PFD_DEVERR_SLOT 4    /* slot_row[j] + B + 1 outside [0, pool_rows]    */
+#define PFD_DEVERR_TIMEOUT 8 /* an internal pipeline wait ran out of budget    */
+#define PFD_DEVERR_SHAPE 16  /* device cu_lq / cu_k disagree with host sizes   */
+
+typedef uint16_t pfd_bf16; /* raw bfloat16 bits */
+
+/* Where one chunk's cached rows live in the pool: rows row .. row+len-1. */
+typedef struct {
+  int32_t row;
+  int32_t len;
+} pfd_chunk_entry;
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st* pfd_stream_t;
+
+/* Supported shapes: head_dim D in {64, 128}; Hq a multiple of Hkv;
+ * W * (Hq / Hkv) <= 512; chunk size 1 <= C <= 8192; 0 <= B <= C. */
+
+/*
+ * Workspace bytes pfd_chunk_prefill needs for these sizes (device memory,
+ * 256-byte aligned, contents need not be initialised).
+ */
+size_t pfd_chunk_prefill_workspace(int N, int C, int W, int Hq, int Hkv, int D, int B);
+
+/*
+ * Chunked prefill of one request: Methodology 1 ("Chunked Prefill and KV
+ * Caching") and the intra-chunk half of Methodology 2 ("Two-Level Sparsity").
+ *
+ * The prefix is N chunks of C tokens; chunk j occupies rows j*(C+1) ..
+ * j*(C+1)+C of q/k/v, its row j*(C+1) being the BOS row put in front of it.
+ * For every chunk and query head h (KV head h / (Hq/Hkv)):
+ *   out   = softmax(sm_scale * Q K^T) V over the chunk's own C+1 rows only
+ *           (bidirectional, no cross-chunk keys);
+ *   scores[j][t] = sum over the W window rows and all Hq heads of the
+ *           window row's softmax probability of chunk row t, the softmax
+ *           taken over the chunk's C+1 keys (the cumulative attention weight
+ *           row t receives from the query tokens);
+ *   kept_idx[j] = the B content tokens (t = 1..C, reported as t-1) with the
+ *           largest fp32 score, ties to the lower index, in ascending order;
+ *   pool rows slot_row[j] .. slot_row[j]+B get the K and V rows of BOS and of
+ *           the kept tokens, in that order (all heads of a row together);
+ *   table[j] = {slot_row[j], B+1}.
+ *
+ * Arguments (device memory unless stated):
+ *   q            [N*(C+1), Hq, D]  bf16
+ *   k, v         [N*(C+1), Hkv, D] bf16
+ *   q_win        [W, Hq, D] bf16 query-window rows (may be NULL when W == 0;
+ *                W == 0 gives all-zero scores and keeps t = 0..B-1)
+ *   sm_scale     softmax scale; <= 0 selects 1/sqrt(D)
+ *   out          [N*(C+1), Hq, D] bf16 (written)
+ *   scores       [N, C+1] fp32 (written; column 0 is BOS)
+ *   kept_idx     [N, B] int32 (written)
+ *   pool_k/v     [pool_rows, Hkv, D] bf16 (rows of the N slots written)
+ *   slot_row     [N] int32, first pool row of each chunk's slot; slots of
+ *                B+1 rows must not overlap (not checked)
+ *   table        [N] pfd_chunk_entry (written)
+ *   dev_err      one int32, or NULL
+ *   workspace    >= pfd_chunk_prefill_workspace(...) bytes
+ */
+pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
+                             const pfd_bf16* q_win, int N, int C, int W, int Hq, int Hkv, int D,
+                             int B, float sm_scale, pfd_bf16* out, float* scores,
+                             int32_t* kept_idx, pfd_bf16* pool_k, pfd_bf16* pool_v,
+                             int64_t pool_rows, const int32_t* slot_row, pfd_chunk_entry* table,
+                             int32_t* dev_err, void* workspace, size_t workspace_bytes,
+                             pfd_stream_t stream);
+
+/*
+ * Chunk selection (Methodology 1, "Selection"; Methodology 2 inter-chunk
+ * sparsity): s = fl32(s_I + s_P) (one fp32 add, round to nearest even), and
+ * sel = the K chunks with the largest s in rank order (s descending, ties to
+ * the lower index, -0.0 == +0.0, NaN below every number).  Both scores are
+ * taken as "higher = more relevant"; a caller holding a raw negative
+ * log-likelihood negates it first.
+ *   s_I, s_P  [N] fp32 device;  sel [K] int32 device (written);
+ *   s_out     [N] fp32 device (written) or NULL.   1 <= K <= N <= 16384.
+ */
+pfd_status pfd_select_chunks(const float* s_I, const float* s_P, int N, int K, int32_t* sel,
+                             float* s_out, pfd_stream_t stream);
+
+/*
+ * Batched form of pfd_select_chunks for several sequences whose chunks are
+ * numbered consecutively in one shared chunk table: sequence b owns table
+ * entries cu_n[b] .. cu_n[b+1]-1 and selects K_b = cu_k[b+1]-cu_k[b] of them.
+ * sel[cu_k[b] + i] receives the table index (cu_n[b] + chunk) of its i-th
+ * best chunk.  cu_n, cu_k: [batch+1] int32 device, non-decreasing.
+ * max_n bounds every sequence's chunk count (<= 16384).
+ */
+pfd_status pfd_select_chunks_batched(const float* s_I, const float* s_P, const int32_t* cu_n,
+                                     const int32_t* cu_k, int batch, int max_n, int32_t* sel,
+                                     float* s_out, pfd_stream_t stream);
+
+/*
+ * Number of KV splits pfd_decode_attention uses for these sizes when
+ * n_splits == 0 (a plan that depends only on the arguments and the device's
+ * SM count).  cu_lq_host, cu_k_host: [batch+1] int32 host memory.
+ */
+int pfd_decode_plan_splits(int batch, const int32_t* cu_lq_host, const int32_t* cu_k_host,
+                           int Hq, int Hkv, int D, int max_chunk_len);
+
+/* Workspace bytes pfd_decode_attention needs (0 when one split is used). */
+size_t pfd_decode_workspace(int batch, const int32_t* cu_lq_host, const int32_t* cu_k_host,
+                            int Hq, int Hkv, int D, int max_chunk_len, int n_splits);
+
+/*
+ * Static-KV decode attention of one denoising step (Methodology 3,
+ * "Decoding with Static KV Reuse"; "Attention Kernel Optimization").
+ *
+ * Sequence b has Lq_b = cu_lq[b+1]-cu_lq[b] live rows (query window +
+ * response) and K_b = cu_k[b+1]-cu_k[b] selected chunks sel[cu_k[b]..].
+ * For each live row and query head h (KV head h / (Hq/Hkv)):
+ *   out = softmax over [ the pool rows table[c].row .. +table[c].len of every
+ *         selected chunk c ; the sequence's Lq_b live rows ] of
+ *         sm_scale * q . k, applied to the matching v rows (no mask);
+ *   lse = natural-log log-sum-exp of the same logits.
+ * The key range is cut into n_splits contiguous splits (0 = automatic); each
+ * split reads its chunks in place through the table (no gather) and keeps a
+ * partial softmax state (max, sum, unnormalised output); the splits are
+ * merged by a log-sum-exp reduction.  The pool is only read.
+ *
+ * Arguments (device memory unless stated):
+ *   q              [total_lq, Hq, D] bf16; k_self, v_self [total_lq, Hkv, D]
+ *   cu_lq          [batch+1] int32; cu_lq_host the same values in host memory
+ *   pool_k/v       [pool_rows, Hkv, D] bf16
+ *   table          [table_len] pfd_chunk_entry (all chunks of all sequences)
+ *   sel            [cu_k[batch]] int32 indices into table
+ *   cu_k, cu_k_host [batch+1] int32 device / host
+ *   max_chunk_len  upper bound of table[].len, used only to plan splits
+ *   out            [total_lq, Hq, D] bf16 (written)
+ *   lse            [total_lq, Hq] fp32 (written) or NULL
+ *   workspace      >= pfd_decode_workspace(...) bytes (may be NULL if 0)
+ */
+pfd_status pfd_decode_attention(const pfd_bf16* q, const pfd_bf16* k_self,
+                                const pfd_bf16* v_self, const int32_t* cu_lq,
+                                const int32_t* cu_lq_host, const pfd_bf16* pool_k,
+                                const pfd_bf16* pool_v, int64_t pool_rows,
+                                const pfd_chunk_entry* table, int32_t table_len,
+                                const int32_t* sel, const int32_t* cu_k, const int32_t* cu_k_host,
+                                int batch, int Hq, int Hkv, int D, int max_chunk_len,
+                                float sm_scale, int n_splits, pfd_bf16* out, float* lse,
+                                int32_t* dev_err, void* workspace, size_t workspace_bytes,
+                                pfd_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* pfd_status_string(pfd_status status);
+
+/* PFD_ABI_VERSION of the loaded library. */
+int pfd_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PFD_H_ */

@@ -1,0 +1,393 @@
+// C ABI of libpfd: argument checks, TMA tensor maps, workspace layout, split
+// planning and kernel launches.  Declarations and contracts: include/pfd.h.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pfd_internal.cuh"
+
+namespace pfd {
+namespace {
+
+constexpr float kLog2e = 1.44269504088896340736f;
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+int device_sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 152;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// 3-D map over a [rows, heads, D] bf16 tensor: box = 16 rows x 1 head x 64
+// columns (128 B), 128-byte swizzle, out-of-range rows read as zero.
+bool make_kv_map(CUtensorMap* map, const void* base, long long rows, int heads, int D) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr || base == nullptr || rows <= 0) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                           static_cast<cuuint64_t>(heads) * D * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kGroupRows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct PrefillWs {
+  size_t win_m, win_l, part_scores, total;
+};
+
+PrefillWs prefill_ws_layout(int N, int C, int W, int Hq, int Hkv) {
+  PrefillWs w;
+  const size_t stats = static_cast<size_t>(N) * Hq * W * sizeof(float);
+  w.win_m = 0;
+  w.win_l = align256(stats);
+  w.part_scores = w.win_l + align256(stats);
+  const size_t ps = W > 0 ? static_cast<size_t>(N) * Hkv * (C + 1) * sizeof(float) : 0;
+  w.total = w.part_scores + align256(ps);
+  return w;
+}
+
+bool shapes_ok(int Hq, int Hkv, int D) {
+  return Hq >= 1 && Hkv >= 1 && Hq % Hkv == 0 && (D == 64 || D == 128);
+}
+
+pfd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PFD_OK : PFD_ERR_CUDA; }
+
+struct DecodeWs {
+  size_t part_m, part_l, part_acc, total;
+};
+
+DecodeWs decode_ws_layout(int n_splits, long long total_lq, int Hq, int D) {
+  DecodeWs w{0, 0, 0, 0};
+  if (n_splits <= 1) return w;
+  const size_t ml = static_cast<size_t>(n_splits) * total_lq * Hq * sizeof(float);
+  w.part_m = 0;
+  w.part_l = align256(ml);
+  w.part_acc = w.part_l + align256(ml);
+  w.total = w.part_acc + align256(ml * D);
+  return w;
+}
+
+bool decode_host_ok(int batch, const int32_t* cu_lq_host, const int32_t* cu_k_host) {
+  if (batch < 1 || cu_lq_host == nullptr || cu_k_host == nullptr) return false;
+  if (cu_lq_host[0] != 0 || cu_k_host[0] != 0) return false;
+  for (int b = 0; b < batch; ++b)
+    if (cu_lq_host[b + 1] < cu_lq_host[b] || cu_k_host[b + 1] < cu_k_host[b]) return false;
+  return cu_lq_host[batch] >= 1;
+}
+
+constexpr int kMaxSplits = 64;
+
+}  // namespace
+}  // namespace pfd
+
+using namespace pfd;
+
+extern "C" {
+
+int pfd_abi_version(void) { return PFD_ABI_VERSION; }
+
+const char* pfd_status_string(pfd_status s) {
+  switch (s) {
+    case PFD_OK: return "PFD_OK";
+    case PFD_ERR_INVALID_ARG: return "PFD_ERR_INVALID_ARG";
+    case PFD_ERR_UNSUPPORTED: return "PFD_ERR_UNSUPPORTED";
+    case PFD_ERR_CUDA: return "PFD_ERR_CUDA";
+  }
+  return "PFD_UNKNOWN_STATUS";
+}
+
+size_t pfd_chunk_prefill_workspace(int N, int C, int W, int Hq, int Hkv, int D, int B) {
+  (void)D;
+  (void)B;
+  if (N < 1 || C < 1 || W < 0 || Hq < 1 || Hkv < 1) return 0;
+  return prefill_ws_layout(N, C, W, Hq, Hkv).total;
+}
+
+pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
+                             const pfd_bf16* q_win, int N, int C, int W, int Hq, int Hkv, int D,
+                             int B, float sm_scale, pfd_bf16* out, float* scores,
+                             int32_t* kept_idx, pfd_bf16* pool_k, pfd_bf16* pool_v,
+                             int64_t pool_rows, const int32_t* slot_row, pfd_chunk_entry* table,
+                             int32_t* dev_err, void* workspace, size_t workspace_bytes,
+                             pfd_stream_t stream) {
+  if (N < 1 || C < 1 || W < 0 || B < 0 || B > C) return PFD_ERR_INVALID_ARG;
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return PFD_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return PFD_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  if (C > 8192 || static_cast<long long>(W) * G > 512) return PFD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(N) * (C + 1) * Hq * D >= (1ll << 40)) return PFD_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !out || !scores || !pool_k || !pool_v || !slot_row || !table)
+    return PFD_ERR_INVALID_ARG;
+  if (B > 0 && !kept_idx) return PFD_ERR_INVALID_ARG;
+  if (W > 0 && !q_win) return PFD_ERR_INVALID_ARG;
+  if (pool_rows < B + 1 || pool_rows >= (1ll << 31)) return PFD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(pool_k) ||
+      !aligned16(pool_v) || (W > 0 && !aligned16(q_win)))
+    return PFD_ERR_INVALID_ARG;
+  const PrefillWs ws = prefill_ws_layout(N, C, W, Hq, Hkv);
+  if (workspace_bytes < ws.total || (ws.total > 0 && workspace == nullptr) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return PFD_ERR_INVALID_ARG;
+  const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  const long long rows = static_cast<long long>(N) * (C + 1);
+
+  AttnParams ap;
+  std::memset(&ap, 0, sizeof(ap));
+  if (!make_kv_map(&ap.tm_k[0], k, rows, Hkv, D) || !make_kv_map(&ap.tm_v[0], v, rows, Hkv, D))
+    return PFD_ERR_CUDA;
+  ap.tm_k[1] = ap.tm_k[0];
+  ap.tm_v[1] = ap.tm_v[0];
+  ap.q = reinterpret_cast<const bf16*>(q);
+  ap.q_win = reinterpret_cast<const bf16*>(q_win);
+  ap.out = reinterpret_cast<bf16*>(out);
+  ap.win_m = reinterpret_cast<float*>(wsb + ws.win_m);
+  ap.win_l = reinterpret_cast<float*>(wsb + ws.win_l);
+  ap.dev_err = dev_err;
+  ap.mode = kModePrefill;
+  ap.Hq = Hq;
+  ap.Hkv = Hkv;
+  ap.G = G;
+  ap.D = D;
+  ap.n_chunks = N;
+  ap.chunk_rows = C + 1;
+  ap.n_win = W;
+  ap.mt_chunk = ceil_div((C + 1) * G, kBlockM);
+  ap.mt_win = W > 0 ? ceil_div(W * G, kBlockM) : 0;
+  ap.n_chunk_items = N * Hkv * ap.mt_chunk;
+  ap.n_splits = 1;
+  ap.scale_log2 = scale * kLog2e;
+  const long long grid = static_cast<long long>(ap.n_chunk_items) + static_cast<long long>(N) * Hkv * ap.mt_win;
+  if (grid >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
+  pfd_status s = from_cuda(launch_attention(ap, static_cast<int>(grid), st));
+  if (s != PFD_OK) return s;
+
+  if (W > 0) {
+    WinScoreParams wp;
+    std::memset(&wp, 0, sizeof(wp));
+    wp.tm_k = ap.tm_k[0];
+    wp.q_win = ap.q_win;
+    wp.win_m = ap.win_m;
+    wp.win_l = ap.win_l;
+    wp.part_scores = reinterpret_cast<float*>(wsb + ws.part_scores);
+    wp.n_chunks = N;
+    wp.chunk_rows = C + 1;
+    wp.n_win = W;
+    wp.Hq = Hq;
+    wp.Hkv = Hkv;
+    wp.G = G;
+    wp.D = D;
+    wp.k_tiles = ceil_div(C + 1, 128);
+    wp.scale_log2 = ap.scale_log2;
+    wp.dev_err = dev_err;
+    s = from_cuda(launch_window_scores(wp, st));
+    if (s != PFD_OK) return s;
+  }
+
+  TopBParams tp;
+  std::memset(&tp, 0, sizeof(tp));
+  tp.part_scores = W > 0 ? reinterpret_cast<const float*>(wsb + ws.part_scores) : nullptr;
+  tp.scores = scores;
+  tp.kept_idx = kept_idx;
+  tp.k = reinterpret_cast<const bf16*>(k);
+  tp.v = reinterpret_cast<const bf16*>(v);
+  tp.pool_k = reinterpret_cast<bf16*>(pool_k);
+  tp.pool_v = reinterpret_cast<bf16*>(pool_v);
+  tp.slot_row = slot_row;
+  tp.table = table;
+  tp.dev_err = dev_err;
+  tp.pool_rows = pool_rows;
+  tp.n_chunks = N;
+  tp.chunk_size = C;
+  tp.n_keep = B;
+  tp.Hkv = Hkv;
+  tp.D = D;
+  const int want = ceil_div(2 * device_sm_count(), N);
+  tp.copy_splits = std::max(1, std::min(want, std::max(1, (B + 1) / 16)));
+  return from_cuda(launch_topb_compact(tp, st));
+}
+
+pfd_status pfd_select_chunks(const float* s_I, const float* s_P, int N, int K, int32_t* sel,
+                             float* s_out, pfd_stream_t stream) {
+  if (!s_I || !s_P || !sel || N < 1 || K < 1 || K > N) return PFD_ERR_INVALID_ARG;
+  if (N > 16384) return PFD_ERR_UNSUPPORTED;
+  return from_cuda(launch_select(s_I, s_P, nullptr, nullptr, N, K, 1, N, sel, s_out,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pfd_status pfd_select_chunks_batched(const float* s_I, const float* s_P, const int32_t* cu_n,
+                                     const int32_t* cu_k, int batch, int max_n, int32_t* sel,
+                                     float* s_out, pfd_stream_t stream) {
+  if (!s_I || !s_P || !sel || !cu_n || !cu_k || batch < 1 || max_n < 1)
+    return PFD_ERR_INVALID_ARG;
+  if (max_n > 16384) return PFD_ERR_UNSUPPORTED;
+  return from_cuda(launch_select(s_I, s_P, cu_n, cu_k, 0, 0, batch, max_n, sel, s_out,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int pfd_decode_plan_splits(int batch, const int32_t* cu_lq_host, const int32_t* cu_k_host,
+                           int Hq, int Hkv, int D, int max_chunk_len) {
+  (void)D;
+  if (!decode_host_ok(batch, cu_lq_host, cu_k_host) || !shapes_ok(Hq, Hkv, 128)) return 1;
+  const int G = Hq / Hkv;
+  long long items = 0, keys_max = 0;
+  for (int b = 0; b < batch; ++b) {
+    const long long lq = cu_lq_host[b + 1] - cu_lq_host[b];
+    const long long kb = cu_k_host[b + 1] - cu_k_host[b];
+    items += Hkv * ((lq * G + kBlockM - 1) / kBlockM);
+    keys_max = std::max(keys_max, kb * std::max(0, max_chunk_len) + lq);
+  }
+  if (items <= 0) return 1;
+  const long long sms = device_sm_count();
+  int best = 1;
+  double best_cost = 1e300;
+  const long long max_s = std::max<long long>(1, std::min<long long>(kMaxSplits, (keys_max + kBlockN - 1) / kBlockN));
+  for (int S = 1; S <= max_s; ++S) {
+    const long long waves = (items * S + sms - 1) / sms;
+    const long long tiles = (keys_max + static_cast<long long>(S) * kBlockN - 1) / (static_cast<long long>(S) * kBlockN);
+    // a CTA's fixed cost (setup, Q load, epilogue) ~ 2 tiles; the merge ~ 1 tile
+    const double cost = static_cast<double>(waves) * (tiles + 2) + (S > 1 ? 1.0 : 0.0);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
+}
+
+size_t pfd_decode_workspace(int batch, const int32_t* cu_lq_host, const int32_t* cu_k_host,
+                            int Hq, int Hkv, int D, int max_chunk_len, int n_splits) {
+  if (!decode_host_ok(batch, cu_lq_host, cu_k_host)) return 0;
+  const int S = n_splits > 0 ? n_splits
+                             : pfd_decode_plan_splits(batch, cu_lq_host, cu_k_host, Hq, Hkv, D,
+                                                      max_chunk_len);
+  return decode_ws_layout(S, cu_lq_host[batch], Hq, D).total;
+}
+
+pfd_status pfd_decode_attention(const pfd_bf16* q, const pfd_bf16* k_self,
+                                const pfd_bf16* v_self, const int32_t* cu_lq,
+                                const int32_t* cu_lq_host, const pfd_bf16* pool_k,
+                                const pfd_bf16* pool_v, int64_t pool_rows,
+                                const pfd_chunk_entry* table, int32_t table_len,
+                                const int32_t* sel, const int32_t* cu_k, const int32_t* cu_k_host,
+                                int batch, int Hq, int Hkv, int D, int max_chunk_len,
+                                float sm_scale, int n_splits, pfd_bf16* out, float* lse,
+                                int32_t* dev_err, void* workspace, size_t workspace_bytes,
+                                pfd_stream_t stream) {
+  if (!decode_host_ok(batch, cu_lq_host, cu_k_host)) return PFD_ERR_INVALID_ARG;
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return PFD_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return PFD_ERR_UNSUPPORTED;
+  if (!q || !k_self || !v_self || !cu_lq || !cu_k || !out) return PFD_ERR_INVALID_ARG;
+  if (n_splits < 0 || n_splits > kMaxSplits) return PFD_ERR_INVALID_ARG;
+  const int total_lq = cu_lq_host[batch];
+  const int total_sel = cu_k_host[batch];
+  if (total_sel > 0 && (!pool_k || !pool_v || !table || !sel || pool_rows < 1 || table_len < 1))
+    return PFD_ERR_INVALID_ARG;
+  if (pool_rows >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_self) || !aligned16(v_self) || !aligned16(out) ||
+      (total_sel > 0 && (!aligned16(pool_k) || !aligned16(pool_v))))
+    return PFD_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  const int S = n_splits > 0 ? n_splits
+                             : pfd_decode_plan_splits(batch, cu_lq_host, cu_k_host, Hq, Hkv, D,
+                                                      max_chunk_len);
+  const DecodeWs ws = decode_ws_layout(S, total_lq, Hq, D);
+  if (workspace_bytes < ws.total || (ws.total > 0 && workspace == nullptr) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return PFD_ERR_INVALID_ARG;
+  const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+
+  AttnParams ap;
+  std::memset(&ap, 0, sizeof(ap));
+  if (!make_kv_map(&ap.tm_k[1], k_self, total_lq, Hkv, D) ||
+      !make_kv_map(&ap.tm_v[1], v_self, total_lq, Hkv, D))
+    return PFD_ERR_CUDA;
+  if (total_sel > 0) {
+    if (!make_kv_map(&ap.tm_k[0], pool_k, pool_rows, Hkv, D) ||
+        !make_kv_map(&ap.tm_v[0], pool_v, pool_rows, Hkv, D))
+      return PFD_ERR_CUDA;
+  } else {
+    ap.tm_k[0] = ap.tm_k[1];
+    ap.tm_v[0] = ap.tm_v[1];
+  }
+  int mt_max = 0;
+  for (int b = 0; b < batch; ++b)
+    mt_max = std::max(mt_max, ceil_div((cu_lq_host[b + 1] - cu_lq_host[b]) * G, kBlockM));
+  ap.q = reinterpret_cast<const bf16*>(q);
+  ap.out = reinterpret_cast<bf16*>(out);
+  ap.lse = lse;
+  ap.part_m = S > 1 ? reinterpret_cast<float*>(wsb + ws.part_m) : nullptr;
+  ap.part_l = S > 1 ? reinterpret_cast<float*>(wsb + ws.part_l) : nullptr;
+  ap.part_acc = S > 1 ? reinterpret_cast<float*>(wsb + ws.part_acc) : nullptr;
+  ap.table = table;
+  ap.sel = sel;
+  ap.cu_k = cu_k;
+  ap.cu_lq = cu_lq;
+  ap.dev_err = dev_err;
+  ap.pool_rows = pool_rows;
+  ap.table_len = table_len;
+  ap.mode = kModeDecode;
+  ap.Hq = Hq;
+  ap.Hkv = Hkv;
+  ap.G = G;
+  ap.D = D;
+  ap.batch = batch;
+  ap.mt_max = mt_max;
+  ap.n_splits = S;
+  ap.total_lq = total_lq;
+  ap.total_sel = total_sel;
+  ap.scale_log2 = scale * kLog2e;
+  const long long grid = static_cast<long long>(batch) * Hkv * S * mt_max;
+  if (grid >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
+  pfd_status s = from_cuda(launch_attention(ap, static_cast<int>(grid), st));
+  if (s != PFD_OK || S == 1) return s;
+  MergeParams mp;
+  mp.part_m = ap.part_m;
+  mp.part_l = ap.part_l;
+  mp.part_acc = ap.part_acc;
+  mp.out = ap.out;
+  mp.lse = lse;
+  mp.n_splits = S;
+  mp.total_lq = total_lq;
+  mp.Hq = Hq;
+  mp.D = D;
+  return from_cuda(launch_lse_merge(mp, st));
+}
+
+}  // extern "C"

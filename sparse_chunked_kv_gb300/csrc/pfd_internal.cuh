@@ -1,0 +1,142 @@
+// Definitions shared by the kernels of libpfd and its C-ABI layer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/pfd.h"
+
+namespace pfd {
+
+using bf16 = __nv_bfloat16;
+
+// ----------------------------------------------------------- attention --
+// One CTA computes one 128-row tile of packed query rows against one
+// contiguous range ("split") of a key sequence.  Query rows of a tile are
+// (token t, head j of the KV group) pairs packed as m = t * G + j, so the G
+// query heads that share KV head g share every K/V tile (GQA packing).
+// The key sequence is a list of segments (row ranges of a K/V tensor); it is
+// consumed in groups of 16 rows, 8 groups per 128-key tile, so segments of
+// any length share tiles and only a segment's last group is ragged.
+constexpr int kBlockM = 128;
+constexpr int kGroupRows = 16;
+constexpr int kGroupsPerTile = 8;
+constexpr int kBlockN = kGroupRows * kGroupsPerTile;
+
+enum AttnMode : int { kModePrefill = 0, kModeDecode = 1 };
+
+struct AttnParams {
+  // Key/value tensors addressed by TMA: index 0 = prefill K/V or the decode
+  // pool, index 1 = the decode live block.  3-D maps over [rows, Hkv, D],
+  // box = 16 rows x 1 head x 64 columns, 128-byte swizzle.
+  CUtensorMap tm_k[2];
+  CUtensorMap tm_v[2];
+
+  const bf16* q;        // prefill: chunk rows; decode: live rows
+  const bf16* q_win;    // prefill: window rows
+  bf16* out;            // [rows, Hq, D]
+  float* lse;           // decode, one split: [total_lq, Hq] (may be null)
+  float* part_m;        // decode, several splits: [S, total_lq, Hq] (log2 units)
+  float* part_l;        // [S, total_lq, Hq]
+  float* part_acc;      // [S, total_lq, Hq, D]
+  float* win_m;         // prefill: [N, Hq, W] running max (log2 units)
+  float* win_l;         // prefill: [N, Hq, W] softmax denominators
+
+  const pfd_chunk_entry* table;
+  const int32_t* sel;
+  const int32_t* cu_k;
+  const int32_t* cu_lq;
+  int32_t* dev_err;
+
+  long long pool_rows;
+  int table_len;
+  int mode;
+  int Hq, Hkv, G, D;
+
+  // prefill
+  int n_chunks, chunk_rows, n_win;
+  int mt_chunk;         // M tiles per (chunk, KV head) of chunk rows
+  int mt_win;           // M tiles per (chunk, KV head) of window rows
+  int n_chunk_items;    // n_chunks * Hkv * mt_chunk
+
+  // decode
+  int batch, mt_max, n_splits, total_lq, total_sel;
+
+  float scale_log2;     // sm_scale * log2(e)
+};
+
+cudaError_t launch_attention(const AttnParams& p, int grid, cudaStream_t stream);
+size_t attention_smem_bytes(int D);
+
+// ------------------------------------------------------- window scores --
+struct WinScoreParams {
+  CUtensorMap tm_k;         // prefill K, same map shape as AttnParams::tm_k
+  const bf16* q_win;        // [W, Hq, D]
+  const float* win_m;       // [N, Hq, W]
+  const float* win_l;       // [N, Hq, W]
+  float* part_scores;       // [N, Hkv, C+1]
+  int n_chunks, chunk_rows, n_win, Hq, Hkv, G, D;
+  int k_tiles;              // ceil((C+1) / 128)
+  float scale_log2;
+  int32_t* dev_err;
+};
+
+cudaError_t launch_window_scores(const WinScoreParams& p, cudaStream_t stream);
+
+// ------------------------------------------------- top-B + compaction --
+struct TopBParams {
+  const float* part_scores;  // [N, Hkv, C+1] or null when W == 0
+  float* scores;             // [N, C+1]
+  int32_t* kept_idx;         // [N, B]
+  const bf16* k;             // [N*(C+1), Hkv, D]
+  const bf16* v;
+  bf16* pool_k;              // [pool_rows, Hkv, D]
+  bf16* pool_v;
+  const int32_t* slot_row;   // [N]
+  pfd_chunk_entry* table;    // [N]
+  int32_t* dev_err;
+  long long pool_rows;
+  int n_chunks, chunk_size, n_keep, Hkv, D;
+  int copy_splits;
+};
+
+cudaError_t launch_topb_compact(const TopBParams& p, cudaStream_t stream);
+
+// ----------------------------------------------------------- selection --
+cudaError_t launch_select(const float* s_i, const float* s_p, const int32_t* cu_n,
+                          const int32_t* cu_k, int n_scalar, int k_scalar, int batch, int max_n,
+                          int32_t* sel, float* s_out, cudaStream_t stream);
+
+// ------------------------------------------------------------ LSE merge --
+struct MergeParams {
+  const float* part_m;
+  const float* part_l;
+  const float* part_acc;
+  bf16* out;
+  float* lse;
+  int n_splits, total_lq, Hq, D;
+};
+
+cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream);
+
+// ------------------------------------------------------------- helpers --
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Maps an fp32 value to an unsigned key whose unsigned order is the rank
+// order: larger value = larger key, -0.0 and +0.0 share a key, NaN gets the
+// smallest key.
+__device__ __forceinline__ uint32_t rank_key(float x) {
+  if (x != x) return 0u;
+  if (x == 0.0f) x = 0.0f;
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ void raise_dev_err(int32_t* dev_err, int bits) {
+  if (dev_err != nullptr) atomicOr(dev_err, bits);
+}
+
+}  // namespace pfd

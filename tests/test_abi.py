@@ -1,0 +1,118 @@
+"""CPU tests of the C ABI: the library builds, loads, exports every symbol the
+header declares, and rejects bad arguments on the host with a status code
+(no kernel runs; these calls return before touching a GPU)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch  # noqa: F401  (loads the CUDA runtime libraries first)
+
+import __graft_entry__ as entry
+from sparse_chunked_kv_gb300 import _abi
+
+HEADER = os.path.join(entry.ROOT, "include", "pfd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_abi.LIB_PATH):
+        entry.build()
+    return _abi.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pfd_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for want in ("pfd_chunk_prefill", "pfd_select_chunks", "pfd_decode_attention"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _abi.LIB_PATH], stdout=subprocess.PIPE,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (pfd_\w+)", out))
+    missing = [n for n in declared_symbols() if n not in exported]
+    assert not missing, missing
+    assert set(_abi.SIGNATURES) == set(declared_symbols())
+
+
+def test_version_and_status_strings(lib):
+    assert _abi.pfd_abi_version() == 1
+    assert _abi.pfd_status_string(0) == "PFD_OK"
+    assert _abi.pfd_status_string(1) == "PFD_ERR_INVALID_ARG"
+    assert _abi.pfd_status_string(2) == "PFD_ERR_UNSUPPORTED"
+
+
+def _prefill_status(lib, **over):
+    a = dict(q=256, k=256, v=256, q_win=256, N=2, C=16, W=4, Hq=4, Hkv=2, D=64, B=4, scale=0.0,
+             out=256, scores=256, kept=256, pk=256, pv=256, pool_rows=10, slot=256, table=256,
+             err=0, ws=256,
+             ws_bytes=1 << 20, stream=0)
+    a.update(over)
+    return lib.pfd_chunk_prefill(a["q"], a["k"], a["v"], a["q_win"], a["N"], a["C"], a["W"], a["Hq"],
+                                 a["Hkv"], a["D"], a["B"], a["scale"], a["out"], a["scores"],
+                                 a["kept"], a["pk"], a["pv"], a["pool_rows"], a["slot"], a["table"],
+                                 a["err"] or None, a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(N=0), 1), (dict(C=0), 1), (dict(B=17), 1), (dict(B=-1), 1), (dict(Hq=5), 1),
+    (dict(D=96), 2), (dict(C=9000), 2), (dict(W=200, Hq=8, Hkv=2), 2), (dict(q=0), 1),
+    (dict(q_win=0), 1), (dict(pool_rows=4), 1), (dict(ws_bytes=0), 1), (dict(q=12), 1),
+    (dict(ws=300), 1),
+])
+def test_prefill_host_checks(lib, over, status):
+    assert _prefill_status(lib, **over) == status
+
+
+def test_prefill_workspace_sizes(lib):
+    small = lib.pfd_chunk_prefill_workspace(2, 16, 4, 4, 2, 64, 4)
+    none = lib.pfd_chunk_prefill_workspace(2, 16, 0, 4, 2, 64, 4)
+    assert small > 0 and small % 256 == 0 and none == 0
+    assert lib.pfd_chunk_prefill_workspace(0, 16, 4, 4, 2, 64, 4) == 0
+
+
+def test_select_host_checks(lib):
+    assert lib.pfd_select_chunks(8, 8, 4, 5, 8, None, None) == 1
+    assert lib.pfd_select_chunks(8, 8, 0, 0, 8, None, None) == 1
+    assert lib.pfd_select_chunks(None, 8, 4, 2, 8, None, None) == 1
+    assert lib.pfd_select_chunks(8, 8, 20000, 2, 8, None, None) == 2
+    assert lib.pfd_select_chunks_batched(8, 8, 8, 8, 0, 4, 8, None, None) == 1
+
+
+def test_decode_host_checks_and_plan(lib):
+    cu_lq = (ctypes.c_int32 * 2)(0, 320)
+    cu_k = (ctypes.c_int32 * 2)(0, 4)
+    bad_lq = (ctypes.c_int32 * 2)(0, 0)
+    args = [256, 256, 256, 256, cu_lq, 256, 256, 100, 256, 16, 256, 256, cu_k, 1, 28, 4, 128, 257,
+            0.0, 1, 256, None, None, None, 0, None]
+    a = list(args)
+    a[0] = 8                      # misaligned q
+    assert lib.pfd_decode_attention(*a) == 1
+    a = list(args)
+    a[19] = 2                     # two splits need a workspace
+    assert lib.pfd_decode_attention(*a) == 1
+    a = list(args)
+    a[4] = bad_lq
+    assert lib.pfd_decode_attention(*a) == 1
+    a = list(args)
+    a[16] = 80
+    assert lib.pfd_decode_attention(*a) == 2
+    a = list(args)
+    a[14] = 27
+    assert lib.pfd_decode_attention(*a) == 1
+    a = list(args)
+    a[19] = 65
+    assert lib.pfd_decode_attention(*a) == 1
+    s = _abi.pfd_decode_plan_splits(1, [0, 320], [0, 4], 28, 4, 128, 257)
+    assert 1 <= s <= 64
+    assert _abi.pfd_decode_workspace(1, [0, 320], [0, 4], 28, 4, 128, 257, 1) == 0
+    ws2 = _abi.pfd_decode_workspace(1, [0, 320], [0, 4], 28, 4, 128, 257, 2)
+    assert ws2 >= 2 * 320 * 28 * (2 + 128) * 4

@@ -1,0 +1,250 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU oracle on
+seeded inputs small enough for the oracle to check every output."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import pfd_oracle as orc
+from sparse_chunked_kv_gb300 import _abi, api
+from sparse_chunked_kv_gb300 import workloads as wl
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+f64 = wl.to_f64
+
+# Small cases spanning several tiles and ragged tails: (name, config).
+PREFILL_CASES = [
+    ("tiny", wl.TINY),
+    ("gqa7_c512", wl.scaled(wl.CTX_8K, n_chunks=3, n_select=2)),
+    ("gqa7_c100_ragged", wl.scaled(wl.CTX_8K, n_chunks=2, chunk_size=100, n_keep=37, n_select=1,
+                                   n_win=7, n_resp=9)),
+    ("d64_c1000", wl.scaled(wl.TINY, n_chunks=2, chunk_size=1000, n_keep=333, n_win=5)),
+    ("keep_all", wl.scaled(wl.TINY, n_chunks=3, chunk_size=48, n_keep=48, n_select=3)),
+    ("keep_none", wl.scaled(wl.TINY, n_chunks=3, chunk_size=48, n_keep=0, n_select=2)),
+    ("no_window", wl.scaled(wl.TINY, n_chunks=2, chunk_size=64, n_keep=10, n_win=0, n_resp=17)),
+    ("one_token_chunks", wl.scaled(wl.TINY, n_chunks=5, chunk_size=1, n_keep=1, n_win=3)),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available()
+    _abi.load()
+
+
+@pytest.mark.parametrize("name,cfg", PREFILL_CASES, ids=[c[0] for c in PREFILL_CASES])
+def test_prefill_parity(name, cfg):
+    req = wl.make_request(cfg, 0)
+    res = P.run_prefill(cfg, req)
+    assert int(res["dev_err"][0]) == 0
+    o_ref = orc.chunk_attention(f64(req["q"]), f64(req["k"]), f64(req["v"]), cfg.n_chunks,
+                                cfg.chunk_size, cfg.sm_scale)
+    P.assert_close_out(res["out"].double().numpy(), o_ref, "prefill out")
+    s_ref = orc.window_scores(f64(req["q_win"]), f64(req["k"]), cfg.n_chunks, cfg.chunk_size,
+                              cfg.sm_scale)
+    s_gpu = res["scores"].double().numpy()
+    tol = P.SCORE_RTOL * np.abs(s_ref) + 1e-6 * max(1, cfg.n_win * cfg.n_q_heads)
+    assert (np.abs(s_gpu - s_ref) <= tol).all(), f"scores: max diff {np.abs(s_gpu - s_ref).max()}"
+    if cfg.n_keep > 0:
+        P.check_kept(res["kept_idx"].numpy(), s_ref, cfg.n_keep)
+    P.check_pool(cfg, req, res)
+
+
+def test_prefill_pool_padding_untouched():
+    cfg = wl.scaled(wl.TINY, n_chunks=4, chunk_size=80, n_keep=20)
+    req = wl.make_request(cfg, 3)
+    res = P.run_prefill(cfg, req, pool_pad=5, pool_fill=float("nan"))
+    stride = cfg.n_keep + 1 + 5
+    for j in range(cfg.n_chunks):
+        base = int(res["slot_row"][j])
+        pad = res["pool_k"][base + cfg.n_keep + 1:base + stride]
+        assert torch.isnan(pad.float()).all()
+    P.check_pool(cfg, req, res)
+
+
+def _select_cases():
+    g = torch.Generator().manual_seed(5)
+    cases = []
+    for n, k in ((8, 2), (16, 4), (32, 8), (512, 64), (128, 32), (1, 1), (300, 300)):
+        cases.append((torch.randn(n, generator=g), torch.randn(n, generator=g), k))
+    ties = torch.round(torch.randn(200, generator=g) * 2) / 2
+    cases.append((ties, torch.zeros(200), 50))
+    cases.append((torch.tensor([0.0, -0.0, 1.0, -0.0, 0.0]), torch.tensor([-0.0, 0.0, -1.0, 0.0, -0.0]), 3))
+    cases.append((torch.tensor([1.0, 0.5, 1.0, 0.75]), torch.tensor([0.0, 0.0, 2.0 ** -25, 0.0]), 4))
+    cases.append((torch.full((64,), 0.5), torch.full((64,), 0.25), 10))
+    return cases
+
+
+@pytest.mark.parametrize("case", range(len(_select_cases())))
+def test_select_bit_exact(case):
+    s_i, s_p, k = _select_cases()[case]
+    sel, s = api.select_chunks(P.cuda(s_i.float()), P.cuda(s_p.float()), k)
+    sel_ref, s_ref = orc.select_chunks(s_i.float().numpy(), s_p.float().numpy(), k)
+    assert sel.cpu().tolist() == sel_ref.tolist()
+    assert np.array_equal(s.cpu().numpy().view(np.uint32) & 0x7FFFFFFF,
+                          s_ref.view(np.uint32) & 0x7FFFFFFF)
+
+
+def test_select_batched_bit_exact():
+    g = torch.Generator().manual_seed(9)
+    ns, ks = [128, 32, 8, 128, 5], [32, 8, 2, 1, 5]
+    s_i, s_p = torch.randn(sum(ns), generator=g), torch.randn(sum(ns), generator=g)
+    cu_n = torch.tensor([0] + list(np.cumsum(ns)), dtype=torch.int32)
+    cu_k = torch.tensor([0] + list(np.cumsum(ks)), dtype=torch.int32)
+    sel, _ = api.select_chunks_batched(P.cuda(s_i), P.cuda(s_p), P.cuda(cu_n), P.cuda(cu_k), max(ns))
+    want = []
+    for b in range(len(ns)):
+        lo = int(cu_n[b])
+        r, _ = orc.select_chunks(s_i[lo:lo + ns[b]].numpy(), s_p[lo:lo + ns[b]].numpy(), ks[b])
+        want += [lo + int(x) for x in r]
+    assert sel.cpu().tolist() == want
+
+
+def _decode_inputs(cfg, seq=0, step=0, pad=0, fill=0.0):
+    """Oracle-built pool for cfg (the GPU decode is checked on the oracle's pool)."""
+    req = wl.make_request(cfg, seq)
+    scores = orc.window_scores(f64(req["q_win"]), f64(req["k"]), cfg.n_chunks, cfg.chunk_size,
+                               cfg.sm_scale)
+    kept = orc.top_b(scores, cfg.n_keep)
+    stride = cfg.n_keep + 1 + pad
+    slot = (req["slot_row"] // cfg.slot_stride) * stride
+    pool_rows = cfg.n_chunks * stride
+    pk, pv, table = P.oracle_pool(cfg, req, kept, slot, pool_rows, fill)
+    sel, _ = orc.select_chunks(req["s_i"].numpy(), req["s_p"].numpy(), cfg.n_select)
+    ql, kl, vl = wl.live_block(req, wl.make_step(cfg, seq, step))
+    return req, pk, pv, table, sel, ql, kl, vl
+
+
+@pytest.mark.parametrize("n_splits", [0, 1, 2, 3, 5])
+@pytest.mark.parametrize("cfg_name", ["tiny", "gqa7"])
+def test_decode_parity(cfg_name, n_splits):
+    cfg = wl.TINY if cfg_name == "tiny" else wl.scaled(wl.CTX_8K, n_chunks=6, n_select=3, n_resp=100)
+    _, pk, pv, table, sel, ql, kl, vl = _decode_inputs(cfg)
+    o_ref, lse_ref = orc.decode_attention(f64(ql), f64(kl), f64(vl), pk, pv, table, sel, cfg.sm_scale)
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = api.decode_attention(P.cuda(ql), P.cuda(kl), P.cuda(vl), P.cuda(P.bf16_of(pk)),
+                                    P.cuda(P.bf16_of(pv)), P.cuda(torch.from_numpy(table)),
+                                    P.cuda(torch.from_numpy(sel)), n_splits=n_splits, dev_err=dev_err)
+    torch.cuda.synchronize()
+    assert int(dev_err.item()) == 0
+    P.assert_close_out(out.cpu().double().numpy(), o_ref, "decode out")
+    assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= P.LSE_MAX_ABS
+
+
+def test_decode_nan_padding_is_masked():
+    cfg = wl.scaled(wl.TINY, n_keep=57, n_select=3)     # 58-row slots: ragged 16-row groups
+    _, pk, pv, table, sel, ql, kl, vl = _decode_inputs(cfg, pad=7, fill=float("nan"))
+    o_ref, lse_ref = orc.decode_attention(f64(ql), f64(kl), f64(vl), pk, pv, table, sel, cfg.sm_scale)
+    for n_splits in (1, 4):
+        out, lse = api.decode_attention(P.cuda(ql), P.cuda(kl), P.cuda(vl), P.cuda(P.bf16_of(pk)),
+                                        P.cuda(P.bf16_of(pv)), P.cuda(torch.from_numpy(table)),
+                                        P.cuda(torch.from_numpy(sel)), n_splits=n_splits)
+        P.assert_close_out(out.cpu().double().numpy(), o_ref, "decode out (NaN padding)")
+        assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= P.LSE_MAX_ABS
+
+
+def test_decode_batched_shared_pool():
+    """Three sequences with different chunk sizes and live lengths in one pool."""
+    cfgs = [wl.scaled(wl.TINY, chunk_size=c, n_keep=b, n_select=k, n_resp=r, n_chunks=n)
+            for c, b, k, r, n in ((64, 16, 3, 40, 6), (256, 64, 2, 17, 4), (32, 8, 4, 100, 8))]
+    pool_k, pool_v, tables, sels, qs, ks, vs, refs = [], [], [], [], [], [], [], []
+    row_base, table_base = 0, 0
+    for i, cfg in enumerate(cfgs):
+        _, pk, pv, table, sel, ql, kl, vl = _decode_inputs(cfg, seq=i)
+        o_ref, lse_ref = orc.decode_attention(f64(ql), f64(kl), f64(vl), pk, pv, table, sel,
+                                              cfg.sm_scale)
+        refs.append((o_ref, lse_ref))
+        pool_k.append(pk)
+        pool_v.append(pv)
+        t = table.copy()
+        t[:, 0] += row_base
+        tables.append(t)
+        sels.append(sel + table_base)
+        row_base += pk.shape[0]
+        table_base += table.shape[0]
+        qs.append(ql)
+        ks.append(kl)
+        vs.append(vl)
+    cu_lq = [0] + list(np.cumsum([q.shape[0] for q in qs]))
+    cu_k = [0] + list(np.cumsum([len(s) for s in sels]))
+    for n_splits in (0, 1, 3):
+        out, lse = api.decode_attention(
+            P.cuda(torch.cat(qs)), P.cuda(torch.cat(ks)), P.cuda(torch.cat(vs)),
+            P.cuda(P.bf16_of(np.concatenate(pool_k))), P.cuda(P.bf16_of(np.concatenate(pool_v))),
+            P.cuda(torch.from_numpy(np.concatenate(tables))),
+            P.cuda(torch.from_numpy(np.concatenate(sels).astype(np.int32))), cu_lq=cu_lq, cu_k=cu_k,
+            n_splits=n_splits)
+        out, lse = out.cpu().double().numpy(), lse.cpu().double().numpy()
+        for b, (o_ref, lse_ref) in enumerate(refs):
+            P.assert_close_out(out[cu_lq[b]:cu_lq[b + 1]], o_ref, f"batched decode seq {b}")
+            assert np.abs(lse[cu_lq[b]:cu_lq[b + 1]] - lse_ref).max() <= P.LSE_MAX_ABS
+
+
+def test_decode_bad_entries_raise_device_error():
+    cfg = wl.TINY
+    _, pk, pv, table, sel, ql, kl, vl = _decode_inputs(cfg)
+    bad_table = table.copy()
+    bad_table[sel[0], 0] = pk.shape[0] + 100          # slot beyond the pool
+    bad_sel = sel.copy()
+    bad_sel[-1] = 1000                                 # index beyond the table
+    for tab, s, bit in ((bad_table, sel, _abi.DEVERR_TABLE), (table, bad_sel, _abi.DEVERR_SEL)):
+        dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out, _ = api.decode_attention(P.cuda(ql), P.cuda(kl), P.cuda(vl), P.cuda(P.bf16_of(pk)),
+                                      P.cuda(P.bf16_of(pv)), P.cuda(torch.from_numpy(tab)),
+                                      P.cuda(torch.from_numpy(s)), dev_err=dev_err)
+        torch.cuda.synchronize()
+        assert int(dev_err.item()) & bit
+        assert torch.isfinite(out.float()).all()
+
+
+def test_prefill_bad_slot_raises_device_error():
+    cfg = wl.scaled(wl.TINY, n_chunks=3, chunk_size=32, n_keep=8)
+    req = wl.make_request(cfg, 0)
+    slot = torch.tensor([0, 9, 1000], dtype=torch.int32)
+    res = api.chunk_prefill(P.cuda(req["q"]), P.cuda(req["k"]), P.cuda(req["v"]),
+                            P.cuda(req["q_win"]), cfg.n_chunks, cfg.chunk_size, cfg.n_keep,
+                            P.cuda(slot), 27)
+    torch.cuda.synchronize()
+    assert int(res["dev_err"].item()) & _abi.DEVERR_SLOT
+    assert res["table"][2].tolist() == [0, 0]
+    assert res["table"][1].tolist() == [9, 9]
+
+
+def test_static_pool_unchanged_by_decode_steps():
+    cfg = wl.TINY
+    req = wl.make_request(cfg, 0)
+    res = P.run_prefill(cfg, req)
+    pk0, pv0 = res["pool_k_dev"].clone(), res["pool_v_dev"].clone()
+    sel, _ = api.select_chunks(P.cuda(req["s_i"]), P.cuda(req["s_p"]), cfg.n_select)
+    for t in range(cfg.n_steps):
+        ql, kl, vl = wl.live_block(req, wl.make_step(cfg, 0, t))
+        api.decode_attention(P.cuda(ql), P.cuda(kl), P.cuda(vl), res["pool_k_dev"],
+                             res["pool_v_dev"], res["table_dev"], sel, n_splits=2)
+    torch.cuda.synchronize()
+    assert torch.equal(pk0.view(torch.int16), res["pool_k_dev"].view(torch.int16))
+    assert torch.equal(pv0.view(torch.int16), res["pool_v_dev"].view(torch.int16))
+
+
+def test_end_to_end_tiny_every_step():
+    """Prefill -> select -> T decode steps on the GPU pool, each step vs the
+    oracle on the oracle's own pool (the kept sets must agree first)."""
+    cfg = wl.TINY
+    req = wl.make_request(cfg, 0)
+    res = P.run_prefill(cfg, req)
+    s_ref = orc.window_scores(f64(req["q_win"]), f64(req["k"]), cfg.n_chunks, cfg.chunk_size,
+                              cfg.sm_scale)
+    ref_kept, n_diff = P.check_kept(res["kept_idx"].numpy(), s_ref, cfg.n_keep)
+    assert n_diff == 0, "tie-band swaps on the tiny workload"
+    pk, pv, table = P.oracle_pool(cfg, req, ref_kept, res["slot_row"], res["pool_rows"])
+    sel, _ = api.select_chunks(P.cuda(req["s_i"]), P.cuda(req["s_p"]), cfg.n_select)
+    sel_ref, _ = orc.select_chunks(req["s_i"].numpy(), req["s_p"].numpy(), cfg.n_select)
+    assert sel.cpu().tolist() == sel_ref.tolist()
+    for t in range(cfg.n_steps):
+        ql, kl, vl = wl.live_block(req, wl.make_step(cfg, 0, t))
+        out, lse = api.decode_attention(P.cuda(ql), P.cuda(kl), P.cuda(vl), res["pool_k_dev"],
+                                        res["pool_v_dev"], res["table_dev"], sel)
+        o_ref, lse_ref = orc.decode_attention(f64(ql), f64(kl), f64(vl), pk, pv, table, sel_ref,
+                                              cfg.sm_scale)
+        P.assert_close_out(out.cpu().double().numpy(), o_ref, f"decode step {t}")
+        assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= P.LSE_MAX_ABS
