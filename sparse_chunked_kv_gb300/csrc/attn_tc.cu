@@ -592,13 +592,11 @@ cudaError_t launch_attention(const AttnParams& p, int grid, cudaStream_t stream)
   const size_t smem = attention_smem_bytes(p.D);
   cudaError_t err;
   if (p.D == 64) {
-    err = cudaFuncSetAttribute(attention_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
+    err = ensure_smem_limit(reinterpret_cast<const void*>(attention_kernel<64>), static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     attention_kernel<64><<<grid, kThreads, smem, stream>>>(p);
   } else {
-    err = cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
+    err = ensure_smem_limit(reinterpret_cast<const void*>(attention_kernel<128>), static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     attention_kernel<128><<<grid, kThreads, smem, stream>>>(p);
   }

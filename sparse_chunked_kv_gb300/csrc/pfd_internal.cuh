@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
+#include <vector>
 
 #include "../../include/pfd.h"
 
@@ -123,6 +125,23 @@ struct MergeParams {
 cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream);
 
 // ------------------------------------------------------------- helpers --
+// Raises a kernel's dynamic shared-memory limit once per (kernel, device), so
+// that later calls -- including calls made while a stream is being captured
+// into a CUDA graph -- only launch.
+inline cudaError_t ensure_smem_limit(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::vector<std::pair<std::pair<const void*, int>, int>> done;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& e : done)
+    if (e.first.first == func && e.first.second == dev && e.second >= bytes) return cudaSuccess;
+  err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess) done.push_back({{func, dev}, bytes});
+  return err;
+}
+
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Maps an fp32 value to an unsigned key whose unsigned order is the rank

@@ -231,9 +231,7 @@ select_kernel(const float* __restrict__ s_i, const float* __restrict__ s_p,
 cudaError_t launch_topb_compact(const TopBParams& p, cudaStream_t stream) {
   const int rows = p.chunk_size + 1;
   const size_t smem = static_cast<size_t>((rows * 4 + 15) & ~15) + static_cast<size_t>(p.n_keep + 1) * 4;
-  cudaError_t err = cudaFuncSetAttribute(topb_compact_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(topb_compact_kernel), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   dim3 grid(p.n_chunks, p.copy_splits);
   topb_compact_kernel<<<grid, kTopBThreads, smem, stream>>>(p);
@@ -244,8 +242,7 @@ cudaError_t launch_select(const float* s_i, const float* s_p, const int32_t* cu_
                           const int32_t* cu_k, int n_scalar, int k_scalar, int batch, int max_n,
                           int32_t* sel, float* s_out, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(max_n) * 4;
-  cudaError_t err = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   select_kernel<<<batch, kSelectThreads, smem, stream>>>(s_i, s_p, cu_n, cu_k, n_scalar, k_scalar,
                                                          max_n, sel, s_out);

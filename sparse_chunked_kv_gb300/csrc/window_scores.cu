@@ -174,13 +174,11 @@ cudaError_t launch_window_scores(const WinScoreParams& p, cudaStream_t stream) {
   const size_t smem = 1024 + static_cast<size_t>(128 + nwp) * p.D * 2;
   cudaError_t err;
   if (p.D == 64) {
-    err = cudaFuncSetAttribute(window_score_kernel<64>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    err = ensure_smem_limit(reinterpret_cast<const void*>(window_score_kernel<64>), static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     window_score_kernel<64><<<grid, kThreads, smem, stream>>>(p);
   } else {
-    err = cudaFuncSetAttribute(window_score_kernel<128>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    err = ensure_smem_limit(reinterpret_cast<const void*>(window_score_kernel<128>), static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     window_score_kernel<128><<<grid, kThreads, smem, stream>>>(p);
   }
