@@ -69,8 +69,9 @@ typedef struct {
 /* cudaStream_t without pulling in the CUDA headers. */
 typedef struct CUstream_st* pfd_stream_t;
 
-/* Supported shapes: head_dim D in {64, 128}; Hq a multiple of Hkv;
- * W * (Hq / Hkv) <= 512; chunk size 1 <= C <= 8192; 0 <= B <= C. */
+/* Supported shapes: head_dim D in {64, 128}; Hq a multiple of Hkv with
+ * Hq / Hkv <= 128; window W <= 256 and W * (Hq / Hkv) <= 512; chunk size
+ * 1 <= C <= 8192; 0 <= B <= C; at most 511 selected chunks per sequence. */
 
 /*
  * Workspace bytes pfd_chunk_prefill needs for these sizes (device memory,

@@ -1,5 +1,5 @@
-// Bidirectional softmax attention of 128-row query tiles over a list of key
-// segments, on tcgen05 tensor cores with TMA-fed K/V tiles.
+// Bidirectional softmax attention of packed query tiles over a list of key
+// segments, on tcgen05 tensor cores with TMA-fed Q/K/V tiles.
 //
 // One kernel serves three kinds of work item:
 //   chunk   (prefill)  rows of chunk j attend to chunk j's own C+1 rows
@@ -7,22 +7,32 @@
 //                      chunk is processed on its own, bidirectionally);
 //   window  (prefill)  query-window rows against chunk j, statistics only
 //                      (row max and softmax denominator), consumed by the
-//                      window-score kernel ("Two-Level Sparsity", ranking by
-//                      cumulative attention weight from the query tokens);
+//                      window-score kernel ("Two-Level Sparsity": ranking by
+//                      the cumulative attention weight from the query tokens);
 //   decode             live rows of one sequence against one contiguous range
 //                      of [selected chunks' pool slots ; live rows], read in
 //                      place through the chunk table ("Decoding with Static KV
-//                      Reuse"; split-KV with log-sum-exp merge from "Attention
-//                      Kernel Optimization").
+//                      Reuse"; split-KV with a log-sum-exp merge from
+//                      "Attention Kernel Optimization").
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: walks the key segments in 16-row groups and
-//               loads K (and V) tiles of 8 groups into a 2-stage ring.
-//   warp 1      allocates TMEM and issues all tcgen05.mma from one thread:
-//               S = Q K^T into one of two TMEM S buffers, O += P V into TMEM.
-//   warps 2..5  one thread per query row (= TMEM lane): masked row max, exp2,
-//               bf16 P into shared memory, rescale of O in TMEM only when the
-//               running max grows by more than 2^8, and the epilogue.
+// A query tile packs Tq = floor(128 / G) tokens x the G query heads of one KV
+// head (row m = t * G + j), so one 3-D TMA box loads it and every K/V tile is
+// shared by the whole GQA group.  The key sequence is consumed in 16-row
+// groups, 8 per 128-key tile; a tile lying inside one segment is loaded with
+// one 128-row box per 64-column panel, other tiles group by group.
+//
+// Per SM two CTAs are resident (96 KB shared memory, 256 TMEM columns each),
+// so one CTA's softmax overlaps the other's MMAs and TMA latency.  Inside a
+// CTA (192 threads):
+//   warp 0      TMA producer (Q once; K and V per tile, single-buffered, the
+//               next K loads while the current tile's softmax runs);
+//   warp 1      TMEM owner and single-thread MMA issuer:
+//               S = Q K^T into TMEM columns [0, 128),
+//               O += P V with P read from TMEM columns [0, 64) (bf16 pairs
+//               written over S) and V from shared memory;
+//   warps 2..5  one thread per tile row (TMEM lane): masked row max, exp2,
+//               P into TMEM, O rescale in TMEM only when the running max grows
+//               by more than 2^8, epilogue.
 #include "pfd_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -31,11 +41,11 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
-constexpr float kRescaleThreshold = 8.0f;   // log2 units
-constexpr uint32_t kPanelBytes = 128u * 128u;  // 128 rows x 128 B
-constexpr uint32_t kTmemCols = 512;
-__device__ __forceinline__ uint32_t tmem_s(int st) { return st ? 128u : 0u; }
-constexpr uint32_t kTmemO = 256u;
+constexpr float kRescaleThreshold = 8.0f;        // log2 units
+constexpr uint32_t kPanelBytes = 128u * 128u;    // 128 rows x 128 B
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemS = 0;                   // S fp32 [0,128), P bf16x2 [0,64)
+constexpr uint32_t kTmemO = 128;
 constexpr float kLn2 = 0.69314718055994530942f;
 
 enum ItemKind : int { kChunk = 0, kWindow = 1, kDecode = 2 };
@@ -48,73 +58,24 @@ struct TileMeta {
 };
 
 struct Shared {
-  uint64_t qfull;
-  uint64_t kfull[2], vfull[2], kvempty[2];
-  uint64_t sfull[2], sempty[2];
-  uint64_t pfull[2], pvdone[2];
-  uint64_t drain;
+  uint64_t qfull, kfull, vfull, kempty, vempty, sfull, pfull, ofinal, drain;
+  uint64_t mfull[2];
   TileMeta meta[2];
   uint32_t tmem_base;
-  int32_t g_lo, g_hi, n_tiles;
+  int32_t g_lo, g_hi, n_tiles, n_seg;
   int32_t failed;
 };
 
 struct Item {
   int kind;
   int g, mt;
-  const bf16* qsrc;
-  long long q_row0;   // token row of t = 0 in qsrc (and in the output)
+  int q_map;          // 0 = main q tensor, 1 = q_win
+  long long q_row0;   // token row of t = 0 in the q tensor (and in the output)
   int n_t;            // tokens in this item's query block
   int chunk;          // prefill
-  int seq, split;     // decode
+  int split;          // decode
   int k0, k1;         // decode: selected-chunk range in sel
 };
-
-struct Segment {
-  int tensor;
-  long long row;
-  int len;
-};
-
-// Segment i of an item's key sequence.
-__device__ __forceinline__ Segment get_segment(const AttnParams& p, const Item& it, int i) {
-  Segment s;
-  if (it.kind != kDecode) {
-    s.tensor = 0;
-    s.row = static_cast<long long>(it.chunk) * p.chunk_rows;
-    s.len = p.chunk_rows;
-    return s;
-  }
-  const int n_sel = it.k1 - it.k0;
-  if (i < n_sel) {
-    const int c = p.sel[it.k0 + i];
-    s.tensor = 0;
-    s.row = 0;
-    s.len = 0;
-    if (c < 0 || c >= p.table_len) {
-      raise_dev_err(p.dev_err, PFD_DEVERR_SEL);
-      return s;
-    }
-    const pfd_chunk_entry e = p.table[c];
-    if (e.row < 0 || e.len < 0 || static_cast<long long>(e.row) + e.len > p.pool_rows) {
-      raise_dev_err(p.dev_err, PFD_DEVERR_TABLE);
-      return s;
-    }
-    s.row = e.row;
-    s.len = e.len;
-    return s;
-  }
-  s.tensor = 1;
-  s.row = it.q_row0;
-  s.len = it.n_t;
-  return s;
-}
-
-__device__ __forceinline__ int num_segments(const Item& it) {
-  return it.kind == kDecode ? (it.k1 - it.k0 + 1) : 1;
-}
-
-__device__ __forceinline__ int groups_of(int len) { return (len + kGroupRows - 1) / kGroupRows; }
 
 // Resolves blockIdx.x into a work item; returns false when the CTA has no work.
 __device__ __forceinline__ bool resolve_item(const AttnParams& p, Item& it) {
@@ -124,23 +85,22 @@ __device__ __forceinline__ bool resolve_item(const AttnParams& p, Item& it) {
       it.kind = kChunk;
       it.mt = bid % p.mt_chunk;
       bid /= p.mt_chunk;
-      it.qsrc = p.q;
+      it.q_map = 0;
       it.n_t = p.chunk_rows;
     } else {
       bid -= p.n_chunk_items;
       it.kind = kWindow;
       it.mt = bid % p.mt_win;
       bid /= p.mt_win;
-      it.qsrc = p.q_win;
+      it.q_map = 1;
       it.n_t = p.n_win;
     }
     it.g = bid % p.Hkv;
     it.chunk = bid / p.Hkv;
     it.q_row0 = it.kind == kChunk ? static_cast<long long>(it.chunk) * p.chunk_rows : 0;
-    it.seq = 0;
     it.split = 0;
     it.k0 = it.k1 = 0;
-    return it.mt * kBlockM < it.n_t * p.G;
+    return it.mt * p.Tq < it.n_t;
   }
   it.kind = kDecode;
   it.mt = bid % p.mt_max;
@@ -148,12 +108,13 @@ __device__ __forceinline__ bool resolve_item(const AttnParams& p, Item& it) {
   it.split = bid % p.n_splits;
   bid /= p.n_splits;
   it.g = bid % p.Hkv;
-  it.seq = bid / p.Hkv;
-  it.qsrc = p.q;
+  const int seq = bid / p.Hkv;
+  it.q_map = 0;
   it.chunk = 0;
-  const int lq0 = p.cu_lq[it.seq], lq1 = p.cu_lq[it.seq + 1];
-  const int k0 = p.cu_k[it.seq], k1 = p.cu_k[it.seq + 1];
-  if (lq0 < 0 || lq1 < lq0 || lq1 > p.total_lq || k0 < 0 || k1 < k0 || k1 > p.total_sel) {
+  const int lq0 = p.cu_lq[seq], lq1 = p.cu_lq[seq + 1];
+  const int k0 = p.cu_k[seq], k1 = p.cu_k[seq + 1];
+  if (lq0 < 0 || lq1 < lq0 || lq1 > p.total_lq || k0 < 0 || k1 < k0 || k1 > p.total_sel ||
+      k1 - k0 >= kMaxSegments) {
     if (threadIdx.x == 0) raise_dev_err(p.dev_err, PFD_DEVERR_SHAPE);
     return false;
   }
@@ -161,26 +122,81 @@ __device__ __forceinline__ bool resolve_item(const AttnParams& p, Item& it) {
   it.n_t = lq1 - lq0;
   it.k0 = k0;
   it.k1 = k1;
-  return it.mt * kBlockM < it.n_t * p.G;
+  return it.mt * p.Tq < it.n_t;
 }
 
 template <int D>
 struct Layout {
-  static constexpr uint32_t kQBytes = kBlockM * D * 2;
-  static constexpr uint32_t kKVBytes = kBlockN * D * 2;
-  static constexpr uint32_t kPBytes = kBlockM * kBlockN * 2;
+  static constexpr uint32_t kTileBytes = 128u * D * 2u;   // Q, K or V tile
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK0 = kQ + kQBytes;
-  static constexpr uint32_t kV0 = kK0 + kKVBytes;
-  static constexpr uint32_t kK1 = kV0 + kKVBytes;
-  static constexpr uint32_t kV1 = kK1 + kKVBytes;
-  static constexpr uint32_t kP0 = kV1 + kKVBytes;
-  static constexpr uint32_t kP1 = kP0 + kPBytes;
-  static constexpr uint32_t kTotal = kP1 + kPBytes;
+  static constexpr uint32_t kK = kQ + kTileBytes;
+  static constexpr uint32_t kV = kK + kTileBytes;
+  static constexpr uint32_t kSegRow = kV + kTileBytes;              // int32 [kMaxSegments]
+  static constexpr uint32_t kSegLen = kSegRow + 4u * kMaxSegments;  // int32
+  static constexpr uint32_t kSegG0 = kSegLen + 4u * kMaxSegments;   // int32 [+1], first group
+  static constexpr uint32_t kTotal = kSegG0 + 4u * (kMaxSegments + 1);
 };
 
+__device__ __forceinline__ int groups_of(int len) { return (len + kGroupRows - 1) / kGroupRows; }
+
+// Fills the segment list of the item (row, length, first global group) in
+// shared memory; run by one full warp.  Decode: the selected chunks' slots
+// through the table, then the live block (the last segment, tensor 1).
+__device__ __forceinline__ int load_segments(const AttnParams& p, const Item& it, int32_t* seg_row,
+                                             int32_t* seg_len, int32_t* seg_g0, int lane) {
+  int nseg;
+  if (it.kind != kDecode) {
+    nseg = 1;
+    if (lane == 0) {
+      seg_row[0] = it.chunk * p.chunk_rows;
+      seg_len[0] = p.chunk_rows;
+    }
+  } else {
+    const int nsel = it.k1 - it.k0;
+    nseg = nsel + 1;
+    for (int i = lane; i < nsel; i += 32) {
+      const int c = p.sel[it.k0 + i];
+      int row = 0, len = 0;
+      if (c < 0 || c >= p.table_len) {
+        raise_dev_err(p.dev_err, PFD_DEVERR_SEL);
+      } else {
+        const pfd_chunk_entry e = p.table[c];
+        if (e.row < 0 || e.len < 0 || static_cast<long long>(e.row) + e.len > p.pool_rows) {
+          raise_dev_err(p.dev_err, PFD_DEVERR_TABLE);
+        } else {
+          row = e.row;
+          len = e.len;
+        }
+      }
+      seg_row[i] = row;
+      seg_len[i] = len;
+    }
+    if (lane == 0) {
+      seg_row[nsel] = static_cast<int32_t>(it.q_row0);
+      seg_len[nsel] = it.n_t;
+    }
+  }
+  __syncwarp();
+  int carry = 0;
+  for (int base = 0; base < nseg; base += 32) {
+    const int i = base + lane;
+    const int n = i < nseg ? groups_of(seg_len[i]) : 0;
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (i < nseg) seg_g0[i] = carry + incl - n;
+    carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+  }
+  if (lane == 0) seg_g0[nseg] = carry;
+  __syncwarp();
+  return nseg;
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 attention_kernel(const __grid_constant__ AttnParams p) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -191,40 +207,55 @@ attention_kernel(const __grid_constant__ AttnParams p) {
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  int32_t* seg_row = reinterpret_cast<int32_t*>(smem + L::kSegRow);
+  int32_t* seg_len = reinterpret_cast<int32_t*>(smem + L::kSegLen);
+  int32_t* seg_g0 = reinterpret_cast<int32_t*>(smem + L::kSegG0);
   const uint32_t s_base = smem_u32(smem);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const bool with_pv = it.kind != kWindow;
+  const int G = p.G;
+  const int q_rows = G * p.Tq;                 // rows of the tile filled by the Q box
 
-  if (tid == 0) {
-    mbar_init(&sh.qfull, kSoftmaxThreads);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sh.kfull[i], 1);
-      mbar_init(&sh.vfull[i], 1);
-      mbar_init(&sh.kvempty[i], 1);
-      mbar_init(&sh.sfull[i], 1);
-      mbar_init(&sh.sempty[i], kSoftmaxThreads);
-      mbar_init(&sh.pfull[i], kSoftmaxThreads);
-      mbar_init(&sh.pvdone[i], 1);
+  // ----------------------------------------------------------- prologue --
+  if (warp == 0) {
+    const int nseg = load_segments(p, it, seg_row, seg_len, seg_g0, lane);
+    if (lane == 0) {
+      mbar_init(&sh.qfull, 1);
+      mbar_init(&sh.kfull, 1);
+      mbar_init(&sh.vfull, 1);
+      mbar_init(&sh.kempty, 1);
+      mbar_init(&sh.vempty, 1);
+      mbar_init(&sh.sfull, 1);
+      mbar_init(&sh.pfull, kSoftmaxThreads);
+      mbar_init(&sh.ofinal, 1);
+      mbar_init(&sh.drain, 1);
+      mbar_init(&sh.mfull[0], 1);
+      mbar_init(&sh.mfull[1], 1);
+      fence_barrier_init();
+      const long long total = seg_g0[nseg];
+      const int n_splits = it.kind == kDecode ? p.n_splits : 1;
+      const long long lo = total * it.split / n_splits;
+      const long long hi = total * (it.split + 1) / n_splits;
+      sh.g_lo = static_cast<int>(lo);
+      sh.g_hi = static_cast<int>(hi);
+      sh.n_tiles = static_cast<int>((hi - lo + kGroupsPerTile - 1) / kGroupsPerTile);
+      sh.n_seg = nseg;
+      sh.failed = 0;
     }
-    mbar_init(&sh.drain, 1);
-    fence_barrier_init();
-    // Group range of this item's split.
-    const int nseg = num_segments(it);
-    long long total = 0;
-    for (int i = 0; i < nseg; ++i) total += groups_of(get_segment(p, it, i).len);
-    const int n_splits = it.kind == kDecode ? p.n_splits : 1;
-    const long long lo = total * it.split / n_splits;
-    const long long hi = total * (it.split + 1) / n_splits;
-    sh.g_lo = static_cast<int>(lo);
-    sh.g_hi = static_cast<int>(hi);
-    sh.n_tiles = static_cast<int>((hi - lo + kGroupsPerTile - 1) / kGroupsPerTile);
-    sh.failed = 0;
-  }
-  if (warp == 1) {
+  } else if (warp == 1) {
     tmem_alloc(&sh.tmem_base, kTmemCols);
     tmem_relinquish();
+  } else if (q_rows < kBlockM) {
+    // Tile rows past the Q box are never loaded: keep them zero.
+    const int ts = tid - 64;
+    for (int idx = ts; idx < (kBlockM - q_rows) * (D / 8); idx += kSoftmaxThreads) {
+      const int r = q_rows + idx / (D / 8), c = idx % (D / 8);
+      *reinterpret_cast<uint4*>(smem + L::kQ + sw128_offset(r, c * 8, kBlockM)) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -237,211 +268,190 @@ attention_kernel(const __grid_constant__ AttnParams p) {
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0 && n_tiles > 0) {
-      tma_prefetch_desc(&p.tm_k[0]);
-      const int nseg = num_segments(it);
-      int seg = 0, gofs = 0;
-      {
-        long long acc = 0;
-        for (; seg < nseg; ++seg) {
-          const int n = groups_of(get_segment(p, it, seg).len);
-          if (acc + n > g_lo) {
-            gofs = static_cast<int>(g_lo - acc);
-            break;
-          }
-          acc += n;
-        }
-      }
-      Segment cur = get_segment(p, it, seg < nseg ? seg : 0);
+      const int nseg = sh.n_seg;
+      const int qm = it.q_map;
+      mbar_arrive_expect_tx(&sh.qfull, static_cast<uint32_t>(q_rows) * D * 2);
+      for (int pn = 0; pn < D / 64; ++pn)
+        tma_load_3d(smem + L::kQ + pn * kPanelBytes, &p.tm_q[qm], &sh.qfull, pn * 64, it.g * G,
+                    static_cast<int>(it.q_row0) + it.mt * p.Tq);
+      int seg = 0;
+      while (seg + 1 < nseg && seg_g0[seg + 1] <= g_lo) ++seg;
+      int gofs = g_lo - seg_g0[seg];
       int g_cur = g_lo;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !mbar_wait(&sh.kvempty[st], ((j >> 1) - 1) & 1)) {
-          atomicOr(&sh.failed, 1);
-          break;
-        }
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        // Group list of tile j.
         int tens[kGroupsPerTile];
         int rows[kGroupsPerTile];
         uint32_t nv_lo = 0, nv_hi = 0;
         int ng = 0;
+        const bool one_box = (g_hi - g_cur >= kGroupsPerTile) &&
+                             ((gofs + kGroupsPerTile) * kGroupRows <= seg_len[seg]);
         for (; ng < kGroupsPerTile && g_cur < g_hi; ++ng, ++g_cur) {
-          const int nv = min(kGroupRows, cur.len - gofs * kGroupRows);
-          tens[ng] = cur.tensor;
-          rows[ng] = static_cast<int>(cur.row) + gofs * kGroupRows;
+          const int len = seg_len[seg];
+          const int nv = min(kGroupRows, len - gofs * kGroupRows);
+          tens[ng] = (it.kind == kDecode && seg == nseg - 1) ? 1 : 0;
+          rows[ng] = seg_row[seg] + gofs * kGroupRows;
           if (ng < 4) nv_lo |= static_cast<uint32_t>(nv) << (8 * ng);
           else nv_hi |= static_cast<uint32_t>(nv) << (8 * (ng - 4));
           ++gofs;
-          if (gofs * kGroupRows >= cur.len) {
+          if (gofs * kGroupRows >= len) {
             gofs = 0;
             ++seg;
-            while (seg < nseg) {
-              cur = get_segment(p, it, seg);
-              if (cur.len > 0) break;
-              ++seg;
-            }
+            while (seg < nseg && seg_len[seg] == 0) ++seg;
           }
         }
-        sh.meta[st].nvalid_lo = nv_lo;
-        sh.meta[st].nvalid_hi = nv_hi;
-        sh.meta[st].ngroups = ng;
-        const uint32_t bytes = static_cast<uint32_t>(ng) * kGroupRows * D * 2;
-        const uint32_t k_dst = s_base + (st ? L::kK1 : L::kK0);
-        const uint32_t v_dst = s_base + (st ? L::kV1 : L::kV0);
-        mbar_arrive_expect_tx(&sh.kfull[st], bytes);
-        for (int k = 0; k < ng; ++k)
+        // K(j) replaces K(j-1): wait for QK(j-1).  The metadata slot j & 1 was
+        // last read by the softmax of tile j-2, which ended before QK(j-1).
+        if (j >= 1 && !mbar_wait(&sh.kempty, (j - 1) & 1)) { ok = false; break; }
+        TileMeta& m = sh.meta[j & 1];
+        m.nvalid_lo = nv_lo;
+        m.nvalid_hi = nv_hi;
+        m.ngroups = ng;
+        mbar_arrive(&sh.mfull[j & 1]);
+        const uint32_t bytes = one_box ? static_cast<uint32_t>(kBlockN) * D * 2
+                                       : static_cast<uint32_t>(ng) * kGroupRows * D * 2;
+        mbar_arrive_expect_tx(&sh.kfull, bytes);
+        if (one_box) {
           for (int pn = 0; pn < D / 64; ++pn)
-            tma_load_3d(smem + (k_dst - s_base) + pn * kPanelBytes + k * 2048, &p.tm_k[tens[k]],
-                        &sh.kfull[st], pn * 64, it.g, rows[k]);
-        if (with_pv) {
-          mbar_arrive_expect_tx(&sh.vfull[st], bytes);
+            tma_load_3d(smem + L::kK + pn * kPanelBytes, &p.tm_k128[tens[0]], &sh.kfull, pn * 64,
+                        it.g, rows[0]);
+        } else {
           for (int k = 0; k < ng; ++k)
             for (int pn = 0; pn < D / 64; ++pn)
-              tma_load_3d(smem + (v_dst - s_base) + pn * kPanelBytes + k * 2048,
-                          &p.tm_v[tens[k]], &sh.vfull[st], pn * 64, it.g, rows[k]);
+              tma_load_3d(smem + L::kK + pn * kPanelBytes + k * 2048, &p.tm_k16[tens[k]],
+                          &sh.kfull, pn * 64, it.g, rows[k]);
+        }
+        if (with_pv) {
+          // V(j) replaces V(j-1): wait for PV(j-1).
+          if (j >= 1 && !mbar_wait(&sh.vempty, (j - 1) & 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sh.vfull, bytes);
+          if (one_box) {
+            for (int pn = 0; pn < D / 64; ++pn)
+              tma_load_3d(smem + L::kV + pn * kPanelBytes, &p.tm_v128[tens[0]], &sh.vfull,
+                          pn * 64, it.g, rows[0]);
+          } else {
+            for (int k = 0; k < ng; ++k)
+              for (int pn = 0; pn < D / 64; ++pn)
+                tma_load_3d(smem + L::kV + pn * kPanelBytes + k * 2048, &p.tm_v16[tens[k]],
+                            &sh.vfull, pn * 64, it.g, rows[k]);
+          }
         }
       }
-      // Drain: the last tiles' loads must have landed before the CTA exits.
-      for (int j = max(0, n_tiles - 2); j < n_tiles; ++j) {
-        mbar_wait(&sh.kfull[j & 1], (j >> 1) & 1);
-        if (with_pv) mbar_wait(&sh.vfull[j & 1], (j >> 1) & 1);
-      }
+      if (!ok) atomicOr(&sh.failed, 1);
+      // The last tile's loads must have landed before the CTA exits.
+      const int jl = n_tiles - 1;
+      mbar_wait(&sh.kfull, jl & 1);
+      if (with_pv) mbar_wait(&sh.vfull, jl & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0 && n_tiles > 0) {
       bool ok = mbar_wait(&sh.qfull, 0);
-      tc_fence_after_sync();
       const uint32_t q_addr = s_base + L::kQ;
-      auto issue_pv = [&](int i) -> bool {
-        const int b = i & 1;
-        if (!mbar_wait(&sh.pfull[b], (i >> 1) & 1)) return false;
-        if (with_pv) {
-          if (!mbar_wait(&sh.vfull[b], (i >> 1) & 1)) return false;
-          tc_fence_after_sync();
-          const int ng = min(sh.meta[b].ngroups, kGroupsPerTile);
-          const uint32_t p_addr = s_base + (b ? L::kP1 : L::kP0);
-          const uint32_t v_addr = s_base + (b ? L::kV1 : L::kV0);
-          constexpr uint32_t idesc = idesc_bf16(kBlockM, D, false, true);
-          for (int kk = 0; kk < ng; ++kk) {
-            const uint64_t a = sw128_desc(p_addr + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t v = sw128_desc(v_addr + kk * 2048, kPanelBytes, 1024);
-            mma_bf16_ss(tmem + kTmemO, a, v, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+      const uint32_t k_addr = s_base + L::kK;
+      const uint32_t v_addr = s_base + L::kV;
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const uint32_t ph = j & 1;
+        if (!mbar_wait(&sh.kfull, ph)) { ok = false; break; }
+        tc_fence_after_sync();
+        const int ng = min(sh.meta[j & 1].ngroups, kGroupsPerTile);
+        const uint32_t idesc_s = idesc_bf16(kBlockM, max(ng, 1) * kGroupRows, false, false);
+        if (ng > 0) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = sw128_desc(q_addr + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
+            const uint64_t b = sw128_desc(k_addr + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
+            mma_bf16_ss(tmem + kTmemS, a, b, idesc_s, kk > 0 ? 1u : 0u);
           }
         }
-        mma_commit(&sh.pvdone[b]);
-        mma_commit(&sh.kvempty[b]);
-        return true;
-      };
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(&sh.kfull[st], (j >> 1) & 1)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(&sh.sempty[st], ((j >> 1) - 1) & 1)) { ok = false; break; }
-        tc_fence_after_sync();
-        const int ng = min(sh.meta[st].ngroups, kGroupsPerTile);
-        const uint32_t idesc = idesc_bf16(kBlockM, max(ng, 1) * kGroupRows, false, false);
-        const uint32_t k_addr = s_base + (st ? L::kK1 : L::kK0);
-#pragma unroll
-        for (int kk = 0; kk < (ng > 0 ? D / 16 : 0); ++kk) {
-          const uint64_t a = sw128_desc(q_addr + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = sw128_desc(k_addr + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
-          mma_bf16_ss(tmem + tmem_s(st), a, b, idesc, kk > 0 ? 1u : 0u);
+        mma_commit(&sh.sfull);
+        mma_commit(&sh.kempty);
+        if (!mbar_wait(&sh.pfull, ph)) { ok = false; break; }
+        if (with_pv) {
+          if (!mbar_wait(&sh.vfull, ph)) { ok = false; break; }
+          tc_fence_after_sync();
+          constexpr uint32_t idesc_o = idesc_bf16(kBlockM, D, false, true);
+          for (int kk = 0; kk < ng; ++kk) {
+            const uint64_t v = sw128_desc(v_addr + kk * 2048, kPanelBytes, 1024);
+            mma_bf16_ts(tmem + kTmemO, tmem + kTmemS + kk * 8, v, idesc_o,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          }
         }
-        mma_commit(&sh.sfull[st]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        mma_commit(&sh.vempty);
       }
-      if (ok) ok = issue_pv(n_tiles - 1);
       if (!ok) atomicOr(&sh.failed, 2);
+      mma_commit(&sh.ofinal);
       // Every MMA issued above has completed once `drain` flips.
       mma_commit(&sh.drain);
       mbar_wait(&sh.drain, 0);
     }
   } else {
     // ---------------------------------------------- softmax + epilogue --
-    const int ts = tid - 64;              // 0..127
     const int quarter = warp & 3;         // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;  // tile row of this thread
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int n_rows = it.n_t * p.G;
-
-    if (n_tiles > 0) {
-      // Q tile -> shared memory, 128-byte swizzled K-major panels.
-      constexpr int kChunks = D / 8;
-      for (int idx = ts; idx < kBlockM * kChunks; idx += kSoftmaxThreads) {
-        const int r = idx / kChunks, c = idx % kChunks;
-        const int m = it.mt * kBlockM + r;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (m < n_rows) {
-          const int t = m / p.G, jj = m - t * p.G;
-          const bf16* src = it.qsrc + ((it.q_row0 + t) * p.Hq + it.g * p.G + jj) * D + c * 8;
-          val = __ldg(reinterpret_cast<const uint4*>(src));
-        }
-        *reinterpret_cast<uint4*>(smem + L::kQ + sw128_offset(r, c * 8, kBlockM)) = val;
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&sh.qfull);
-    }
+    const float scale = p.scale_log2;
 
     float m_used = -INFINITY;
     float l_sum = 0.0f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!mbar_wait_warp(&sh.sfull[st], ph) || !mbar_wait_warp(&sh.kfull[st], ph)) { ok = false; break; }
+      const uint32_t ph = j & 1;
+      if (!mbar_wait_warp(&sh.mfull[j & 1], (j >> 1) & 1) || !mbar_wait_warp(&sh.sfull, ph)) {
+        ok = false;
+        break;
+      }
       tc_fence_after_sync();
-      const TileMeta meta = sh.meta[st];
+      const TileMeta meta = sh.meta[j & 1];
       const int ncol = meta.ngroups * kGroupRows;
       const bool full = meta.ngroups == kGroupsPerTile && meta.nvalid_lo == 0x10101010u &&
                         meta.nvalid_hi == 0x10101010u;
-
-      uint32_t s0[32], s1[32], s2[32], s3[32];
-      const uint32_t s_addr = lane_base + tmem_s(st);
-      tmem_ld32(s_addr + 0, s0);
-      if (ncol > 32) tmem_ld32(s_addr + 32, s1);
-      if (ncol > 64) tmem_ld32(s_addr + 64, s2);
-      if (ncol > 96) tmem_ld32(s_addr + 96, s3);
-      tmem_ld_wait(s0);
-      reg_fence(s1);
-      reg_fence(s2);
-      reg_fence(s3);
-      tc_fence_before_sync();
-      mbar_arrive(&sh.sempty[st]);
-
-      // Masked logits: a column is valid when its row exists in its group.
       auto nv_of = [&](int grp) -> int {
         const uint32_t w = grp < 4 ? meta.nvalid_lo : meta.nvalid_hi;
         return static_cast<int>((w >> (8 * (grp & 3))) & 0xFFu);
       };
-      float x[128];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        x[i] = __uint_as_float(s0[i]);
-        x[32 + i] = __uint_as_float(s1[i]);
-        x[64 + i] = __uint_as_float(s2[i]);
-        x[96 + i] = __uint_as_float(s3[i]);
-      }
-      if (!full) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if ((c & 15) >= nv_of(c >> 4)) x[c] = -INFINITY;
-      }
-      float tmax = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 128; ++c) tmax = fmaxf(tmax, x[c]);
-      const float m_tile = tmax * p.scale_log2;
 
-      // P buffer st was read by PV(j-2).
-      if (j >= 2 && !mbar_wait_warp(&sh.pvdone[st], ((j >> 1) - 1) & 1)) { ok = false; break; }
-      // Rescale decision per row; the TMEM rescale itself is warp-collective,
-      // so a warp rescales when any of its rows needs it (alpha = 1 elsewhere).
+      // Pass 1: row max of the valid logits.
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        if (ch * 32 < ncol) {
+          uint32_t s[32];
+          tmem_ld32(lane_base + kTmemS + ch * 32, s);
+          tmem_ld_wait(s);
+          if (full) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              mx0 = fmaxf(mx0, __uint_as_float(s[i]));
+              mx1 = fmaxf(mx1, __uint_as_float(s[i + 1]));
+              mx2 = fmaxf(mx2, __uint_as_float(s[i + 2]));
+              mx3 = fmaxf(mx3, __uint_as_float(s[i + 3]));
+            }
+          } else {
+            const int nva = nv_of(2 * ch), nvb = nv_of(2 * ch + 1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const bool valid = (i & 15) < (i < 16 ? nva : nvb);
+              const float x = valid ? __uint_as_float(s[i]) : -INFINITY;
+              if ((i & 3) == 0) mx0 = fmaxf(mx0, x);
+              else if ((i & 3) == 1) mx1 = fmaxf(mx1, x);
+              else if ((i & 3) == 2) mx2 = fmaxf(mx2, x);
+              else mx3 = fmaxf(mx3, x);
+            }
+          }
+        }
+      }
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale;
+
+      // Rescale decision per row; the TMEM rescale of O is warp-collective,
+      // so a warp rescales when any of its rows needs it (alpha = 1 for the
+      // others).  sfull(j) also covers PV(j-1): O is complete here.
       const bool mine = m_tile > m_used + kRescaleThreshold;
       if (__any_sync(0xFFFFFFFFu, mine)) {
         const float m_new = mine ? m_tile : m_used;
         const float alpha = mine ? ex2_approx(m_used - m_new) : 1.0f;
         if (j >= 1 && with_pv) {
-          // O holds tiles 0..j-1 relative to the old max: rescale it in TMEM
-          // once PV(j-1) has landed.
-          if (!mbar_wait_warp(&sh.pvdone[(j - 1) & 1], ((j - 1) >> 1) & 1)) { ok = false; break; }
-          tc_fence_after_sync();
 #pragma unroll 1
           for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t o[32];
@@ -451,42 +461,59 @@ attention_kernel(const __grid_constant__ AttnParams p) {
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
             tmem_st32(lane_base + kTmemO + ch * 32, o);
           }
-          tmem_st_wait();
         }
         l_sum *= alpha;
         m_used = m_new;
       }
 
-      // Probabilities (relative to m_used) -> bf16 P tile, row sum in fp32.
+      // Pass 2: probabilities relative to m_used -> bf16 pairs in TMEM
+      // columns [0, 64) (over S columns already read), fp32 row sum.
       const float neg_m = -m_used;
-      float part = 0.0f;
-      uint8_t* p_tile = smem + (st ? L::kP1 : L::kP0);
+      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t packed[16];
+      for (int half = 0; half < 2; ++half) {
+        if (half * 64 < ncol) {
+          uint32_t packed[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a = ex2_approx(fmaf(x[ch * 32 + 2 * i], p.scale_log2, neg_m));
-          const float b = ex2_approx(fmaf(x[ch * 32 + 2 * i + 1], p.scale_log2, neg_m));
-          part += a + b;
-          packed[i] = pack_bf16x2(a, b);
-        }
-        if (with_pv && ch * 32 < ncol) {
+          for (int sub = 0; sub < 2; ++sub) {
+            const int ch = half * 2 + sub;
+            uint32_t s[32];
+            tmem_ld32(lane_base + kTmemS + ch * 32, s);
+            tmem_ld_wait(s);
+            if (full) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const uint32_t off = sw128_offset(row, ch * 32 + q4 * 8, kBlockM);
-            *reinterpret_cast<uint4*>(p_tile + off) =
-                make_uint4(packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2], packed[4 * q4 + 3]);
+              for (int i = 0; i < 16; ++i) {
+                const float a = ex2_approx(fmaf(__uint_as_float(s[2 * i]), scale, neg_m));
+                const float b = ex2_approx(fmaf(__uint_as_float(s[2 * i + 1]), scale, neg_m));
+                if (i & 1) { sum2 += a; sum3 += b; } else { sum0 += a; sum1 += b; }
+                packed[sub * 16 + i] = pack_bf16x2(a, b);
+              }
+            } else {
+              const int nva = nv_of(2 * ch), nvb = nv_of(2 * ch + 1);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int c0 = 2 * i, c1 = 2 * i + 1;
+                const bool v0 = (c0 & 15) < (c0 < 16 ? nva : nvb);
+                const bool v1 = (c1 & 15) < (c1 < 16 ? nva : nvb);
+                const float a = v0 ? ex2_approx(fmaf(__uint_as_float(s[c0]), scale, neg_m)) : 0.0f;
+                const float b = v1 ? ex2_approx(fmaf(__uint_as_float(s[c1]), scale, neg_m)) : 0.0f;
+                if (i & 1) { sum2 += a; sum3 += b; } else { sum0 += a; sum1 += b; }
+                packed[sub * 16 + i] = pack_bf16x2(a, b);
+              }
+            }
           }
+          if (with_pv) tmem_st32(lane_base + kTmemS + half * 32, packed);
         }
       }
-      l_sum += part;
+      l_sum += (sum0 + sum1) + (sum2 + sum3);
+      if (with_pv) tmem_st_wait();
 
       if (with_pv && !full) {
         // Rows of a ragged group that lie past its segment may hold anything
         // (another slot, padding): zero them in V so that 0 * v stays 0.
-        if (!mbar_wait_warp(&sh.vfull[st], ph)) { ok = false; break; }
-        uint8_t* v_tile = smem + (st ? L::kV1 : L::kV0);
+        if (!mbar_wait_warp(&sh.vfull, ph)) { ok = false; break; }
+        const int ts = tid - 64;
+        uint8_t* v_tile = smem + L::kV;
         for (int grp = 0; grp < meta.ngroups; ++grp) {
           const int nv = nv_of(grp);
           const int n_bad = (kGroupRows - nv) * (D / 64) * 8;  // 16-byte chunks to clear
@@ -499,24 +526,22 @@ attention_kernel(const __grid_constant__ AttnParams p) {
                                       c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       tc_fence_before_sync();
-      mbar_arrive(&sh.pfull[st]);
+      mbar_arrive(&sh.pfull);
     }
 
     // ------------------------------------------------------------ epilogue --
-    if (ok && n_tiles > 0 &&
-        !mbar_wait_warp(&sh.pvdone[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1))
-      ok = false;
+    if (ok && n_tiles > 0 && !mbar_wait_warp(&sh.ofinal, 0)) ok = false;
     tc_fence_after_sync();
     if (!ok) atomicOr(&sh.failed, 4);
 
-    const int m = it.mt * kBlockM + row;
-    const bool row_ok = m < n_rows;
-    const int t = row_ok ? m / p.G : 0;
-    const int jj = m - t * p.G;
-    const int head = it.g * p.G + jj;
+    const int t_local = row / G;
+    const int jj = row - t_local * G;
+    const int t = it.mt * p.Tq + t_local;
+    const bool row_ok = row < q_rows && t < it.n_t;
+    const int head = it.g * G + jj;
     if (it.kind == kWindow) {
       if (row_ok) {
         const long long idx = (static_cast<long long>(it.chunk) * p.Hq + head) * p.n_win + t;

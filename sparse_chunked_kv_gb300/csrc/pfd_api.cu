@@ -42,22 +42,31 @@ int device_sm_count() {
   return n;
 }
 
-// 3-D map over a [rows, heads, D] bf16 tensor: box = 16 rows x 1 head x 64
-// columns (128 B), 128-byte swizzle, out-of-range rows read as zero.
-bool make_kv_map(CUtensorMap* map, const void* base, long long rows, int heads, int D) {
+// 3-D map over a [rows, heads, D] bf16 tensor with a box of box_rows rows x
+// box_heads heads x 64 columns (128 B), 128-byte swizzle; out-of-range rows
+// read as zero.
+bool make_map(CUtensorMap* map, const void* base, long long rows, int heads, int D, int box_heads,
+              int box_rows) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr || base == nullptr || rows <= 0) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads),
                         static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                            static_cast<cuuint64_t>(heads) * D * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kGroupRows)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// K or V maps of one tensor: one-group (16-row) and one-tile (128-row) boxes.
+bool make_kv_maps(CUtensorMap* m16, CUtensorMap* m128, const void* base, long long rows, int heads,
+                  int D) {
+  return make_map(m16, base, rows, heads, D, 1, kGroupRows) &&
+         make_map(m128, base, rows, heads, D, 1, kBlockN);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -147,7 +156,8 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
   if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return PFD_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return PFD_ERR_UNSUPPORTED;
   const int G = Hq / Hkv;
-  if (C > 8192 || static_cast<long long>(W) * G > 512) return PFD_ERR_UNSUPPORTED;
+  if (C > 8192 || G > kBlockM || W > 256 || static_cast<long long>(W) * G > 512)
+    return PFD_ERR_UNSUPPORTED;
   if (static_cast<long long>(N) * (C + 1) * Hq * D >= (1ll << 40)) return PFD_ERR_UNSUPPORTED;
   if (!q || !k || !v || !out || !scores || !pool_k || !pool_v || !slot_row || !table)
     return PFD_ERR_INVALID_ARG;
@@ -166,12 +176,23 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
   const long long rows = static_cast<long long>(N) * (C + 1);
 
+  const int Tq = kBlockM / G;
   AttnParams ap;
   std::memset(&ap, 0, sizeof(ap));
-  if (!make_kv_map(&ap.tm_k[0], k, rows, Hkv, D) || !make_kv_map(&ap.tm_v[0], v, rows, Hkv, D))
+  if (!make_kv_maps(&ap.tm_k16[0], &ap.tm_k128[0], k, rows, Hkv, D) ||
+      !make_kv_maps(&ap.tm_v16[0], &ap.tm_v128[0], v, rows, Hkv, D) ||
+      !make_map(&ap.tm_q[0], q, rows, Hq, D, G, Tq))
     return PFD_ERR_CUDA;
-  ap.tm_k[1] = ap.tm_k[0];
-  ap.tm_v[1] = ap.tm_v[0];
+  ap.tm_k16[1] = ap.tm_k16[0];
+  ap.tm_v16[1] = ap.tm_v16[0];
+  ap.tm_k128[1] = ap.tm_k128[0];
+  ap.tm_v128[1] = ap.tm_v128[0];
+  if (W > 0) {
+    if (!make_map(&ap.tm_q[1], q_win, W, Hq, D, G, Tq)) return PFD_ERR_CUDA;
+  } else {
+    ap.tm_q[1] = ap.tm_q[0];
+  }
+  ap.Tq = Tq;
   ap.q = reinterpret_cast<const bf16*>(q);
   ap.q_win = reinterpret_cast<const bf16*>(q_win);
   ap.out = reinterpret_cast<bf16*>(out);
@@ -186,8 +207,8 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
   ap.n_chunks = N;
   ap.chunk_rows = C + 1;
   ap.n_win = W;
-  ap.mt_chunk = ceil_div((C + 1) * G, kBlockM);
-  ap.mt_win = W > 0 ? ceil_div(W * G, kBlockM) : 0;
+  ap.mt_chunk = ceil_div(C + 1, Tq);
+  ap.mt_win = W > 0 ? ceil_div(W, Tq) : 0;
   ap.n_chunk_items = N * Hkv * ap.mt_chunk;
   ap.n_splits = 1;
   ap.scale_log2 = scale * kLog2e;
@@ -199,7 +220,8 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
   if (W > 0) {
     WinScoreParams wp;
     std::memset(&wp, 0, sizeof(wp));
-    wp.tm_k = ap.tm_k[0];
+    wp.tm_k = ap.tm_k128[0];
+    if (!make_map(&wp.tm_qwin, q_win, W, Hq, D, G, W)) return PFD_ERR_CUDA;
     wp.q_win = ap.q_win;
     wp.win_m = ap.win_m;
     wp.win_l = ap.win_l;
@@ -264,15 +286,17 @@ int pfd_decode_plan_splits(int batch, const int32_t* cu_lq_host, const int32_t* 
   (void)D;
   if (!decode_host_ok(batch, cu_lq_host, cu_k_host) || !shapes_ok(Hq, Hkv, 128)) return 1;
   const int G = Hq / Hkv;
+  if (G > kBlockM) return 1;
+  const int Tq = kBlockM / G;
   long long items = 0, keys_max = 0;
   for (int b = 0; b < batch; ++b) {
     const long long lq = cu_lq_host[b + 1] - cu_lq_host[b];
     const long long kb = cu_k_host[b + 1] - cu_k_host[b];
-    items += Hkv * ((lq * G + kBlockM - 1) / kBlockM);
+    items += Hkv * ((lq + Tq - 1) / Tq);
     keys_max = std::max(keys_max, kb * std::max(0, max_chunk_len) + lq);
   }
   if (items <= 0) return 1;
-  const long long sms = device_sm_count();
+  const long long sms = 2LL * device_sm_count();   // two CTAs resident per SM
   int best = 1;
   double best_cost = 1e300;
   const long long max_s = std::max<long long>(1, std::min<long long>(kMaxSplits, (keys_max + kBlockN - 1) / kBlockN));
@@ -313,6 +337,9 @@ pfd_status pfd_decode_attention(const pfd_bf16* q, const pfd_bf16* k_self,
   if (D != 64 && D != 128) return PFD_ERR_UNSUPPORTED;
   if (!q || !k_self || !v_self || !cu_lq || !cu_k || !out) return PFD_ERR_INVALID_ARG;
   if (n_splits < 0 || n_splits > kMaxSplits) return PFD_ERR_INVALID_ARG;
+  if (Hq / Hkv > kBlockM) return PFD_ERR_UNSUPPORTED;
+  for (int b = 0; b < batch; ++b)
+    if (cu_k_host[b + 1] - cu_k_host[b] >= kMaxSegments) return PFD_ERR_UNSUPPORTED;
   const int total_lq = cu_lq_host[batch];
   const int total_sel = cu_k_host[batch];
   if (total_sel > 0 && (!pool_k || !pool_v || !table || !sel || pool_rows < 1 || table_len < 1))
@@ -333,22 +360,28 @@ pfd_status pfd_decode_attention(const pfd_bf16* q, const pfd_bf16* k_self,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
 
+  const int Tq = kBlockM / G;
   AttnParams ap;
   std::memset(&ap, 0, sizeof(ap));
-  if (!make_kv_map(&ap.tm_k[1], k_self, total_lq, Hkv, D) ||
-      !make_kv_map(&ap.tm_v[1], v_self, total_lq, Hkv, D))
+  if (!make_kv_maps(&ap.tm_k16[1], &ap.tm_k128[1], k_self, total_lq, Hkv, D) ||
+      !make_kv_maps(&ap.tm_v16[1], &ap.tm_v128[1], v_self, total_lq, Hkv, D) ||
+      !make_map(&ap.tm_q[0], q, total_lq, Hq, D, G, Tq))
     return PFD_ERR_CUDA;
+  ap.tm_q[1] = ap.tm_q[0];
   if (total_sel > 0) {
-    if (!make_kv_map(&ap.tm_k[0], pool_k, pool_rows, Hkv, D) ||
-        !make_kv_map(&ap.tm_v[0], pool_v, pool_rows, Hkv, D))
+    if (!make_kv_maps(&ap.tm_k16[0], &ap.tm_k128[0], pool_k, pool_rows, Hkv, D) ||
+        !make_kv_maps(&ap.tm_v16[0], &ap.tm_v128[0], pool_v, pool_rows, Hkv, D))
       return PFD_ERR_CUDA;
   } else {
-    ap.tm_k[0] = ap.tm_k[1];
-    ap.tm_v[0] = ap.tm_v[1];
+    ap.tm_k16[0] = ap.tm_k16[1];
+    ap.tm_v16[0] = ap.tm_v16[1];
+    ap.tm_k128[0] = ap.tm_k128[1];
+    ap.tm_v128[0] = ap.tm_v128[1];
   }
+  ap.Tq = Tq;
   int mt_max = 0;
   for (int b = 0; b < batch; ++b)
-    mt_max = std::max(mt_max, ceil_div((cu_lq_host[b + 1] - cu_lq_host[b]) * G, kBlockM));
+    mt_max = std::max(mt_max, ceil_div(cu_lq_host[b + 1] - cu_lq_host[b], Tq));
   ap.q = reinterpret_cast<const bf16*>(q);
   ap.out = reinterpret_cast<bf16*>(out);
   ap.lse = lse;

@@ -27,15 +27,22 @@ constexpr int kBlockM = 128;
 constexpr int kGroupRows = 16;
 constexpr int kGroupsPerTile = 8;
 constexpr int kBlockN = kGroupRows * kGroupsPerTile;
+constexpr int kMaxSegments = 512;   // selected chunks per sequence + the live block
 
 enum AttnMode : int { kModePrefill = 0, kModeDecode = 1 };
 
 struct AttnParams {
-  // Key/value tensors addressed by TMA: index 0 = prefill K/V or the decode
-  // pool, index 1 = the decode live block.  3-D maps over [rows, Hkv, D],
-  // box = 16 rows x 1 head x 64 columns, 128-byte swizzle.
-  CUtensorMap tm_k[2];
-  CUtensorMap tm_v[2];
+  // Query tensors addressed by TMA: index 0 = prefill chunk rows or decode
+  // live rows, index 1 = prefill window rows.  3-D maps over [tokens, Hq, D],
+  // box = Tq tokens x G heads x 64 columns, 128-byte swizzle.
+  CUtensorMap tm_q[2];
+  // Key/value tensors: index 0 = prefill K/V or the decode pool, index 1 =
+  // the decode live block.  3-D maps over [rows, Hkv, D], 128-byte swizzle,
+  // box = 16 rows (one group) or 128 rows (one tile) x 1 head x 64 columns.
+  CUtensorMap tm_k16[2];
+  CUtensorMap tm_v16[2];
+  CUtensorMap tm_k128[2];
+  CUtensorMap tm_v128[2];
 
   const bf16* q;        // prefill: chunk rows; decode: live rows
   const bf16* q_win;    // prefill: window rows
@@ -57,11 +64,12 @@ struct AttnParams {
   int table_len;
   int mode;
   int Hq, Hkv, G, D;
+  int Tq;               // tokens per query tile: floor(128 / G)
 
   // prefill
   int n_chunks, chunk_rows, n_win;
-  int mt_chunk;         // M tiles per (chunk, KV head) of chunk rows
-  int mt_win;           // M tiles per (chunk, KV head) of window rows
+  int mt_chunk;         // query tiles per (chunk, KV head) of chunk rows
+  int mt_win;           // query tiles per (chunk, KV head) of window rows
   int n_chunk_items;    // n_chunks * Hkv * mt_chunk
 
   // decode
@@ -75,7 +83,8 @@ size_t attention_smem_bytes(int D);
 
 // ------------------------------------------------------- window scores --
 struct WinScoreParams {
-  CUtensorMap tm_k;         // prefill K, same map shape as AttnParams::tm_k
+  CUtensorMap tm_k;         // prefill K, 128-row box (as AttnParams::tm_k128)
+  CUtensorMap tm_qwin;      // q_win [W, Hq, D], box = W tokens x G heads x 64 columns
   const bf16* q_win;        // [W, Hq, D]
   const float* win_m;       // [N, Hq, W]
   const float* win_l;       // [N, Hq, W]

@@ -5,13 +5,14 @@
 //               softmax over the C+1 rows of chunk j of (scale * q_win[w,h] . k[t,g]).
 //
 // The attention kernel has already produced, for every (chunk, head, window
-// row), the row maximum m (log2 units) and the denominator l.  This kernel
+// row), the row maximum m (log2 units) and the denominator l, folded here into
+// one constant b = m + log2(l) per window row (p = 2^(s*scale - b)).  This kernel
 // recomputes the logits transposed -- S^T = K Q_win^T with the 128 key rows of
 // one tile on the TMEM lanes and the W*G window rows of one KV group on the
-// TMEM columns -- so each thread owns one key and sums exp2(s - m_n) / l_n over
-// its TMEM row with no cross-thread reduction.  One CTA = (chunk, KV head,
-// 128-key tile); it writes that head group's partial score, and the top-B
-// kernel adds the Hkv partials in a fixed order.
+// TMEM columns -- so each thread owns one key and sums exp2(scale*s - b_n)
+// over its TMEM row with no cross-thread reduction.  One CTA = (chunk, KV
+// head, 128-key tile); it writes that head group's partial score, and the
+// top-B kernel adds the Hkv partials in a fixed order.
 #include "pfd_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -30,8 +31,7 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
   __shared__ uint64_t bar_mma[2];
   __shared__ uint32_t tmem_base;
   __shared__ int failed;
-  __shared__ float m_sh[kMaxWindowRows];
-  __shared__ float il_sh[kMaxWindowRows];
+  __shared__ __align__(16) float b_sh[kMaxWindowRows];   // per column: m_n + log2(l_n)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int bid = blockIdx.x;
@@ -50,51 +50,34 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
   uint8_t* q_tile = smem + 128 * D * 2;                 // [nwp rows x D], panels of nwp*128 B
   const uint32_t q_panel = static_cast<uint32_t>(nwp) * 128u;
 
-  if (tid == 0) {
+  if (warp >= 1) {
+    // Padding rows of the window tile are never loaded: keep them zero.
+    const int ts = tid - 32;
+    for (int idx = ts; idx < (nwp - nw) * (D / 8); idx += 128) {
+      const int n = nw + idx / (D / 8), c = idx % (D / 8);
+      *reinterpret_cast<uint4*>(q_tile + sw128_offset(n, c * 8, nwp)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+    for (int n = ts; n < nwp; n += 128) {
+      float b = INFINITY;  // padding columns contribute exp2(-inf) = 0
+      if (n < nw) {
+        const int w = n / p.G, jj = n - w * p.G;
+        const long long idx = (static_cast<long long>(chunk) * p.Hq + g * p.G + jj) * p.n_win + w;
+        const float l = p.win_l[idx];
+        b = l > 0.0f ? p.win_m[idx] + log2f(l) : INFINITY;
+      }
+      b_sh[n] = b;
+    }
+  } else if (lane == 0) {
     mbar_init(&bar_k, 1);
     mbar_init(&bar_mma[0], 1);
     mbar_init(&bar_mma[1], 1);
     fence_barrier_init();
     failed = 0;
-    // K rows of this tile (rows past the chunk are loaded but never written out).
-    const uint32_t bytes = 8u * 16u * D * 2u;
-    mbar_arrive_expect_tx(&bar_k, bytes);
-    const int row0 = chunk * p.chunk_rows + kt * 128;
-    for (int grp = 0; grp < 8; ++grp)
-      for (int pn = 0; pn < D / 64; ++pn)
-        tma_load_3d(k_tile + pn * kPanelBytes + grp * 2048, &p.tm_k, &bar_k, pn * 64, g,
-                    row0 + grp * 16);
   }
   if (warp == 0) {
     tmem_alloc(&tmem_base, tmem_cols);
     tmem_relinquish();
-  }
-  if (warp >= 1) {
-    const int ts = tid - 32;
-    constexpr int kChunks = D / 8;
-    for (int idx = ts; idx < nwp * kChunks; idx += 128) {
-      const int n = idx / kChunks, c = idx % kChunks;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (n < nw) {
-        const int w = n / p.G, jj = n - w * p.G;
-        val = __ldg(reinterpret_cast<const uint4*>(
-            p.q_win + (static_cast<long long>(w) * p.Hq + g * p.G + jj) * D + c * 8));
-      }
-      *reinterpret_cast<uint4*>(q_tile + sw128_offset(n, c * 8, nwp)) = val;
-    }
-    for (int n = ts; n < nwp; n += 128) {
-      if (n < nw) {
-        const int w = n / p.G, jj = n - w * p.G;
-        const long long idx = (static_cast<long long>(chunk) * p.Hq + g * p.G + jj) * p.n_win + w;
-        const float l = p.win_l[idx];
-        m_sh[n] = p.win_m[idx];
-        il_sh[n] = l > 0.0f ? 1.0f / l : 0.0f;
-      } else {
-        m_sh[n] = INFINITY;  // padding rows contribute exp2(-inf) * 0 = 0
-        il_sh[n] = 0.0f;
-      }
-    }
-    fence_proxy_async_smem();
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -104,6 +87,15 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
 
   if (warp == 0) {
     if (lane == 0) {
+      // K rows of this tile (rows past the chunk are loaded but never written
+      // out) and the group's window rows, one box per 64-column panel each.
+      const uint32_t bytes = 128u * D * 2u + static_cast<uint32_t>(nw) * D * 2u;
+      mbar_arrive_expect_tx(&bar_k, bytes);
+      const int row0 = chunk * p.chunk_rows + kt * 128;
+      for (int pn = 0; pn < D / 64; ++pn) {
+        tma_load_3d(k_tile + pn * kPanelBytes, &p.tm_k, &bar_k, pn * 64, g, row0);
+        tma_load_3d(q_tile + pn * q_panel, &p.tm_qwin, &bar_k, pn * 64, g * p.G, 0);
+      }
       bool ok = mbar_wait(&bar_k, 0);
       tc_fence_after_sync();
       const uint32_t ka = smem_u32(k_tile), qa = smem_u32(q_tile);
@@ -131,7 +123,7 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float acc = 0.0f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     bool ok = true;
     for (int nc = 0; nc < n_chunks_n; ++nc) {
       if (!mbar_wait_warp(&bar_mma[nc], 0)) { ok = false; break; }
@@ -142,19 +134,24 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
         uint32_t s[32];
         tmem_ld32(lane_base + n0 + cc, s);
         tmem_ld_wait(s);
+        const float4* b4 = reinterpret_cast<const float4*>(b_sh + n0 + cc);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int n = n0 + cc + i;
-          if (n < nwp)
-            acc = fmaf(ex2_approx(fmaf(__uint_as_float(s[i]), p.scale_log2, -m_sh[n])), il_sh[n],
-                       acc);
+        for (int i = 0; i < 8; ++i) {
+          if (n0 + cc + 4 * i < nwp) {
+            const float4 b = b4[i];
+            acc[0] += ex2_approx(fmaf(__uint_as_float(s[4 * i + 0]), p.scale_log2, -b.x));
+            acc[1] += ex2_approx(fmaf(__uint_as_float(s[4 * i + 1]), p.scale_log2, -b.y));
+            acc[2] += ex2_approx(fmaf(__uint_as_float(s[4 * i + 2]), p.scale_log2, -b.z));
+            acc[3] += ex2_approx(fmaf(__uint_as_float(s[4 * i + 3]), p.scale_log2, -b.w));
+          }
         }
       }
     }
     if (!ok) atomicOr(&failed, 2);
     const int t = kt * 128 + row;
     if (t < p.chunk_rows)
-      p.part_scores[(static_cast<long long>(chunk) * p.Hkv + g) * p.chunk_rows + t] = acc;
+      p.part_scores[(static_cast<long long>(chunk) * p.Hkv + g) * p.chunk_rows + t] =
+          (acc[0] + acc[1]) + (acc[2] + acc[3]);
   }
   tc_fence_before_sync();
   __syncthreads();
