@@ -17,58 +17,75 @@
 //
 // A query tile packs Tq = floor(128 / G) tokens x the G query heads of one KV
 // head (row m = t * G + j), so one 3-D TMA box loads it and every K/V tile is
-// shared by the whole GQA group.  The key sequence is consumed in 16-row
-// groups, 8 per 128-key tile; a tile lying inside one segment is loaded with
-// one 128-row box per 64-column panel, other tiles group by group.
+// shared by the whole GQA group.  A work item holds two such tiles (a, b) and
+// one key range; the key sequence is consumed in 16-row groups, 8 per 128-key
+// tile, and a tile inside one segment is loaded with one 128-row box per
+// 64-column panel.
 //
-// Per SM two CTAs are resident (96 KB shared memory, 256 TMEM columns each),
-// so one CTA's softmax overlaps the other's MMAs and TMA latency.  Inside a
-// CTA (192 threads):
-//   warp 0      TMA producer (Q once; K and V per tile, single-buffered, the
-//               next K loads while the current tile's softmax runs);
-//   warp 1      TMEM owner and single-thread MMA issuer:
-//               S = Q K^T into TMEM columns [0, 128),
-//               O += P V with P read from TMEM columns [0, 64) (bf16 pairs
-//               written over S) and V from shared memory;
-//   warps 2..5  one thread per tile row (TMEM lane): masked row max, exp2,
-//               P into TMEM, O rescale in TMEM only when the running max grows
-//               by more than 2^8, epilogue.
+// The kernel is persistent (one CTA per SM, items strided over the grid) and
+// warp-specialised (352 threads):
+//   warp 0      TMA producer of K and V tiles into a 4-slot ring (K(j), V(j),
+//               K(j+1), ...), so loads run two tiles ahead, also across item
+//               boundaries; it also publishes each tile's group metadata;
+//   warp 10     TMA loader of the item's two Q tiles (once the previous
+//               item's last QK has read the Q buffers);
+//   warp 1      TMEM owner and single-thread MMA issuer, ping-ponging the two
+//               query tiles:  QK_a(0) QK_b(0) | PV_a(j) QK_a(j+1) PV_b(j)
+//               QK_b(j+1) | ...  so the tensor core works on one tile while
+//               the other tile's softmax runs;
+//   warps 2..5  softmax warpgroup of tile a, warps 6..9 of tile b: one thread
+//               per row (TMEM lane): masked row max, exp2, P as bf16 pairs in
+//               TMEM over the S columns already read (the A operand of PV),
+//               O rescale in TMEM only when the running max grows by more than
+//               2^8, and the epilogue of the item.
+// TMEM (512 columns): S_a [0,128), S_b [128,256), O_a [256,..), O_b [384,..).
 #include "pfd_internal.cuh"
 #include "sm103_ptx.cuh"
 
 namespace pfd {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = 352;
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kSoftmaxWarp0 = 2;                  // warps 2..5: tile a, 6..9: tile b
+constexpr int kQLoaderWarp = 10;
+
+constexpr int kWgThreads = 128;
+constexpr int kRing = 4;
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 constexpr uint32_t kPanelBytes = 128u * 128u;    // 128 rows x 128 B
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kTmemS = 0;                   // S fp32 [0,128), P bf16x2 [0,64)
-constexpr uint32_t kTmemO = 128;
+constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.69314718055994530942f;
+
+__device__ __forceinline__ uint32_t tmem_s_col(int x) { return x ? 128u : 0u; }
+__device__ __forceinline__ uint32_t tmem_o_col(int x) { return x ? 384u : 256u; }
 
 enum ItemKind : int { kChunk = 0, kWindow = 1, kDecode = 2 };
 
 struct TileMeta {
   uint32_t nvalid_lo;  // valid rows of groups 0..3, one byte each
   uint32_t nvalid_hi;  // groups 4..7
-  int32_t ngroups;
-  int32_t pad;
+  int32_t ngroups;     // 0 only for the single tile of an empty item
+  int32_t last;        // 1 on the last tile of an item
 };
 
 struct Shared {
-  uint64_t qfull, kfull, vfull, kempty, vempty, sfull, pfull, ofinal, drain;
-  uint64_t mfull[2];
-  TileMeta meta[2];
+  uint64_t q_full, q_empty;
+  uint64_t ring_full[kRing], ring_empty[kRing];
+  uint64_t meta_full[kRing], meta_empty[kRing];
+  uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
+  uint64_t drain;
+  TileMeta meta[kRing];
   uint32_t tmem_base;
-  int32_t g_lo, g_hi, n_tiles, n_seg;
   int32_t failed;
 };
 
 struct Item {
   int kind;
-  int g, mt;
+  int g;
+  int ta;             // query tile index of tile a (tile b = ta + 1)
+  bool has_b;
   int q_map;          // 0 = main q tensor, 1 = q_win
   long long q_row0;   // token row of t = 0 in the q tensor (and in the output)
   int n_t;            // tokens in this item's query block
@@ -77,74 +94,85 @@ struct Item {
   int k0, k1;         // decode: selected-chunk range in sel
 };
 
-// Resolves blockIdx.x into a work item; returns false when the CTA has no work.
-__device__ __forceinline__ bool resolve_item(const AttnParams& p, Item& it) {
-  int bid = blockIdx.x;
+// Work item `idx`; returns false when it holds no query rows.
+__device__ __forceinline__ bool resolve_item(const AttnParams& p, int idx, Item& it) {
   if (p.mode == kModePrefill) {
-    if (bid < p.n_chunk_items) {
+    int pairs;
+    if (idx < p.n_chunk_items) {
       it.kind = kChunk;
-      it.mt = bid % p.mt_chunk;
-      bid /= p.mt_chunk;
+      pairs = (p.mt_chunk + 1) / 2;
       it.q_map = 0;
       it.n_t = p.chunk_rows;
     } else {
-      bid -= p.n_chunk_items;
+      idx -= p.n_chunk_items;
       it.kind = kWindow;
-      it.mt = bid % p.mt_win;
-      bid /= p.mt_win;
+      pairs = (p.mt_win + 1) / 2;
       it.q_map = 1;
       it.n_t = p.n_win;
     }
-    it.g = bid % p.Hkv;
-    it.chunk = bid / p.Hkv;
+    it.ta = 2 * (idx % pairs);
+    idx /= pairs;
+    it.g = idx % p.Hkv;
+    it.chunk = idx / p.Hkv;
     it.q_row0 = it.kind == kChunk ? static_cast<long long>(it.chunk) * p.chunk_rows : 0;
     it.split = 0;
     it.k0 = it.k1 = 0;
-    return it.mt * p.Tq < it.n_t;
+  } else {
+    const int pairs = (p.mt_max + 1) / 2;
+    it.kind = kDecode;
+    it.ta = 2 * (idx % pairs);
+    idx /= pairs;
+    it.split = idx % p.n_splits;
+    idx /= p.n_splits;
+    it.g = idx % p.Hkv;
+    const int seq = idx / p.Hkv;
+    it.q_map = 0;
+    it.chunk = 0;
+    const int lq0 = p.cu_lq[seq], lq1 = p.cu_lq[seq + 1];
+    const int k0 = p.cu_k[seq], k1 = p.cu_k[seq + 1];
+    if (lq0 < 0 || lq1 < lq0 || lq1 > p.total_lq || k0 < 0 || k1 < k0 || k1 > p.total_sel ||
+        k1 - k0 >= kMaxSegments)
+      return false;  // reported by the producer
+    it.q_row0 = lq0;
+    it.n_t = lq1 - lq0;
+    it.k0 = k0;
+    it.k1 = k1;
   }
-  it.kind = kDecode;
-  it.mt = bid % p.mt_max;
-  bid /= p.mt_max;
-  it.split = bid % p.n_splits;
-  bid /= p.n_splits;
-  it.g = bid % p.Hkv;
-  const int seq = bid / p.Hkv;
-  it.q_map = 0;
-  it.chunk = 0;
+  it.has_b = (it.ta + 1) * p.Tq < it.n_t;
+  return it.ta * p.Tq < it.n_t;
+}
+
+__device__ __forceinline__ bool item_shape_error(const AttnParams& p, int idx) {
+  if (p.mode == kModePrefill) return false;
+  const int pairs = (p.mt_max + 1) / 2;
+  const int seq = idx / pairs / p.n_splits / p.Hkv;
   const int lq0 = p.cu_lq[seq], lq1 = p.cu_lq[seq + 1];
   const int k0 = p.cu_k[seq], k1 = p.cu_k[seq + 1];
-  if (lq0 < 0 || lq1 < lq0 || lq1 > p.total_lq || k0 < 0 || k1 < k0 || k1 > p.total_sel ||
-      k1 - k0 >= kMaxSegments) {
-    if (threadIdx.x == 0) raise_dev_err(p.dev_err, PFD_DEVERR_SHAPE);
-    return false;
-  }
-  it.q_row0 = lq0;
-  it.n_t = lq1 - lq0;
-  it.k0 = k0;
-  it.k1 = k1;
-  return it.mt * p.Tq < it.n_t;
+  return lq0 < 0 || lq1 < lq0 || lq1 > p.total_lq || k0 < 0 || k1 < k0 || k1 > p.total_sel ||
+         k1 - k0 >= kMaxSegments;
 }
 
 template <int D>
 struct Layout {
   static constexpr uint32_t kTileBytes = 128u * D * 2u;   // Q, K or V tile
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kTileBytes;
-  static constexpr uint32_t kV = kK + kTileBytes;
-  static constexpr uint32_t kSegRow = kV + kTileBytes;              // int32 [kMaxSegments]
-  static constexpr uint32_t kSegLen = kSegRow + 4u * kMaxSegments;  // int32
-  static constexpr uint32_t kSegG0 = kSegLen + 4u * kMaxSegments;   // int32 [+1], first group
+  static constexpr uint32_t kQ0 = 0;
+  static constexpr uint32_t kQ1 = kQ0 + kTileBytes;
+  static constexpr uint32_t kRing0 = kQ1 + kTileBytes;     // kRing slots of one tile
+  static constexpr uint32_t kSegRow = kRing0 + kRing * kTileBytes;   // int32 [kMaxSegments]
+  static constexpr uint32_t kSegLen = kSegRow + 4u * kMaxSegments;
+  static constexpr uint32_t kSegG0 = kSegLen + 4u * kMaxSegments;    // [kMaxSegments + 1]
   static constexpr uint32_t kTotal = kSegG0 + 4u * (kMaxSegments + 1);
 };
 
 __device__ __forceinline__ int groups_of(int len) { return (len + kGroupRows - 1) / kGroupRows; }
 
-// Fills the segment list of the item (row, length, first global group) in
-// shared memory; run by one full warp.  Decode: the selected chunks' slots
+// Fills the item's segment list (row, length, first global group) in shared
+// memory; run by the whole producer warp.  Decode: the selected chunks' slots
 // through the table, then the live block (the last segment, tensor 1).
 __device__ __forceinline__ int load_segments(const AttnParams& p, const Item& it, int32_t* seg_row,
                                              int32_t* seg_len, int32_t* seg_g0, int lane) {
   int nseg;
+  __syncwarp();
   if (it.kind != kDecode) {
     nseg = 1;
     if (lane == 0) {
@@ -195,15 +223,18 @@ __device__ __forceinline__ int load_segments(const AttnParams& p, const Item& it
   return nseg;
 }
 
+// Softmax warpgroup state that persists over the tiles of one item.
+struct RowState {
+  float m_used;
+  float l_sum;
+};
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 attention_kernel(const __grid_constant__ AttnParams p) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
-
-  Item it;
-  if (!resolve_item(p, it)) return;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -214,45 +245,41 @@ attention_kernel(const __grid_constant__ AttnParams p) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const bool with_pv = it.kind != kWindow;
   const int G = p.G;
-  const int q_rows = G * p.Tq;                 // rows of the tile filled by the Q box
+  const int q_rows = G * p.Tq;   // rows of a query tile filled by the Q box
 
   // ----------------------------------------------------------- prologue --
-  if (warp == 0) {
-    const int nseg = load_segments(p, it, seg_row, seg_len, seg_g0, lane);
-    if (lane == 0) {
-      mbar_init(&sh.qfull, 1);
-      mbar_init(&sh.kfull, 1);
-      mbar_init(&sh.vfull, 1);
-      mbar_init(&sh.kempty, 1);
-      mbar_init(&sh.vempty, 1);
-      mbar_init(&sh.sfull, 1);
-      mbar_init(&sh.pfull, kSoftmaxThreads);
-      mbar_init(&sh.ofinal, 1);
-      mbar_init(&sh.drain, 1);
-      mbar_init(&sh.mfull[0], 1);
-      mbar_init(&sh.mfull[1], 1);
-      fence_barrier_init();
-      const long long total = seg_g0[nseg];
-      const int n_splits = it.kind == kDecode ? p.n_splits : 1;
-      const long long lo = total * it.split / n_splits;
-      const long long hi = total * (it.split + 1) / n_splits;
-      sh.g_lo = static_cast<int>(lo);
-      sh.g_hi = static_cast<int>(hi);
-      sh.n_tiles = static_cast<int>((hi - lo + kGroupsPerTile - 1) / kGroupsPerTile);
-      sh.n_seg = nseg;
-      sh.failed = 0;
+  if (tid == 0) {
+    mbar_init(&sh.q_full, 1);
+    mbar_init(&sh.q_empty, 1);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&sh.ring_full[i], 1);
+      mbar_init(&sh.ring_empty[i], 1);
+      mbar_init(&sh.meta_full[i], 1);
+      mbar_init(&sh.meta_empty[i], 1 + 8);   // the MMA thread + one lane per softmax warp
     }
-  } else if (warp == 1) {
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&sh.s_full[x], 1);
+      mbar_init(&sh.p_full[x], kWgThreads);
+      mbar_init(&sh.o_full[x], 1);
+      mbar_init(&sh.o_free[x], kWgThreads);
+    }
+    mbar_init(&sh.drain, 1);
+    fence_barrier_init();
+    sh.failed = 0;
+  }
+  if (warp == kMmaWarp) {
     tmem_alloc(&sh.tmem_base, kTmemCols);
     tmem_relinquish();
-  } else if (q_rows < kBlockM) {
-    // Tile rows past the Q box are never loaded: keep them zero.
-    const int ts = tid - 64;
-    for (int idx = ts; idx < (kBlockM - q_rows) * (D / 8); idx += kSoftmaxThreads) {
-      const int r = q_rows + idx / (D / 8), c = idx % (D / 8);
-      *reinterpret_cast<uint4*>(smem + L::kQ + sw128_offset(r, c * 8, kBlockM)) =
+  }
+  if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 8 && q_rows < kBlockM) {
+    // Rows of the Q tiles past the Q box are never loaded: keep them zero.
+    const int ts = tid - kSoftmaxWarp0 * 32;
+    for (int idx = ts; idx < 2 * (kBlockM - q_rows) * (D / 8); idx += 2 * kWgThreads) {
+      const int x = idx / ((kBlockM - q_rows) * (D / 8));
+      const int rem = idx % ((kBlockM - q_rows) * (D / 8));
+      const int r = q_rows + rem / (D / 8), c = rem % (D / 8);
+      *reinterpret_cast<uint4*>(smem + (x ? L::kQ1 : L::kQ0) + sw128_offset(r, c * 8, kBlockM)) =
           make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
@@ -260,347 +287,481 @@ attention_kernel(const __grid_constant__ AttnParams p) {
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-
   const uint32_t tmem = sh.tmem_base;
-  const int n_tiles = sh.n_tiles;
-  const int g_lo = sh.g_lo, g_hi = sh.g_hi;
+  const int n_items = p.n_items;
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------ TMA producer --
-    if (lane == 0 && n_tiles > 0) {
-      const int nseg = sh.n_seg;
-      const int qm = it.q_map;
-      mbar_arrive_expect_tx(&sh.qfull, static_cast<uint32_t>(q_rows) * D * 2);
-      for (int pn = 0; pn < D / 64; ++pn)
-        tma_load_3d(smem + L::kQ + pn * kPanelBytes, &p.tm_q[qm], &sh.qfull, pn * 64, it.g * G,
-                    static_cast<int>(it.q_row0) + it.mt * p.Tq);
-      int seg = 0;
-      while (seg + 1 < nseg && seg_g0[seg + 1] <= g_lo) ++seg;
-      int gofs = g_lo - seg_g0[seg];
-      int g_cur = g_lo;
-      bool ok = true;
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        // Group list of tile j.
-        int tens[kGroupsPerTile];
-        int rows[kGroupsPerTile];
-        uint32_t nv_lo = 0, nv_hi = 0;
-        int ng = 0;
-        const bool one_box = (g_hi - g_cur >= kGroupsPerTile) &&
-                             ((gofs + kGroupsPerTile) * kGroupRows <= seg_len[seg]);
-        for (; ng < kGroupsPerTile && g_cur < g_hi; ++ng, ++g_cur) {
-          const int len = seg_len[seg];
-          const int nv = min(kGroupRows, len - gofs * kGroupRows);
-          tens[ng] = (it.kind == kDecode && seg == nseg - 1) ? 1 : 0;
-          rows[ng] = seg_row[seg] + gofs * kGroupRows;
-          if (ng < 4) nv_lo |= static_cast<uint32_t>(nv) << (8 * ng);
-          else nv_hi |= static_cast<uint32_t>(nv) << (8 * (ng - 4));
-          ++gofs;
-          if (gofs * kGroupRows >= len) {
-            gofs = 0;
-            ++seg;
-            while (seg < nseg && seg_len[seg] == 0) ++seg;
+    uint32_t ring_ctr = 0;   // ring loads issued
+    uint32_t tile_ctr = 0;   // tiles published
+    int items_done = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+      Item it;
+      if (!resolve_item(p, idx, it)) {
+        if (lane == 0 && item_shape_error(p, idx)) raise_dev_err(p.dev_err, PFD_DEVERR_SHAPE);
+        continue;
+      }
+      const bool with_pv = it.kind != kWindow;
+      const int nseg = load_segments(p, it, seg_row, seg_len, seg_g0, lane);
+      if (lane == 0) {
+        const long long total = seg_g0[nseg];
+        const int n_splits = it.kind == kDecode ? p.n_splits : 1;
+        const int g_lo = static_cast<int>(total * it.split / n_splits);
+        const int g_hi = static_cast<int>(total * (it.split + 1) / n_splits);
+        const int n_tiles = (g_hi - g_lo + kGroupsPerTile - 1) / kGroupsPerTile;
+        int seg = 0;
+        while (seg + 1 < nseg && seg_g0[seg + 1] <= g_lo) ++seg;
+        int gofs = g_lo - seg_g0[seg];
+        int g_cur = g_lo;
+        const int tiles_to_publish = n_tiles > 0 ? n_tiles : 1;
+        for (int j = 0; ok && j < tiles_to_publish; ++j) {
+          int tens[kGroupsPerTile];
+          int rows[kGroupsPerTile];
+          uint32_t nv_lo = 0, nv_hi = 0;
+          int ng = 0;
+          const bool one_box = n_tiles > 0 && (g_hi - g_cur >= kGroupsPerTile) &&
+                               ((gofs + kGroupsPerTile) * kGroupRows <= seg_len[seg]);
+          for (; n_tiles > 0 && ng < kGroupsPerTile && g_cur < g_hi; ++ng, ++g_cur) {
+            const int len = seg_len[seg];
+            const int nv = min(kGroupRows, len - gofs * kGroupRows);
+            tens[ng] = (it.kind == kDecode && seg == nseg - 1) ? 1 : 0;
+            rows[ng] = seg_row[seg] + gofs * kGroupRows;
+            if (ng < 4) nv_lo |= static_cast<uint32_t>(nv) << (8 * ng);
+            else nv_hi |= static_cast<uint32_t>(nv) << (8 * (ng - 4));
+            ++gofs;
+            if (gofs * kGroupRows >= len) {
+              gofs = 0;
+              ++seg;
+              while (seg < nseg && seg_len[seg] == 0) ++seg;
+            }
           }
-        }
-        // K(j) replaces K(j-1): wait for QK(j-1).  The metadata slot j & 1 was
-        // last read by the softmax of tile j-2, which ended before QK(j-1).
-        if (j >= 1 && !mbar_wait(&sh.kempty, (j - 1) & 1)) { ok = false; break; }
-        TileMeta& m = sh.meta[j & 1];
-        m.nvalid_lo = nv_lo;
-        m.nvalid_hi = nv_hi;
-        m.ngroups = ng;
-        mbar_arrive(&sh.mfull[j & 1]);
-        const uint32_t bytes = one_box ? static_cast<uint32_t>(kBlockN) * D * 2
-                                       : static_cast<uint32_t>(ng) * kGroupRows * D * 2;
-        mbar_arrive_expect_tx(&sh.kfull, bytes);
-        if (one_box) {
-          for (int pn = 0; pn < D / 64; ++pn)
-            tma_load_3d(smem + L::kK + pn * kPanelBytes, &p.tm_k128[tens[0]], &sh.kfull, pn * 64,
-                        it.g, rows[0]);
-        } else {
-          for (int k = 0; k < ng; ++k)
-            for (int pn = 0; pn < D / 64; ++pn)
-              tma_load_3d(smem + L::kK + pn * kPanelBytes + k * 2048, &p.tm_k16[tens[k]],
-                          &sh.kfull, pn * 64, it.g, rows[k]);
-        }
-        if (with_pv) {
-          // V(j) replaces V(j-1): wait for PV(j-1).
-          if (j >= 1 && !mbar_wait(&sh.vempty, (j - 1) & 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(&sh.vfull, bytes);
-          if (one_box) {
-            for (int pn = 0; pn < D / 64; ++pn)
-              tma_load_3d(smem + L::kV + pn * kPanelBytes, &p.tm_v128[tens[0]], &sh.vfull,
-                          pn * 64, it.g, rows[0]);
-          } else {
-            for (int k = 0; k < ng; ++k)
+          // Metadata slot tile_ctr % kRing: every consumer must have read the
+          // tile published there kRing tiles ago.
+          const int ms = tile_ctr % kRing;
+          if (tile_ctr >= kRing && !mbar_wait(&sh.meta_empty[ms], ((tile_ctr / kRing) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          TileMeta& m = sh.meta[ms];
+          m.nvalid_lo = nv_lo;
+          m.nvalid_hi = nv_hi;
+          m.ngroups = ng;
+          m.last = (j == tiles_to_publish - 1) ? 1 : 0;
+          mbar_arrive(&sh.meta_full[ms]);
+          ++tile_ctr;
+          if (ng == 0) break;
+          const uint32_t bytes = one_box ? static_cast<uint32_t>(kBlockN) * D * 2
+                                         : static_cast<uint32_t>(ng) * kGroupRows * D * 2;
+          for (int kv = 0; kv < (with_pv ? 2 : 1); ++kv) {
+            const int rs = ring_ctr % kRing;
+            if (ring_ctr >= kRing && !mbar_wait(&sh.ring_empty[rs], ((ring_ctr / kRing) - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            uint8_t* dst = smem + L::kRing0 + rs * L::kTileBytes;
+            const CUtensorMap* m128 = kv ? p.tm_v128 : p.tm_k128;
+            const CUtensorMap* m16 = kv ? p.tm_v16 : p.tm_k16;
+            mbar_arrive_expect_tx(&sh.ring_full[rs], bytes);
+            if (one_box) {
               for (int pn = 0; pn < D / 64; ++pn)
-                tma_load_3d(smem + L::kV + pn * kPanelBytes + k * 2048, &p.tm_v16[tens[k]],
-                            &sh.vfull, pn * 64, it.g, rows[k]);
+                tma_load_3d(dst + pn * kPanelBytes, &m128[tens[0]], &sh.ring_full[rs], pn * 64, it.g,
+                            rows[0]);
+            } else {
+              for (int k = 0; k < ng; ++k)
+                for (int pn = 0; pn < D / 64; ++pn)
+                  tma_load_3d(dst + pn * kPanelBytes + k * 2048, &m16[tens[k]], &sh.ring_full[rs],
+                              pn * 64, it.g, rows[k]);
+            }
+            ++ring_ctr;
           }
         }
       }
-      if (!ok) atomicOr(&sh.failed, 1);
-      // The last tile's loads must have landed before the CTA exits.
-      const int jl = n_tiles - 1;
-      mbar_wait(&sh.kfull, jl & 1);
-      if (with_pv) mbar_wait(&sh.vfull, jl & 1);
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      ++items_done;
     }
-  } else if (warp == 1) {
+    if (lane == 0) {
+      if (!ok) atomicOr(&sh.failed, 1);
+      // Loads still in flight must land before the CTA exits.
+      for (uint32_t c = ring_ctr > kRing ? ring_ctr - kRing : 0; c < ring_ctr; ++c)
+        mbar_wait(&sh.ring_full[c % kRing], (c / kRing) & 1);
+    }
+  } else if (warp == kQLoaderWarp) {
+    // -------------------------------------------------------- Q loader --
+    if (lane == 0) {
+      int items_done = 0;
+      bool ok = true;
+      const uint32_t q_bytes = static_cast<uint32_t>(q_rows) * D * 2;
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+        Item it;
+        if (!resolve_item(p, idx, it)) continue;
+        // The Q buffers are free once the previous item's last QK has run.
+        if (items_done > 0 && !mbar_wait(&sh.q_empty, (items_done - 1) & 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(&sh.q_full, it.has_b ? 2 * q_bytes : q_bytes);
+        for (int x = 0; x < (it.has_b ? 2 : 1); ++x)
+          for (int pn = 0; pn < D / 64; ++pn)
+            tma_load_3d(smem + (x ? L::kQ1 : L::kQ0) + pn * kPanelBytes, &p.tm_q[it.q_map],
+                        &sh.q_full, pn * 64, it.g * G,
+                        static_cast<int>(it.q_row0) + (it.ta + x) * p.Tq);
+        ++items_done;
+      }
+      if (!ok) atomicOr(&sh.failed, 8);
+      if (items_done > 0) mbar_wait(&sh.q_full, (items_done - 1) & 1);
+    }
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------- MMA issuer --
-    if (lane == 0 && n_tiles > 0) {
-      bool ok = mbar_wait(&sh.qfull, 0);
-      const uint32_t q_addr = s_base + L::kQ;
-      const uint32_t k_addr = s_base + L::kK;
-      const uint32_t v_addr = s_base + L::kV;
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const uint32_t ph = j & 1;
-        if (!mbar_wait(&sh.kfull, ph)) { ok = false; break; }
-        tc_fence_after_sync();
-        const int ng = min(sh.meta[j & 1].ngroups, kGroupsPerTile);
-        const uint32_t idesc_s = idesc_bf16(kBlockM, max(ng, 1) * kGroupRows, false, false);
-        if (ng > 0) {
+    if (lane == 0) {
+      uint32_t ring_ctr = 0, tile_ctr = 0;
+      uint32_t p_ph[2] = {0, 0};
+      int items_done = 0;
+      bool ok = true;
+      constexpr uint32_t idesc_o = idesc_bf16(kBlockM, D, false, true);
+      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+        Item it;
+        if (!resolve_item(p, idx, it)) continue;
+        const bool with_pv = it.kind != kWindow;
+        const int nx = it.has_b ? 2 : 1;
+        bool ofree_done[2] = {items_done == 0, items_done == 0};
+        auto wait_ofree = [&](int x) -> bool {
+          if (ofree_done[x]) return true;
+          ofree_done[x] = true;
+          const bool r = mbar_wait(&sh.o_free[x], (items_done - 1) & 1);
+          tc_fence_after_sync();
+          return r;
+        };
+        if (!mbar_wait(&sh.q_full, items_done & 1)) { ok = false; break; }
+        // QK of one tile into S_x from the K slot `ks`.
+        auto issue_qk = [&](int x, int ng, uint32_t ks) {
+          const uint32_t q_addr = s_base + (x ? L::kQ1 : L::kQ0);
+          const uint32_t k_addr = s_base + L::kRing0 + ks * L::kTileBytes;
+          const uint32_t idesc_s = idesc_bf16(kBlockM, ng * kGroupRows, false, false);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t a = sw128_desc(q_addr + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
             const uint64_t b = sw128_desc(k_addr + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
-            mma_bf16_ss(tmem + kTmemS, a, b, idesc_s, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem + tmem_s_col(x), a, b, idesc_s, kk > 0 ? 1u : 0u);
           }
-        }
-        mma_commit(&sh.sfull);
-        mma_commit(&sh.kempty);
-        if (!mbar_wait(&sh.pfull, ph)) { ok = false; break; }
-        if (with_pv) {
-          if (!mbar_wait(&sh.vfull, ph)) { ok = false; break; }
-          tc_fence_after_sync();
-          constexpr uint32_t idesc_o = idesc_bf16(kBlockM, D, false, true);
+          mma_commit(&sh.s_full[x]);
+        };
+        // Rows of a ragged group past its segment may hold anything (another
+        // slot, padding): zero them in V so that 0 * v stays 0 in PV.
+        auto fix_v = [&](const TileMeta& m, uint32_t vs) {
+          uint8_t* v_tile = smem + L::kRing0 + vs * L::kTileBytes;
+          for (int grp = 0; grp < m.ngroups; ++grp) {
+            const uint32_t w = grp < 4 ? m.nvalid_lo : m.nvalid_hi;
+            const int nv = static_cast<int>((w >> (8 * (grp & 3))) & 0xFFu);
+            for (int r = nv; r < kGroupRows; ++r)
+              for (int pn = 0; pn < D / 64; ++pn) {
+                uint4* dst = reinterpret_cast<uint4*>(v_tile + pn * kPanelBytes + (grp * kGroupRows + r) * 128);
+#pragma unroll
+                for (int c16 = 0; c16 < 8; ++c16) dst[c16] = make_uint4(0u, 0u, 0u, 0u);
+              }
+          }
+          fence_proxy_async_smem();
+        };
+        auto issue_pv = [&](int x, int ng, uint32_t vs, bool first) {
+          const uint32_t v_addr = s_base + L::kRing0 + vs * L::kTileBytes;
           for (int kk = 0; kk < ng; ++kk) {
             const uint64_t v = sw128_desc(v_addr + kk * 2048, kPanelBytes, 1024);
-            mma_bf16_ts(tmem + kTmemO, tmem + kTmemS + kk * 8, v, idesc_o,
-                        (j > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ts(tmem + tmem_o_col(x), tmem + tmem_s_col(x) + kk * 8, v, idesc_o,
+                        (!first || kk > 0) ? 1u : 0u);
           }
+        };
+        // Tile 0.
+        int ms = tile_ctr % kRing;
+        if (!mbar_wait(&sh.meta_full[ms], (tile_ctr / kRing) & 1)) { ok = false; break; }
+        TileMeta mt = sh.meta[ms];
+        mbar_arrive(&sh.meta_empty[ms]);
+        ++tile_ctr;
+        if (mt.ngroups > 0) {
+          uint32_t ks = ring_ctr % kRing;
+          if (!mbar_wait(&sh.ring_full[ks], (ring_ctr / kRing) & 1)) { ok = false; break; }
+          tc_fence_after_sync();
+          for (int x = 0; x < nx; ++x) issue_qk(x, mt.ngroups, ks);
+          mma_commit(&sh.ring_empty[ks]);
+          ++ring_ctr;
+          for (int j = 0;; ++j) {
+            const bool last = mt.last != 0;
+            const int ng = mt.ngroups;
+            uint32_t vs = 0;
+            if (with_pv) {
+              vs = ring_ctr % kRing;
+              if (!mbar_wait(&sh.ring_full[vs], (ring_ctr / kRing) & 1)) { ok = false; break; }
+              ++ring_ctr;
+              const bool full_tile = mt.ngroups == kGroupsPerTile && mt.nvalid_lo == 0x10101010u &&
+                                     mt.nvalid_hi == 0x10101010u;
+              if (!full_tile) fix_v(mt, vs);
+            }
+            TileMeta mn = mt;
+            uint32_t ks_next = 0;
+            if (!last) {
+              ms = tile_ctr % kRing;
+              if (!mbar_wait(&sh.meta_full[ms], (tile_ctr / kRing) & 1)) { ok = false; break; }
+              mn = sh.meta[ms];
+              mbar_arrive(&sh.meta_empty[ms]);
+              ++tile_ctr;
+              ks_next = ring_ctr % kRing;
+            }
+            for (int x = 0; x < nx; ++x) {
+              // softmax x finished tile j (S_x read, P_x written)
+              if (!mbar_wait(&sh.p_full[x], p_ph[x])) { ok = false; break; }
+              p_ph[x] ^= 1u;
+              tc_fence_after_sync();
+              if (with_pv) {
+                if (j == 0 && !wait_ofree(x)) { ok = false; break; }
+                issue_pv(x, ng, vs, j == 0);
+              }
+              if (!last) {
+                if (x == 0 && !mbar_wait(&sh.ring_full[ks_next], (ring_ctr / kRing) & 1)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after_sync();
+                issue_qk(x, mn.ngroups, ks_next);
+              }
+            }
+            if (!ok) break;
+            if (with_pv) mma_commit(&sh.ring_empty[vs]);
+            if (last) break;
+            mma_commit(&sh.ring_empty[ks_next]);
+            ++ring_ctr;
+            mt = mn;
+          }
+          if (!ok) break;
         }
-        mma_commit(&sh.vempty);
+        // Every item waits for the previous item's epilogue of both tiles
+        // exactly once (before its first PV into O_x, else here), so the
+        // o_free phases are consumed in order.
+        for (int x = 0; ok && x < 2; ++x)
+          if (!wait_ofree(x)) ok = false;
+        if (!ok) break;
+        // O_x of this item is final once every MMA issued so far completes.
+        mma_commit(&sh.o_full[0]);
+        mma_commit(&sh.o_full[1]);
+        mma_commit(&sh.q_empty);
+        ++items_done;
       }
       if (!ok) atomicOr(&sh.failed, 2);
-      mma_commit(&sh.ofinal);
-      // Every MMA issued above has completed once `drain` flips.
       mma_commit(&sh.drain);
       mbar_wait(&sh.drain, 0);
     }
-  } else {
-    // ---------------------------------------------- softmax + epilogue --
+  } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 8) {
+    // ------------------------------------------------- softmax warpgroups --
+    const int x = warp >= kSoftmaxWarp0 + 4 ? 1 : 0;   // query tile of this warpgroup
     const int quarter = warp & 3;         // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;  // tile row of this thread
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t s_col = tmem_s_col(x), o_col = tmem_o_col(x);
     const float scale = p.scale_log2;
-
-    float m_used = -INFINITY;
-    float l_sum = 0.0f;
+    uint32_t tile_ctr = 0, ring_ctr = 0, s_ph = 0;
+    int items_done = 0;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const uint32_t ph = j & 1;
-      if (!mbar_wait_warp(&sh.mfull[j & 1], (j >> 1) & 1) || !mbar_wait_warp(&sh.sfull, ph)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      const TileMeta meta = sh.meta[j & 1];
-      const int ncol = meta.ngroups * kGroupRows;
-      const bool full = meta.ngroups == kGroupsPerTile && meta.nvalid_lo == 0x10101010u &&
-                        meta.nvalid_hi == 0x10101010u;
-      auto nv_of = [&](int grp) -> int {
-        const uint32_t w = grp < 4 ? meta.nvalid_lo : meta.nvalid_hi;
-        return static_cast<int>((w >> (8 * (grp & 3))) & 0xFFu);
-      };
+    for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+      Item it;
+      if (!resolve_item(p, idx, it)) continue;
+      const bool with_pv = it.kind != kWindow;
+      const bool active = x == 0 || it.has_b;
+      float m_used = -INFINITY, l_sum = 0.0f;
+      int n_seen = 0;
+      for (;;) {
+        const int ms = tile_ctr % kRing;
+        if (!mbar_wait_warp(&sh.meta_full[ms], (tile_ctr / kRing) & 1)) { ok = false; break; }
+        const TileMeta meta = sh.meta[ms];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.meta_empty[ms]);
+        ++tile_ctr;
+        if (meta.ngroups == 0) break;
+        ring_ctr += with_pv ? 2 : 1;
+        ++n_seen;
+        if (!active) {
+          if (meta.last) break;
+          continue;
+        }
+        if (!mbar_wait_warp(&sh.s_full[x], s_ph)) { ok = false; break; }
+        s_ph ^= 1u;
+        tc_fence_after_sync();
+        const int ncol = meta.ngroups * kGroupRows;
+        const bool full = meta.ngroups == kGroupsPerTile && meta.nvalid_lo == 0x10101010u &&
+                          meta.nvalid_hi == 0x10101010u;
+        auto nv_of = [&](int grp) -> int {
+          const uint32_t w = grp < 4 ? meta.nvalid_lo : meta.nvalid_hi;
+          return static_cast<int>((w >> (8 * (grp & 3))) & 0xFFu);
+        };
 
-      // Pass 1: row max of the valid logits.
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+        // Ragged tiles: logits of rows past a group's valid count become -inf
+        // (their exp2 is then 0), so one code path serves every tile.
+        auto mask_half = [&](uint32_t (&sr)[2][32], int half) {
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        if (ch * 32 < ncol) {
-          uint32_t s[32];
-          tmem_ld32(lane_base + kTmemS + ch * 32, s);
-          tmem_ld_wait(s);
-          if (full) {
+          for (int gq = 0; gq < 4; ++gq) {
+            const int nv = nv_of(half * 4 + gq);
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              mx0 = fmaxf(mx0, __uint_as_float(s[i]));
-              mx1 = fmaxf(mx1, __uint_as_float(s[i + 1]));
-              mx2 = fmaxf(mx2, __uint_as_float(s[i + 2]));
-              mx3 = fmaxf(mx3, __uint_as_float(s[i + 3]));
-            }
-          } else {
-            const int nva = nv_of(2 * ch), nvb = nv_of(2 * ch + 1);
+            for (int i = 0; i < 16; ++i)
+              if (i >= nv) sr[gq >> 1][(gq & 1) * 16 + i] = __float_as_uint(-INFINITY);
+          }
+        };
+
+        // Pass 1: row max over the tile, 64 columns (two TMEM loads) at a time.
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          if (half * 64 < ncol) {
+            uint32_t sr[2][32];
+            tmem_ld32(lane_base + s_col + half * 64, sr[0]);
+            tmem_ld32(lane_base + s_col + half * 64 + 32, sr[1]);
+            tmem_ld_wait(sr[0]);
+            reg_fence(sr[1]);
+            if (!full) mask_half(sr, half);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const bool valid = (i & 15) < (i < 16 ? nva : nvb);
-              const float x = valid ? __uint_as_float(s[i]) : -INFINITY;
-              if ((i & 3) == 0) mx0 = fmaxf(mx0, x);
-              else if ((i & 3) == 1) mx1 = fmaxf(mx1, x);
-              else if ((i & 3) == 2) mx2 = fmaxf(mx2, x);
-              else mx3 = fmaxf(mx3, x);
+              mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(sr[0][i]));
+              mx[(i + 2) & 3] = fmaxf(mx[(i + 2) & 3], __uint_as_float(sr[1][i]));
             }
           }
         }
-      }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale;
+        const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale;
 
-      // Rescale decision per row; the TMEM rescale of O is warp-collective,
-      // so a warp rescales when any of its rows needs it (alpha = 1 for the
-      // others).  sfull(j) also covers PV(j-1): O is complete here.
-      const bool mine = m_tile > m_used + kRescaleThreshold;
-      if (__any_sync(0xFFFFFFFFu, mine)) {
-        const float m_new = mine ? m_tile : m_used;
-        const float alpha = mine ? ex2_approx(m_used - m_new) : 1.0f;
-        if (j >= 1 && with_pv) {
+        // Rescale decision per row; the TMEM rescale of O is warp-collective,
+        // so a warp rescales when any of its rows needs it (alpha = 1 for the
+        // others).  s_full covers PV(j-1): O_x is complete here.
+        const bool mine = m_tile > m_used + kRescaleThreshold;
+        if (__any_sync(0xFFFFFFFFu, mine)) {
+          const float m_new = mine ? m_tile : m_used;
+          const float alpha = mine ? ex2_approx(m_used - m_new) : 1.0f;
+          if (n_seen > 1 && with_pv) {
+            uint32_t o0[32], o1[32];
+#pragma unroll 1
+            for (int ch = 0; ch < D / 32; ch += 2) {
+              tmem_ld32(lane_base + o_col + ch * 32, o0);
+              tmem_ld32(lane_base + o_col + ch * 32 + 32, o1);
+              tmem_ld_wait(o0);
+              reg_fence(o1);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                o0[i] = __float_as_uint(__uint_as_float(o0[i]) * alpha);
+                o1[i] = __float_as_uint(__uint_as_float(o1[i]) * alpha);
+              }
+              tmem_st32(lane_base + o_col + ch * 32, o0);
+              tmem_st32(lane_base + o_col + ch * 32 + 32, o1);
+            }
+          }
+          l_sum *= alpha;
+          m_used = m_new;
+        }
+
+        // Pass 2: probabilities relative to m_used -> bf16 pairs in TMEM
+        // columns [0, 64) of S_x (over logits already read), fp32 row sum.
+        const float neg_m = -m_used;
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          if (half * 64 < ncol) {
+            uint32_t sr[2][32];
+            tmem_ld32(lane_base + s_col + half * 64, sr[0]);
+            tmem_ld32(lane_base + s_col + half * 64 + 32, sr[1]);
+            tmem_ld_wait(sr[0]);
+            reg_fence(sr[1]);
+            if (!full) mask_half(sr, half);
+            uint32_t packed[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float a0 = ex2_approx(fmaf(__uint_as_float(sr[0][i]), scale, neg_m));
+              const float a1 = ex2_approx(fmaf(__uint_as_float(sr[0][i + 1]), scale, neg_m));
+              const float b0 = ex2_approx(fmaf(__uint_as_float(sr[1][i]), scale, neg_m));
+              const float b1 = ex2_approx(fmaf(__uint_as_float(sr[1][i + 1]), scale, neg_m));
+              sum[0] += a0;
+              sum[1] += a1;
+              sum[2] += b0;
+              sum[3] += b1;
+              packed[i >> 1] = pack_bf16x2(a0, a1);
+              packed[16 + (i >> 1)] = pack_bf16x2(b0, b1);
+            }
+            if (with_pv) tmem_st32(lane_base + s_col + half * 32, packed);
+          }
+        }
+        l_sum += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+        if (with_pv) tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&sh.p_full[x]);
+        if (meta.last) break;
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue --
+      if (!mbar_wait_warp(&sh.o_full[x], items_done & 1)) { ok = false; break; }
+      tc_fence_after_sync();
+      if (active) {
+        const int t_local = row / G;
+        const int jj = row - t_local * G;
+        const int t = (it.ta + x) * p.Tq + t_local;
+        const bool row_ok = row < q_rows && t < it.n_t;
+        const int head = it.g * G + jj;
+        if (it.kind == kWindow) {
+          if (row_ok) {
+            const long long idx2 = (static_cast<long long>(it.chunk) * p.Hq + head) * p.n_win + t;
+            p.win_m[idx2] = m_used;
+            p.win_l[idx2] = l_sum;
+          }
+        } else {
+          const long long tok = it.q_row0 + t;
+          const bool final_out = it.kind == kChunk || p.n_splits == 1;
+          const float inv_l = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
 #pragma unroll 1
           for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t o[32];
-            tmem_ld32(lane_base + kTmemO + ch * 32, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(lane_base + kTmemO + ch * 32, o);
-          }
-        }
-        l_sum *= alpha;
-        m_used = m_new;
-      }
-
-      // Pass 2: probabilities relative to m_used -> bf16 pairs in TMEM
-      // columns [0, 64) (over S columns already read), fp32 row sum.
-      const float neg_m = -m_used;
-      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        if (half * 64 < ncol) {
-          uint32_t packed[32];
-#pragma unroll
-          for (int sub = 0; sub < 2; ++sub) {
-            const int ch = half * 2 + sub;
-            uint32_t s[32];
-            tmem_ld32(lane_base + kTmemS + ch * 32, s);
-            tmem_ld_wait(s);
-            if (full) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float a = ex2_approx(fmaf(__uint_as_float(s[2 * i]), scale, neg_m));
-                const float b = ex2_approx(fmaf(__uint_as_float(s[2 * i + 1]), scale, neg_m));
-                if (i & 1) { sum2 += a; sum3 += b; } else { sum0 += a; sum1 += b; }
-                packed[sub * 16 + i] = pack_bf16x2(a, b);
-              }
+            if (n_seen > 0) {
+              tmem_ld32(lane_base + o_col + ch * 32, o);
+              tmem_ld_wait(o);
             } else {
-              const int nva = nv_of(2 * ch), nvb = nv_of(2 * ch + 1);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int c0 = 2 * i, c1 = 2 * i + 1;
-                const bool v0 = (c0 & 15) < (c0 < 16 ? nva : nvb);
-                const bool v1 = (c1 & 15) < (c1 < 16 ? nva : nvb);
-                const float a = v0 ? ex2_approx(fmaf(__uint_as_float(s[c0]), scale, neg_m)) : 0.0f;
-                const float b = v1 ? ex2_approx(fmaf(__uint_as_float(s[c1]), scale, neg_m)) : 0.0f;
-                if (i & 1) { sum2 += a; sum3 += b; } else { sum0 += a; sum1 += b; }
-                packed[sub * 16 + i] = pack_bf16x2(a, b);
-              }
+              for (int i = 0; i < 32; ++i) o[i] = 0u;
+            }
+            if (!row_ok) continue;
+            if (final_out) {
+              uint32_t packed[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                packed[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                        __uint_as_float(o[2 * i + 1]) * inv_l);
+              uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * p.Hq + head) * D + ch * 32);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4)
+                dst[q4] = make_uint4(packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2],
+                                     packed[4 * q4 + 3]);
+            } else {
+              float4* dst = reinterpret_cast<float4*>(
+                  p.part_acc +
+                  ((static_cast<long long>(it.split) * p.total_lq + tok) * p.Hq + head) * D + ch * 32);
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4)
+                dst[q4] = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
+                                      __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
             }
           }
-          if (with_pv) tmem_st32(lane_base + kTmemS + half * 32, packed);
-        }
-      }
-      l_sum += (sum0 + sum1) + (sum2 + sum3);
-      if (with_pv) tmem_st_wait();
-
-      if (with_pv && !full) {
-        // Rows of a ragged group that lie past its segment may hold anything
-        // (another slot, padding): zero them in V so that 0 * v stays 0.
-        if (!mbar_wait_warp(&sh.vfull, ph)) { ok = false; break; }
-        const int ts = tid - 64;
-        uint8_t* v_tile = smem + L::kV;
-        for (int grp = 0; grp < meta.ngroups; ++grp) {
-          const int nv = nv_of(grp);
-          const int n_bad = (kGroupRows - nv) * (D / 64) * 8;  // 16-byte chunks to clear
-          for (int u = ts; u < n_bad; u += kSoftmaxThreads) {
-            const int c16 = u & 7;
-            const int rest = u >> 3;
-            const int pn = rest % (D / 64);
-            const int r = nv + rest / (D / 64);
-            *reinterpret_cast<uint4*>(v_tile + pn * kPanelBytes + (grp * kGroupRows + r) * 128 +
-                                      c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+          if (row_ok && it.kind == kDecode) {
+            if (p.n_splits == 1) {
+              if (p.lse != nullptr)
+                p.lse[tok * p.Hq + head] =
+                    l_sum > 0.0f ? (m_used + log2f(l_sum)) * kLn2 : -INFINITY;
+            } else {
+              const long long idx2 =
+                  (static_cast<long long>(it.split) * p.total_lq + tok) * p.Hq + head;
+              p.part_m[idx2] = m_used;
+              p.part_l[idx2] = l_sum;
+            }
           }
         }
-        fence_proxy_async_smem();
       }
       tc_fence_before_sync();
-      mbar_arrive(&sh.pfull);
+      mbar_arrive(&sh.o_free[x]);
+      ++items_done;
     }
-
-    // ------------------------------------------------------------ epilogue --
-    if (ok && n_tiles > 0 && !mbar_wait_warp(&sh.ofinal, 0)) ok = false;
-    tc_fence_after_sync();
     if (!ok) atomicOr(&sh.failed, 4);
-
-    const int t_local = row / G;
-    const int jj = row - t_local * G;
-    const int t = it.mt * p.Tq + t_local;
-    const bool row_ok = row < q_rows && t < it.n_t;
-    const int head = it.g * G + jj;
-    if (it.kind == kWindow) {
-      if (row_ok) {
-        const long long idx = (static_cast<long long>(it.chunk) * p.Hq + head) * p.n_win + t;
-        p.win_m[idx] = m_used;
-        p.win_l[idx] = l_sum;
-      }
-    } else {
-      const long long tok = it.q_row0 + t;
-      const bool final_out = it.kind == kChunk || p.n_splits == 1;
-      const float inv_l = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t o[32];
-        if (n_tiles > 0) {
-          tmem_ld32(lane_base + kTmemO + ch * 32, o);
-          tmem_ld_wait(o);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
-        }
-        if (!row_ok) continue;
-        if (final_out) {
-          uint32_t packed[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            packed[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
-                                    __uint_as_float(o[2 * i + 1]) * inv_l);
-          uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * p.Hq + head) * D + ch * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            dst[q4] = make_uint4(packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2],
-                                 packed[4 * q4 + 3]);
-        } else {
-          float4* dst = reinterpret_cast<float4*>(
-              p.part_acc + ((static_cast<long long>(it.split) * p.total_lq + tok) * p.Hq + head) * D +
-              ch * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            dst[q4] = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
-                                  __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
-        }
-      }
-      if (row_ok && it.kind == kDecode) {
-        if (p.n_splits == 1) {
-          if (p.lse != nullptr)
-            p.lse[tok * p.Hq + head] = l_sum > 0.0f ? (m_used + log2f(l_sum)) * kLn2 : -INFINITY;
-        } else {
-          const long long idx = (static_cast<long long>(it.split) * p.total_lq + tok) * p.Hq + head;
-          p.part_m[idx] = m_used;
-          p.part_l[idx] = l_sum;
-        }
-      }
-    }
   }
 
   tc_fence_before_sync();
   __syncthreads();
   if (tid == 0 && sh.failed != 0) raise_dev_err(p.dev_err, PFD_DEVERR_TIMEOUT);
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -613,7 +774,7 @@ size_t attention_smem_bytes(int D) {
 }
 
 cudaError_t launch_attention(const AttnParams& p, int grid, cudaStream_t stream) {
-  if (grid <= 0) return cudaSuccess;
+  if (grid <= 0 || p.n_items <= 0) return cudaSuccess;
   const size_t smem = attention_smem_bytes(p.D);
   cudaError_t err;
   if (p.D == 64) {

@@ -209,12 +209,15 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
   ap.n_win = W;
   ap.mt_chunk = ceil_div(C + 1, Tq);
   ap.mt_win = W > 0 ? ceil_div(W, Tq) : 0;
-  ap.n_chunk_items = N * Hkv * ap.mt_chunk;
+  ap.n_chunk_items = N * Hkv * ceil_div(ap.mt_chunk, 2);
   ap.n_splits = 1;
   ap.scale_log2 = scale * kLog2e;
-  const long long grid = static_cast<long long>(ap.n_chunk_items) + static_cast<long long>(N) * Hkv * ap.mt_win;
-  if (grid >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
-  pfd_status s = from_cuda(launch_attention(ap, static_cast<int>(grid), st));
+  const long long items =
+      static_cast<long long>(ap.n_chunk_items) + static_cast<long long>(N) * Hkv * ceil_div(ap.mt_win, 2);
+  if (items >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
+  ap.n_items = static_cast<int>(items);
+  const int grid = static_cast<int>(std::min<long long>(items, device_sm_count()));
+  pfd_status s = from_cuda(launch_attention(ap, grid, st));
   if (s != PFD_OK) return s;
 
   if (W > 0) {
@@ -292,19 +295,20 @@ int pfd_decode_plan_splits(int batch, const int32_t* cu_lq_host, const int32_t* 
   for (int b = 0; b < batch; ++b) {
     const long long lq = cu_lq_host[b + 1] - cu_lq_host[b];
     const long long kb = cu_k_host[b + 1] - cu_k_host[b];
-    items += Hkv * ((lq + Tq - 1) / Tq);
+    items += Hkv * (((lq + Tq - 1) / Tq + 1) / 2);   // two query tiles per item
     keys_max = std::max(keys_max, kb * std::max(0, max_chunk_len) + lq);
   }
   if (items <= 0) return 1;
-  const long long sms = 2LL * device_sm_count();   // two CTAs resident per SM
+  const long long sms = device_sm_count();   // one persistent CTA per SM
   int best = 1;
   double best_cost = 1e300;
   const long long max_s = std::max<long long>(1, std::min<long long>(kMaxSplits, (keys_max + kBlockN - 1) / kBlockN));
   for (int S = 1; S <= max_s; ++S) {
     const long long waves = (items * S + sms - 1) / sms;
     const long long tiles = (keys_max + static_cast<long long>(S) * kBlockN - 1) / (static_cast<long long>(S) * kBlockN);
-    // a CTA's fixed cost (setup, Q load, epilogue) ~ 2 tiles; the merge ~ 1 tile
-    const double cost = static_cast<double>(waves) * (tiles + 2) + (S > 1 ? 1.0 : 0.0);
+    // an item costs ~2 units per key tile (two query tiles) plus ~3 units of
+    // fixed cost (Q load, pipeline fill, epilogue); the merge ~ 2 units
+    const double cost = static_cast<double>(waves) * (2.0 * tiles + 3.0) + (S > 1 ? 2.0 : 0.0);
     if (cost < best_cost) {
       best_cost = cost;
       best = S;
@@ -406,9 +410,11 @@ pfd_status pfd_decode_attention(const pfd_bf16* q, const pfd_bf16* k_self,
   ap.total_lq = total_lq;
   ap.total_sel = total_sel;
   ap.scale_log2 = scale * kLog2e;
-  const long long grid = static_cast<long long>(batch) * Hkv * S * mt_max;
-  if (grid >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
-  pfd_status s = from_cuda(launch_attention(ap, static_cast<int>(grid), st));
+  const long long items = static_cast<long long>(batch) * Hkv * S * ceil_div(mt_max, 2);
+  if (items >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
+  ap.n_items = static_cast<int>(items);
+  const int grid = static_cast<int>(std::min<long long>(items, device_sm_count()));
+  pfd_status s = from_cuda(launch_attention(ap, grid, st));
   if (s != PFD_OK || S == 1) return s;
   MergeParams mp;
   mp.part_m = ap.part_m;

@@ -9,7 +9,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/pfd.h"
+#include "pfd.h"
 
 namespace pfd {
 
@@ -65,6 +65,7 @@ struct AttnParams {
   int mode;
   int Hq, Hkv, G, D;
   int Tq;               // tokens per query tile: floor(128 / G)
+  int n_items;          // work items (pairs of query tiles x key range)
 
   // prefill
   int n_chunks, chunk_rows, n_win;

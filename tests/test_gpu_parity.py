@@ -144,6 +144,38 @@ def test_decode_nan_padding_is_masked():
         assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= P.LSE_MAX_ABS
 
 
+def test_running_max_jumps_between_tiles():
+    """Logits that grow by far more than 2^8 from tile to tile force the
+    rescale of O (and the redo of a tile's probabilities) on every tile."""
+    cfg = wl.scaled(wl.TINY, n_chunks=2, chunk_size=700, n_keep=200, n_select=2, n_win=16,
+                    n_resp=48)
+    req = wl.make_request(cfg, 0)
+    rows = cfg.chunk_size + 1
+    ramp = torch.linspace(0.2, 6.0, rows).repeat(cfg.n_chunks)[:, None, None]
+    req["k"] = (req["k"].float() * ramp).to(torch.bfloat16)
+    res = P.run_prefill(cfg, req)
+    assert int(res["dev_err"][0]) == 0
+    o_ref = orc.chunk_attention(f64(req["q"]), f64(req["k"]), f64(req["v"]), cfg.n_chunks,
+                                cfg.chunk_size, cfg.sm_scale)
+    P.assert_close_out(res["out"].double().numpy(), o_ref, "prefill out (ramped keys)")
+    s_ref = orc.window_scores(f64(req["q_win"]), f64(req["k"]), cfg.n_chunks, cfg.chunk_size,
+                              cfg.sm_scale)
+    P.check_kept(res["kept_idx"].numpy(), s_ref, cfg.n_keep)
+    # decode: live keys much larger than the pool's so the last split tile jumps
+    pk, pv, table = P.oracle_pool(cfg, req, orc.top_b(s_ref, cfg.n_keep), res["slot_row"],
+                                  res["pool_rows"])
+    sel = np.array([1, 0], dtype=np.int32)
+    ql, kl, vl = wl.live_block(req, wl.make_step(cfg, 0, 0))
+    kl = (kl.float() * 8.0).to(torch.bfloat16)
+    o_ref, lse_ref = orc.decode_attention(f64(ql), f64(kl), f64(vl), pk, pv, table, sel, cfg.sm_scale)
+    for n_splits in (1, 2):
+        out, lse = api.decode_attention(P.cuda(ql), P.cuda(kl), P.cuda(vl), P.cuda(P.bf16_of(pk)),
+                                        P.cuda(P.bf16_of(pv)), P.cuda(torch.from_numpy(table)),
+                                        P.cuda(torch.from_numpy(sel)), n_splits=n_splits)
+        P.assert_close_out(out.cpu().double().numpy(), o_ref, "decode out (jumping max)")
+        assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= P.LSE_MAX_ABS
+
+
 def test_decode_batched_shared_pool():
     """Three sequences with different chunk sizes and live lengths in one pool."""
     cfgs = [wl.scaled(wl.TINY, chunk_size=c, n_keep=b, n_select=k, n_resp=r, n_chunks=n)
