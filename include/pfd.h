@@ -198,6 +198,40 @@ pfd_status pfd_decode_attention(const pfd_bf16* q, const pfd_bf16* k_self,
                                 int32_t* dev_err, void* workspace, size_t workspace_bytes,
                                 pfd_stream_t stream);
 
+/* Bytes of the static device scratch used by
+ * pfd_decode_attention_static_scratch (per device). */
+#define PFD_DECODE_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * pfd_decode_attention without a workspace argument.  The pages describe no
+ * such call: it is a library convenience for callers that cannot allocate
+ * device memory when they call (a host program that links only this library
+ * and holds no device allocator; a hook inside another runtime that owns and
+ * accounts every device byte and forbids allocation there).
+ *
+ * The split-KV partials go to one statically allocated device buffer of
+ * PFD_DECODE_STATIC_SCRATCH_BYTES per device instead of caller workspace;
+ * nothing is allocated.  The first call made on a device, with that device
+ * current, looks up that device's copy of the buffer (cudaGetSymbolAddress)
+ * and caches the address; make that first call before any stream capture
+ * begins.  Every call on a device shares the buffer, so calls whose work
+ * overlaps on the GPU (streams with no ordering between them) race and give
+ * undefined results; calls on one stream run in order and are safe.
+ *
+ * Arguments, results and device-side errors are those of
+ * pfd_decode_attention.  Returns PFD_ERR_UNSUPPORTED, with nothing launched,
+ * when these sizes need more than PFD_DECODE_STATIC_SCRATCH_BYTES of
+ * workspace (pfd_decode_workspace(...) reports the need), and PFD_ERR_CUDA
+ * when the buffer's address cannot be found on the current device.
+ */
+pfd_status pfd_decode_attention_static_scratch(
+    const pfd_bf16* q, const pfd_bf16* k_self, const pfd_bf16* v_self, const int32_t* cu_lq,
+    const int32_t* cu_lq_host, const pfd_bf16* pool_k, const pfd_bf16* pool_v, int64_t pool_rows,
+    const pfd_chunk_entry* table, int32_t table_len, const int32_t* sel, const int32_t* cu_k,
+    const int32_t* cu_k_host, int batch, int Hq, int Hkv, int D, int max_chunk_len,
+    float sm_scale, int n_splits, pfd_bf16* out, float* lse, int32_t* dev_err,
+    pfd_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* pfd_status_string(pfd_status status);
 

@@ -14,6 +14,9 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpfd.so")
 PFD_OK = 0
 STATUS_NAMES = {0: "PFD_OK", 1: "PFD_ERR_INVALID_ARG", 2: "PFD_ERR_UNSUPPORTED", 3: "PFD_ERR_CUDA"}
 
+# PFD_DECODE_STATIC_SCRATCH_BYTES of include/pfd.h
+DECODE_STATIC_SCRATCH_BYTES = 32 << 20
+
 DEVERR_TABLE, DEVERR_SEL, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_SHAPE = 1, 2, 4, 8, 16
 
 # (restype, argtypes) of every exported symbol, in the order of include/pfd.h.
@@ -32,6 +35,9 @@ SIGNATURES = {
     "pfd_decode_workspace": (_SZ, [_I, _P, _P, _I, _I, _I, _I, _I]),
     "pfd_decode_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _P, ctypes.c_int32, _P, _P, _P,
                                   _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _SZ, _P]),
+    "pfd_decode_attention_static_scratch": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _P,
+                                                 ctypes.c_int32, _P, _P, _P, _I, _I, _I, _I, _I,
+                                                 _F, _I, _P, _P, _P, _P]),
     "pfd_status_string": (ctypes.c_char_p, [_I]),
     "pfd_abi_version": (_I, []),
 }
@@ -141,3 +147,24 @@ def pfd_decode_attention(q, k_self, v_self, cu_lq, cu_lq_host, pool_k, pool_v, p
         _ptr(pool_v), int(pool_rows), _ptr(table), int(table_len), _ptr(sel), _ptr(cu_k),
         ctypes.cast(b, _P), batch, Hq, Hkv, D, max_chunk_len, float(sm_scale), n_splits, _ptr(out),
         _ptr(lse), _ptr(dev_err), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def pfd_decode_attention_static_scratch(q, k_self, v_self, cu_lq, cu_lq_host, pool_k, pool_v,
+                                        pool_rows, table, table_len, sel, cu_k, cu_k_host, batch,
+                                        Hq, Hkv, D, max_chunk_len, sm_scale, n_splits, out, lse,
+                                        dev_err, stream=None):
+    """pfd_decode_attention with its split partials in the library's static
+    device scratch (no workspace argument, nothing allocated)."""
+    a, b = _host_i32(cu_lq_host), _host_i32(cu_k_host)
+    status = load().pfd_decode_attention_static_scratch(
+        _ptr(q), _ptr(k_self), _ptr(v_self), _ptr(cu_lq), ctypes.cast(a, _P), _ptr(pool_k),
+        _ptr(pool_v), int(pool_rows), _ptr(table), int(table_len), _ptr(sel), _ptr(cu_k),
+        ctypes.cast(b, _P), batch, Hq, Hkv, D, max_chunk_len, float(sm_scale), n_splits, _ptr(out),
+        _ptr(lse), _ptr(dev_err), _stream(stream))
+    if status == 2:
+        need = pfd_decode_workspace(batch, cu_lq_host, cu_k_host, Hq, Hkv, D, max_chunk_len,
+                                    n_splits)
+        if need > DECODE_STATIC_SCRATCH_BYTES:
+            raise PfdError(f"PFD_ERR_UNSUPPORTED: these sizes need {need} bytes of decode scratch, "
+                           f"more than the static {DECODE_STATIC_SCRATCH_BYTES} bytes")
+    _check(status)
