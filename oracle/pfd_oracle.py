@@ -107,6 +107,27 @@ def chunk_attention(q, k, v, n_chunks, chunk_size, sm_scale, counter=None):
     return out
 
 
+def chunk_attention_rows(q, k, v, chunk_size, rows, sm_scale):
+    """[M1] The chunk-attention output at the listed prefix rows only.
+
+    rows: global row indices into q.  Row r belongs to chunk r // (C+1) and
+    attends to that chunk's C+1 rows, exactly as in chunk_attention; this
+    evaluates the same definition at fewer rows, so that sampled rows of a
+    large prefix can be checked.  Returns [len(rows), Hq, D] fp64.
+    """
+    span = chunk_size + 1
+    n_q_heads, head_dim = q.shape[1], q.shape[2]
+    group = n_q_heads // k.shape[1]
+    out = np.empty((len(rows), n_q_heads, head_dim), dtype=np.float64)
+    for i, r in enumerate(rows):
+        lo = (int(r) // span) * span
+        for h in range(n_q_heads):
+            g = h // group
+            logits = sm_scale * (q[r, h, :][None, :] @ k[lo:lo + span, g, :].T)
+            out[i, h, :] = (softmax_rows(logits) @ v[lo:lo + span, g, :])[0]
+    return out
+
+
 def window_scores(q_win, k, n_chunks, chunk_size, sm_scale, counter=None):
     """[M2] + R2: cumulative attention weight each chunk row receives.
 

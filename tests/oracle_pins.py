@@ -43,6 +43,10 @@ def check_chunk_attention(orc, seed=1, n=3, c=6, hq=4, hkv=2, d=8):
         g = h // (hq // hkv)
         want = sdpa(q[:, h], k[:, g], v[:, g], mask, scale)
         assert np.max(np.abs(got[:, h] - want)) < 1e-12, "chunk attention != masked dense SDPA"
+        some = [0, c, c + 1, rows - 1, rows // 2]
+        at_rows = orc.chunk_attention_rows(q, k, v, c, some, scale)
+        assert np.max(np.abs(at_rows[:, h] - want[some])) < 1e-12, \
+            "chunk attention at sampled rows != masked dense SDPA"
 
 
 # ------------------------------------------------------------ window scores --
