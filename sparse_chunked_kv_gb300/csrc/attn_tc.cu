@@ -63,8 +63,17 @@ __device__ __forceinline__ uint32_t tmem_o_col(int x) { return x ? 384u : 256u; 
 
 enum ItemKind : int { kChunk = 0, kWindow = 1, kDecode = 2 };
 
+// Valid rows of a 16-row key group, one byte per group: 16 for a full
+// group, 0 for a group past the tile's end, n (1..15) for the last group of a
+// segment loaded from its first row (rows n..15 lie past the segment), and
+// kShifted | n for that group loaded as the 16 rows ending at the segment's
+// end (rows 0..15-n repeat keys of the previous group).  A segment of 16 or
+// more rows is always loaded shifted, so every V row the tensor core reads
+// belongs to the segment.
+constexpr uint32_t kShifted = 0x80u;
+
 struct TileMeta {
-  uint32_t nvalid_lo;  // valid rows of groups 0..3, one byte each
+  uint32_t nvalid_lo;  // valid-row codes of groups 0..3, one byte each
   uint32_t nvalid_hi;  // groups 4..7
   int32_t ngroups;     // 0 only for the single tile of an empty item
   int32_t last;        // 1 on the last tile of an item
@@ -325,10 +334,12 @@ attention_kernel(const __grid_constant__ AttnParams p) {
           for (; n_tiles > 0 && ng < kGroupsPerTile && g_cur < g_hi; ++ng, ++g_cur) {
             const int len = seg_len[seg];
             const int nv = min(kGroupRows, len - gofs * kGroupRows);
+            const bool shifted = nv < kGroupRows && len >= kGroupRows;
             tens[ng] = (it.kind == kDecode && seg == nseg - 1) ? 1 : 0;
-            rows[ng] = seg_row[seg] + gofs * kGroupRows;
-            if (ng < 4) nv_lo |= static_cast<uint32_t>(nv) << (8 * ng);
-            else nv_hi |= static_cast<uint32_t>(nv) << (8 * (ng - 4));
+            rows[ng] = seg_row[seg] + (shifted ? len - kGroupRows : gofs * kGroupRows);
+            const uint32_t code = static_cast<uint32_t>(nv) | (shifted ? kShifted : 0u);
+            if (ng < 4) nv_lo |= code << (8 * ng);
+            else nv_hi |= code << (8 * (ng - 4));
             ++gofs;
             if (gofs * kGroupRows >= len) {
               gofs = 0;
@@ -443,13 +454,17 @@ attention_kernel(const __grid_constant__ AttnParams p) {
           }
           mma_commit(&sh.s_full[x]);
         };
-        // Rows of a ragged group past its segment may hold anything (another
-        // slot, padding): zero them in V so that 0 * v stays 0 in PV.
+        // Rows of an unshifted ragged group past its (shorter than 16 rows)
+        // segment may hold anything (another slot, padding): zero them in V so
+        // that 0 * v stays 0 in PV.
         auto fix_v = [&](const TileMeta& m, uint32_t vs) {
           uint8_t* v_tile = smem + L::kRing0 + vs * L::kTileBytes;
+          bool wrote = false;
           for (int grp = 0; grp < m.ngroups; ++grp) {
             const uint32_t w = grp < 4 ? m.nvalid_lo : m.nvalid_hi;
             const int nv = static_cast<int>((w >> (8 * (grp & 3))) & 0xFFu);
+            if (nv & kShifted) continue;   // all 16 rows belong to the segment
+            wrote = wrote || nv < kGroupRows;
             for (int r = nv; r < kGroupRows; ++r)
               for (int pn = 0; pn < D / 64; ++pn) {
                 uint4* dst = reinterpret_cast<uint4*>(v_tile + pn * kPanelBytes + (grp * kGroupRows + r) * 128);
@@ -457,7 +472,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
                 for (int c16 = 0; c16 < 8; ++c16) dst[c16] = make_uint4(0u, 0u, 0u, 0u);
               }
           }
-          fence_proxy_async_smem();
+          if (wrote) fence_proxy_async_smem();
         };
         auto issue_pv = [&](int x, int ng, uint32_t vs, bool first) {
           const uint32_t v_addr = s_base + L::kRing0 + vs * L::kTileBytes;
@@ -588,15 +603,21 @@ attention_kernel(const __grid_constant__ AttnParams p) {
           return static_cast<int>((w >> (8 * (grp & 3))) & 0xFFu);
         };
 
-        // Ragged tiles: logits of rows past a group's valid count become -inf
-        // (their exp2 is then 0), so one code path serves every tile.
+        // Ragged tiles: logits of key rows outside a group's valid rows become
+        // -inf (their exp2 is then 0): the rows past the count, or for a
+        // shifted group the leading rows that repeat the previous group's keys.
         auto mask_half = [&](uint32_t (&sr)[2][32], int half) {
 #pragma unroll
           for (int gq = 0; gq < 4; ++gq) {
-            const int nv = nv_of(half * 4 + gq);
+            const int code = nv_of(half * 4 + gq);
+            if (code != kGroupRows) {   // warp-uniform: ragged, shifted or absent
+              const bool sh_grp = (code & kShifted) != 0;
+              const int lo = sh_grp ? kGroupRows - (code & 0x1f) : 0;
+              const int hi = sh_grp ? kGroupRows : code;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (i >= nv) sr[gq >> 1][(gq & 1) * 16 + i] = __float_as_uint(-INFINITY);
+              for (int i = 0; i < 16; ++i)
+                if (i < lo || i >= hi) sr[gq >> 1][(gq & 1) * 16 + i] = __float_as_uint(-INFINITY);
+            }
           }
         };
 
@@ -716,25 +737,36 @@ attention_kernel(const __grid_constant__ AttnParams p) {
               for (int i = 0; i < 32; ++i) o[i] = 0u;
             }
             if (!row_ok) continue;
+            // Each lane writes its own row; whole 32-byte sectors where the
+            // destination allows it (half the store instructions, no
+            // half-filled sectors).
             if (final_out) {
               uint32_t packed[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i)
                 packed[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
                                         __uint_as_float(o[2 * i + 1]) * inv_l);
-              uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * p.Hq + head) * D + ch * 32);
+              bf16* dst = p.out + (tok * p.Hq + head) * D + ch * 32;
+              if (p.out_v8) {
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-                dst[q4] = make_uint4(packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2],
-                                     packed[4 * q4 + 3]);
+                for (int q8 = 0; q8 < 2; ++q8)
+                  st_global_v8(dst + q8 * 16, packed[8 * q8], packed[8 * q8 + 1], packed[8 * q8 + 2],
+                               packed[8 * q8 + 3], packed[8 * q8 + 4], packed[8 * q8 + 5],
+                               packed[8 * q8 + 6], packed[8 * q8 + 7]);
+              } else {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                  reinterpret_cast<uint4*>(dst)[q4] = make_uint4(
+                      packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2], packed[4 * q4 + 3]);
+              }
             } else {
-              float4* dst = reinterpret_cast<float4*>(
-                  p.part_acc +
-                  ((static_cast<long long>(it.split) * p.total_lq + tok) * p.Hq + head) * D + ch * 32);
+              // Workspace partials: 256-byte aligned base, 128-byte row chunks.
+              float* dst = p.part_acc +
+                  ((static_cast<long long>(it.split) * p.total_lq + tok) * p.Hq + head) * D + ch * 32;
 #pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4)
-                dst[q4] = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
-                                      __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
+              for (int q8 = 0; q8 < 4; ++q8)
+                st_global_v8(dst + q8 * 8, o[8 * q8], o[8 * q8 + 1], o[8 * q8 + 2], o[8 * q8 + 3],
+                             o[8 * q8 + 4], o[8 * q8 + 5], o[8 * q8 + 6], o[8 * q8 + 7]);
             }
           }
           if (row_ok && it.kind == kDecode) {

@@ -13,28 +13,68 @@ namespace pfd {
 namespace {
 
 constexpr int kMergeThreads = 256;
+constexpr int kAccBatch = 8;   // split partials of acc loaded per round trip
 constexpr float kLn2 = 0.69314718055994530942f;
 
+// One warp per (row, head).  Lane s loads split s's (m, l) (lanes loop when
+// S > 32), so the statistics of every split arrive in one round trip; the
+// acc rows of up to kAccBatch splits are loaded in the same round trip, each
+// lane holding 4 consecutive columns of D.
 __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergeParams p) {
   const long long pair = static_cast<long long>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
   const long long n_pairs = static_cast<long long>(p.total_lq) * p.Hq;
   if (pair >= n_pairs) return;
   const int lane = threadIdx.x & 31;
-  float big_m = -INFINITY;
-  for (int s = 0; s < p.n_splits; ++s) big_m = fmaxf(big_m, p.part_m[s * n_pairs + pair]);
-  float big_l = 0.0f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int S = p.n_splits;
   const bool active = lane * 4 < p.D;
-  for (int s = 0; s < p.n_splits; ++s) {
-    const float m = p.part_m[s * n_pairs + pair];
-    const float w = (m == -INFINITY) ? 0.0f : ex2_approx(m - big_m);
-    big_l = fmaf(w, p.part_l[s * n_pairs + pair], big_l);
-    if (active && w != 0.0f) {
-      const float4 a = *reinterpret_cast<const float4*>(p.part_acc + (s * n_pairs + pair) * p.D + lane * 4);
-      acc.x = fmaf(w, a.x, acc.x);
-      acc.y = fmaf(w, a.y, acc.y);
-      acc.z = fmaf(w, a.z, acc.z);
-      acc.w = fmaf(w, a.w, acc.w);
+  const float* acc_base = p.part_acc + pair * p.D + lane * 4;
+  const long long acc_stride = n_pairs * p.D;
+
+  float4 a[kAccBatch];
+#pragma unroll
+  for (int s = 0; s < kAccBatch; ++s)
+    if (active && s < S) a[s] = __ldg(reinterpret_cast<const float4*>(acc_base + s * acc_stride));
+
+  // Running max over the splits, then each split's weight 2^(m_s - M).
+  float m_lane = -INFINITY, l_lane = 0.0f;   // lane's own splits s = lane, lane + 32
+  float m_hi = -INFINITY, l_hi = 0.0f;
+  if (lane < S) {
+    m_lane = __ldg(p.part_m + lane * n_pairs + pair);
+    l_lane = __ldg(p.part_l + lane * n_pairs + pair);
+  }
+  if (lane + 32 < S) {
+    m_hi = __ldg(p.part_m + (lane + 32) * n_pairs + pair);
+    l_hi = __ldg(p.part_l + (lane + 32) * n_pairs + pair);
+  }
+  float big_m = fmaxf(m_lane, m_hi);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) big_m = fmaxf(big_m, __shfl_xor_sync(0xFFFFFFFFu, big_m, o));
+  const float w_lane = (m_lane == -INFINITY) ? 0.0f : ex2_approx(m_lane - big_m);
+  const float w_hi = (m_hi == -INFINITY) ? 0.0f : ex2_approx(m_hi - big_m);
+  float big_l = w_lane * l_lane + w_hi * l_hi;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) big_l += __shfl_xor_sync(0xFFFFFFFFu, big_l, o);
+
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < S; s0 += kAccBatch) {
+    if (s0 > 0) {
+#pragma unroll
+      for (int s = 0; s < kAccBatch; ++s)
+        if (active && s0 + s < S)
+          a[s] = __ldg(reinterpret_cast<const float4*>(acc_base + (s0 + s) * acc_stride));
+    }
+#pragma unroll
+    for (int s = 0; s < kAccBatch; ++s) {
+      const int src = (s0 + s) & 31;
+      const float wl = __shfl_sync(0xFFFFFFFFu, w_lane, src);
+      const float wh = __shfl_sync(0xFFFFFFFFu, w_hi, src);
+      const float w = (s0 + s) < 32 ? wl : wh;
+      if (active && s0 + s < S && w != 0.0f) {
+        acc.x = fmaf(w, a[s].x, acc.x);
+        acc.y = fmaf(w, a[s].y, acc.y);
+        acc.z = fmaf(w, a[s].z, acc.z);
+        acc.w = fmaf(w, a[s].w, acc.w);
+      }
     }
   }
   const float inv = big_l > 0.0f ? 1.0f / big_l : 0.0f;

@@ -196,6 +196,7 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
   ap.q = reinterpret_cast<const bf16*>(q);
   ap.q_win = reinterpret_cast<const bf16*>(q_win);
   ap.out = reinterpret_cast<bf16*>(out);
+  ap.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
   ap.win_m = reinterpret_cast<float*>(wsb + ws.win_m);
   ap.win_l = reinterpret_cast<float*>(wsb + ws.win_l);
   ap.dev_err = dev_err;
@@ -388,6 +389,7 @@ pfd_status pfd_decode_attention(const pfd_bf16* q, const pfd_bf16* k_self,
     mt_max = std::max(mt_max, ceil_div(cu_lq_host[b + 1] - cu_lq_host[b], Tq));
   ap.q = reinterpret_cast<const bf16*>(q);
   ap.out = reinterpret_cast<bf16*>(out);
+  ap.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
   ap.lse = lse;
   ap.part_m = S > 1 ? reinterpret_cast<float*>(wsb + ws.part_m) : nullptr;
   ap.part_l = S > 1 ? reinterpret_cast<float*>(wsb + ws.part_l) : nullptr;

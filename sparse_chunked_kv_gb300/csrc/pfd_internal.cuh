@@ -77,6 +77,7 @@ struct AttnParams {
   int batch, mt_max, n_splits, total_lq, total_sel;
 
   float scale_log2;     // sm_scale * log2(e)
+  int out_v8;           // out is 32-byte aligned: whole-sector (32-byte) stores
 };
 
 cudaError_t launch_attention(const AttnParams& p, int grid, cudaStream_t stream);

@@ -75,6 +75,16 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity)) != 0;
 }
 
+// --------------------------------------------------------- global stores --
+// One 32-byte store (a whole sector) of 8 words; addr must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* addr, uint32_t w0, uint32_t w1, uint32_t w2,
+                                             uint32_t w3, uint32_t w4, uint32_t w5, uint32_t w6,
+                                             uint32_t w7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(addr), "r"(w0),
+               "r"(w1), "r"(w2), "r"(w3), "r"(w4), "r"(w5), "r"(w6), "r"(w7)
+               : "memory");
+}
+
 // -------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -280,3 +280,36 @@ def test_end_to_end_tiny_every_step():
                                               cfg.sm_scale)
         P.assert_close_out(out.cpu().double().numpy(), o_ref, f"decode step {t}")
         assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= P.LSE_MAX_ABS
+
+
+def test_outputs_aligned_to_16_but_not_32_bytes():
+    """Output buffers that start 16 bytes past a 32-byte boundary take the
+    16-byte store path; results are the same as the oracle's."""
+    cfg = wl.scaled(wl.CTX_8K, n_chunks=2, chunk_size=100, n_keep=20, n_select=2, n_resp=30)
+    req = wl.make_request(cfg, 0)
+    rows, hq, d = req["q"].shape
+    base = torch.empty(rows * hq * d + 64, dtype=torch.bfloat16, device="cuda")
+    off = (32 - base.data_ptr() % 32) // 2 + 8      # element offset: 16 bytes past a 32-byte boundary
+    out = base[off:off + rows * hq * d].view(rows, hq, d)
+    assert out.data_ptr() % 32 == 16
+    slot = req["slot_row"].to(torch.int32)
+    res = api.chunk_prefill(P.cuda(req["q"]), P.cuda(req["k"]), P.cuda(req["v"]), P.cuda(req["q_win"]),
+                            cfg.n_chunks, cfg.chunk_size, cfg.n_keep, P.cuda(slot), cfg.pool_rows,
+                            out=out)
+    torch.cuda.synchronize()
+    assert int(res["dev_err"][0]) == 0
+    o_ref = orc.chunk_attention(f64(req["q"]), f64(req["k"]), f64(req["v"]), cfg.n_chunks,
+                                cfg.chunk_size, cfg.sm_scale)
+    P.assert_close_out(out.cpu().double().numpy(), o_ref, "prefill out (16-byte aligned)")
+    _, pk, pv, table, sel, ql, kl, vl = _decode_inputs(cfg)
+    o_ref, _ = orc.decode_attention(f64(ql), f64(kl), f64(vl), pk, pv, table, sel, cfg.sm_scale)
+    lq = ql.shape[0]
+    base = torch.empty(lq * hq * d + 64, dtype=torch.bfloat16, device="cuda")
+    off = (32 - base.data_ptr() % 32) // 2 + 8
+    dout = base[off:off + lq * hq * d].view(lq, hq, d)
+    for n_splits in (1, 3):
+        api.decode_attention(P.cuda(ql), P.cuda(kl), P.cuda(vl), P.cuda(P.bf16_of(pk)),
+                             P.cuda(P.bf16_of(pv)), P.cuda(torch.from_numpy(table)),
+                             P.cuda(torch.from_numpy(sel)), n_splits=n_splits, out=dout)
+        torch.cuda.synchronize()
+        P.assert_close_out(dout.cpu().double().numpy(), o_ref, "decode out (16-byte aligned)")
