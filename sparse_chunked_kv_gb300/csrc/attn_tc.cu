@@ -296,6 +296,9 @@ attention_kernel(const __grid_constant__ AttnParams p) {
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // Everything above touched only this CTA's shared memory and TMEM; global
+  // inputs may come from the previous kernel on the stream.
+  grid_dependency_wait();
   const uint32_t tmem = sh.tmem_base;
   const int n_items = p.n_items;
 
@@ -792,6 +795,9 @@ attention_kernel(const __grid_constant__ AttnParams p) {
 
   tc_fence_before_sync();
   __syncthreads();
+  // Only now may the next kernel's CTAs be scheduled: launched earlier they
+  // would sit on the SMs (registers, warp slots) while this grid still works.
+  grid_dependents_launch();
   if (tid == 0 && sh.failed != 0) raise_dev_err(p.dev_err, PFD_DEVERR_TIMEOUT);
   if (warp == kMmaWarp) {
     tc_fence_after_sync();
@@ -812,11 +818,11 @@ cudaError_t launch_attention(const AttnParams& p, int grid, cudaStream_t stream)
   if (p.D == 64) {
     err = ensure_smem_limit(reinterpret_cast<const void*>(attention_kernel<64>), static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    attention_kernel<64><<<grid, kThreads, smem, stream>>>(p);
+    return launch_pdl(attention_kernel<64>, dim3(grid), dim3(kThreads), smem, stream, p);
   } else {
     err = ensure_smem_limit(reinterpret_cast<const void*>(attention_kernel<128>), static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    attention_kernel<128><<<grid, kThreads, smem, stream>>>(p);
+    return launch_pdl(attention_kernel<128>, dim3(grid), dim3(kThreads), smem, stream, p);
   }
   return cudaGetLastError();
 }

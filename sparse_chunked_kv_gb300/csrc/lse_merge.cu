@@ -21,6 +21,7 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // acc rows of up to kAccBatch splits are loaded in the same round trip, each
 // lane holding 4 consecutive columns of D.
 __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergeParams p) {
+  grid_dependency_wait();
   const long long pair = static_cast<long long>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
   const long long n_pairs = static_cast<long long>(p.total_lq) * p.Hq;
   if (pair >= n_pairs) return;
@@ -86,6 +87,9 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergePar
   }
   if (lane == 0 && p.lse != nullptr)
     p.lse[pair] = big_l > 0.0f ? (big_m + log2f(big_l)) * kLn2 : -INFINITY;
+  // Late trigger: a next attention grid scheduled early would hold registers
+  // that the merge's later waves need.
+  grid_dependents_launch();
 }
 
 }  // namespace
@@ -94,8 +98,8 @@ cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream) {
   const long long n_pairs = static_cast<long long>(p.total_lq) * p.Hq;
   const long long blocks = (n_pairs + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
   if (blocks <= 0) return cudaSuccess;
-  lse_merge_kernel<<<static_cast<unsigned>(blocks), kMergeThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(lse_merge_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kMergeThreads), 0,
+                    stream, p);
 }
 
 }  // namespace pfd

@@ -7,6 +7,7 @@
 
 #include <cstdint>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "pfd.h"
@@ -151,6 +152,40 @@ inline cudaError_t ensure_smem_limit(const void* func, int bytes) {
   err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (err == cudaSuccess) done.push_back({{func, dev}, bytes});
   return err;
+}
+
+// Launch that lets the kernel start while the previous kernel on the stream
+// is still finishing (programmatic dependent launch): its CTAs may be
+// scheduled early and run their prologue, and each one calls
+// grid_dependency_wait() before it touches global memory, which returns once
+// the previous grid has completed and its writes are visible.  Every kernel of
+// this library is launched this way and waits before its first global access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Waits until the grid launched before this one on the stream has completed
+// and its memory writes are visible (a no-op without a programmatic launch).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next grid on the stream be scheduled now; it still waits in
+// grid_dependency_wait() for this grid to complete.
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }

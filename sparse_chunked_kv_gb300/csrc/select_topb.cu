@@ -59,6 +59,8 @@ topb_compact_kernel(const TopBParams p) {
   __shared__ uint32_t sel_prefix;
   __shared__ int sel_remaining;
 
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int j = blockIdx.x;
   const int part = blockIdx.y;
@@ -203,6 +205,8 @@ select_kernel(const float* __restrict__ s_i, const float* __restrict__ s_p,
               const int32_t* __restrict__ cu_n, const int32_t* __restrict__ cu_k, int n_scalar,
               int k_scalar, int max_n, int32_t* __restrict__ sel, float* __restrict__ s_out) {
   extern __shared__ uint32_t keys[];
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int b = blockIdx.x;
   const int off = cu_n ? cu_n[b] : 0;
   const int n = cu_n ? cu_n[b + 1] - off : n_scalar;
@@ -234,8 +238,7 @@ cudaError_t launch_topb_compact(const TopBParams& p, cudaStream_t stream) {
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(topb_compact_kernel), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   dim3 grid(p.n_chunks, p.copy_splits);
-  topb_compact_kernel<<<grid, kTopBThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(topb_compact_kernel, grid, dim3(kTopBThreads), smem, stream, p);
 }
 
 cudaError_t launch_select(const float* s_i, const float* s_p, const int32_t* cu_n,
@@ -244,9 +247,8 @@ cudaError_t launch_select(const float* s_i, const float* s_p, const int32_t* cu_
   const size_t smem = static_cast<size_t>(max_n) * 4;
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  select_kernel<<<batch, kSelectThreads, smem, stream>>>(s_i, s_p, cu_n, cu_k, n_scalar, k_scalar,
-                                                         max_n, sel, s_out);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel, dim3(batch), dim3(kSelectThreads), smem, stream, s_i, s_p, cu_n,
+                    cu_k, n_scalar, k_scalar, max_n, sel, s_out);
 }
 
 }  // namespace pfd

@@ -33,6 +33,8 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
   __shared__ int failed;
   __shared__ __align__(16) float b_sh[kMaxWindowRows];   // per column: m_n + log2(l_n)
 
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int bid = blockIdx.x;
   const int kt = bid % p.k_tiles;
@@ -173,11 +175,11 @@ cudaError_t launch_window_scores(const WinScoreParams& p, cudaStream_t stream) {
   if (p.D == 64) {
     err = ensure_smem_limit(reinterpret_cast<const void*>(window_score_kernel<64>), static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    window_score_kernel<64><<<grid, kThreads, smem, stream>>>(p);
+    return launch_pdl(window_score_kernel<64>, dim3(grid), dim3(kThreads), smem, stream, p);
   } else {
     err = ensure_smem_limit(reinterpret_cast<const void*>(window_score_kernel<128>), static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    window_score_kernel<128><<<grid, kThreads, smem, stream>>>(p);
+    return launch_pdl(window_score_kernel<128>, dim3(grid), dim3(kThreads), smem, stream, p);
   }
   return cudaGetLastError();
 }
