@@ -316,79 +316,92 @@ attention_kernel(const __grid_constant__ AttnParams p) {
       }
       const bool with_pv = it.kind != kWindow;
       const int nseg = load_segments(p, it, seg_row, seg_len, seg_g0, lane);
-      if (lane == 0) {
-        const long long total = seg_g0[nseg];
-        const int n_splits = it.kind == kDecode ? p.n_splits : 1;
-        const int g_lo = static_cast<int>(total * it.split / n_splits);
-        const int g_hi = static_cast<int>(total * (it.split + 1) / n_splits);
-        const int n_tiles = (g_hi - g_lo + kGroupsPerTile - 1) / kGroupsPerTile;
-        int seg = 0;
-        while (seg + 1 < nseg && seg_g0[seg + 1] <= g_lo) ++seg;
-        int gofs = g_lo - seg_g0[seg];
-        int g_cur = g_lo;
-        const int tiles_to_publish = n_tiles > 0 ? n_tiles : 1;
-        for (int j = 0; ok && j < tiles_to_publish; ++j) {
-          int tens[kGroupsPerTile];
-          int rows[kGroupsPerTile];
-          uint32_t nv_lo = 0, nv_hi = 0;
-          int ng = 0;
-          const bool one_box = n_tiles > 0 && (g_hi - g_cur >= kGroupsPerTile) &&
-                               ((gofs + kGroupsPerTile) * kGroupRows <= seg_len[seg]);
-          for (; n_tiles > 0 && ng < kGroupsPerTile && g_cur < g_hi; ++ng, ++g_cur) {
-            const int len = seg_len[seg];
-            const int nv = min(kGroupRows, len - gofs * kGroupRows);
-            const bool shifted = nv < kGroupRows && len >= kGroupRows;
-            tens[ng] = (it.kind == kDecode && seg == nseg - 1) ? 1 : 0;
-            rows[ng] = seg_row[seg] + (shifted ? len - kGroupRows : gofs * kGroupRows);
-            const uint32_t code = static_cast<uint32_t>(nv) | (shifted ? kShifted : 0u);
-            if (ng < 4) nv_lo |= code << (8 * ng);
-            else nv_hi |= code << (8 * (ng - 4));
-            ++gofs;
-            if (gofs * kGroupRows >= len) {
-              gofs = 0;
-              ++seg;
-              while (seg < nseg && seg_len[seg] == 0) ++seg;
-            }
+      const long long total = seg_g0[nseg];
+      const int n_splits = it.kind == kDecode ? p.n_splits : 1;
+      const int g_lo = static_cast<int>(total * it.split / n_splits);
+      const int g_hi = static_cast<int>(total * (it.split + 1) / n_splits);
+      const int n_tiles = (g_hi - g_lo + kGroupsPerTile - 1) / kGroupsPerTile;
+      const int tiles_to_publish = n_tiles > 0 ? n_tiles : 1;
+      for (int j = 0; ok && j < tiles_to_publish; ++j) {
+        // Lanes 0..ng-1 each place one 16-row key group of the tile: its
+        // segment (binary search in the group prefix sums), source row,
+        // tensor and valid-row code.
+        const int g0 = g_lo + j * kGroupsPerTile;
+        const int ng = n_tiles > 0 ? min(kGroupsPerTile, g_hi - g0) : 0;
+        int row = 0, t = 0;
+        uint32_t code = 0;
+        if (lane < ng) {
+          const int g = g0 + lane;
+          int lo = 0, hi = nseg;   // seg_g0[lo] <= g < seg_g0[hi]
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (seg_g0[mid] <= g) lo = mid;
+            else hi = mid;
           }
-          // Metadata slot tile_ctr % kRing: every consumer must have read the
-          // tile published there kRing tiles ago.
-          const int ms = tile_ctr % kRing;
-          if (tile_ctr >= kRing && !mbar_wait(&sh.meta_empty[ms], ((tile_ctr / kRing) - 1) & 1)) {
-            ok = false;
-            break;
-          }
+          const int len = seg_len[lo];
+          const int gofs = g - seg_g0[lo];
+          const int nv = min(kGroupRows, len - gofs * kGroupRows);
+          const bool shifted = nv < kGroupRows && len >= kGroupRows;
+          t = (it.kind == kDecode && lo == nseg - 1) ? 1 : 0;
+          row = seg_row[lo] + (shifted ? len - kGroupRows : gofs * kGroupRows);
+          code = static_cast<uint32_t>(nv) | (shifted ? kShifted : 0u);
+        }
+        uint32_t packed = lane < kGroupsPerTile ? code << (8 * (lane & 3)) : 0u;
+        packed |= __shfl_xor_sync(0xFFFFFFFFu, packed, 1);
+        packed |= __shfl_xor_sync(0xFFFFFFFFu, packed, 2);
+        const uint32_t nv_lo = __shfl_sync(0xFFFFFFFFu, packed, 0);
+        const uint32_t nv_hi = __shfl_sync(0xFFFFFFFFu, packed, 4);
+        // Runs: group k continues group k-1's run when it is the next 16 rows
+        // of the same tensor.  A lane that starts a run loads the whole run,
+        // one box per set bit of its length (16..128 rows).
+        const int prev_row = __shfl_up_sync(0xFFFFFFFFu, row, 1);
+        const int prev_t = __shfl_up_sync(0xFFFFFFFFu, t, 1);
+        const bool cont = lane > 0 && lane < ng && t == prev_t && row == prev_row + kGroupRows;
+        const uint32_t cont_mask = __ballot_sync(0xFFFFFFFFu, cont);
+        const bool starts = lane < ng && !cont;
+        const int run_len = starts ? __ffs(~(cont_mask >> (lane + 1))) : 0;   // 1 + continuing groups
+
+        // Metadata slot tile_ctr % kRing: every consumer must have read the
+        // tile published there kRing tiles ago.
+        const int ms = tile_ctr % kRing;
+        if (tile_ctr >= kRing && !mbar_wait_warp(&sh.meta_empty[ms], ((tile_ctr / kRing) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
           TileMeta& m = sh.meta[ms];
           m.nvalid_lo = nv_lo;
           m.nvalid_hi = nv_hi;
           m.ngroups = ng;
           m.last = (j == tiles_to_publish - 1) ? 1 : 0;
           mbar_arrive(&sh.meta_full[ms]);
-          ++tile_ctr;
-          if (ng == 0) break;
-          const uint32_t bytes = one_box ? static_cast<uint32_t>(kBlockN) * D * 2
-                                         : static_cast<uint32_t>(ng) * kGroupRows * D * 2;
-          for (int kv = 0; kv < (with_pv ? 2 : 1); ++kv) {
-            const int rs = ring_ctr % kRing;
-            if (ring_ctr >= kRing && !mbar_wait(&sh.ring_empty[rs], ((ring_ctr / kRing) - 1) & 1)) {
-              ok = false;
-              break;
-            }
-            uint8_t* dst = smem + L::kRing0 + rs * L::kTileBytes;
-            const CUtensorMap* m128 = kv ? p.tm_v128 : p.tm_k128;
-            const CUtensorMap* m16 = kv ? p.tm_v16 : p.tm_k16;
-            mbar_arrive_expect_tx(&sh.ring_full[rs], bytes);
-            if (one_box) {
-              for (int pn = 0; pn < D / 64; ++pn)
-                tma_load_3d(dst + pn * kPanelBytes, &m128[tens[0]], &sh.ring_full[rs], pn * 64, it.g,
-                            rows[0]);
-            } else {
-              for (int k = 0; k < ng; ++k)
-                for (int pn = 0; pn < D / 64; ++pn)
-                  tma_load_3d(dst + pn * kPanelBytes + k * 2048, &m16[tens[k]], &sh.ring_full[rs],
-                              pn * 64, it.g, rows[k]);
-            }
-            ++ring_ctr;
+        }
+        ++tile_ctr;
+        if (ng == 0) break;
+        const uint32_t bytes = static_cast<uint32_t>(ng) * kGroupRows * D * 2;
+        for (int kv = 0; kv < (with_pv ? 2 : 1); ++kv) {
+          const int rs = ring_ctr % kRing;
+          if (ring_ctr >= kRing && !mbar_wait_warp(&sh.ring_empty[rs], ((ring_ctr / kRing) - 1) & 1)) {
+            ok = false;
+            break;
           }
+          if (lane == 0) mbar_arrive_expect_tx(&sh.ring_full[rs], bytes);
+          __syncwarp();
+          if (starts) {
+            uint8_t* dst = smem + L::kRing0 + rs * L::kTileBytes;
+            const CUtensorMap(*maps)[2] = kv ? p.tm_v : p.tm_k;
+            int off = 0;
+#pragma unroll
+            for (int lv = kBoxLevels - 1; lv >= 0; --lv) {
+              if (run_len - off < (1 << lv)) continue;
+#pragma unroll
+              for (int pn = 0; pn < D / 64; ++pn)
+                tma_load_3d(dst + pn * kPanelBytes + (lane + off) * 2048, &maps[lv][t],
+                            &sh.ring_full[rs], pn * 64, it.g, row + off * kGroupRows);
+              off += 1 << lv;
+            }
+          }
+          ++ring_ctr;
         }
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;

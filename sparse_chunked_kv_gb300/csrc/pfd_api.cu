@@ -62,11 +62,17 @@ bool make_map(CUtensorMap* map, const void* base, long long rows, int heads, int
   return r == CUDA_SUCCESS;
 }
 
-// K or V maps of one tensor: one-group (16-row) and one-tile (128-row) boxes.
-bool make_kv_maps(CUtensorMap* m16, CUtensorMap* m128, const void* base, long long rows, int heads,
+// K or V maps of one tensor (slot t of maps[level][t]): boxes of 16, 32, 64
+// and 128 rows.
+bool make_kv_maps(CUtensorMap (*maps)[2], int t, const void* base, long long rows, int heads,
                   int D) {
-  return make_map(m16, base, rows, heads, D, 1, kGroupRows) &&
-         make_map(m128, base, rows, heads, D, 1, kBlockN);
+  for (int lv = 0; lv < kBoxLevels; ++lv)
+    if (!make_map(&maps[lv][t], base, rows, heads, D, 1, kGroupRows << lv)) return false;
+  return true;
+}
+
+void copy_kv_maps(CUtensorMap (*maps)[2], int to, int from) {
+  for (int lv = 0; lv < kBoxLevels; ++lv) maps[lv][to] = maps[lv][from];
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -179,14 +185,11 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
   const int Tq = kBlockM / G;
   AttnParams ap;
   std::memset(&ap, 0, sizeof(ap));
-  if (!make_kv_maps(&ap.tm_k16[0], &ap.tm_k128[0], k, rows, Hkv, D) ||
-      !make_kv_maps(&ap.tm_v16[0], &ap.tm_v128[0], v, rows, Hkv, D) ||
+  if (!make_kv_maps(ap.tm_k, 0, k, rows, Hkv, D) || !make_kv_maps(ap.tm_v, 0, v, rows, Hkv, D) ||
       !make_map(&ap.tm_q[0], q, rows, Hq, D, G, Tq))
     return PFD_ERR_CUDA;
-  ap.tm_k16[1] = ap.tm_k16[0];
-  ap.tm_v16[1] = ap.tm_v16[0];
-  ap.tm_k128[1] = ap.tm_k128[0];
-  ap.tm_v128[1] = ap.tm_v128[0];
+  copy_kv_maps(ap.tm_k, 1, 0);
+  copy_kv_maps(ap.tm_v, 1, 0);
   if (W > 0) {
     if (!make_map(&ap.tm_q[1], q_win, W, Hq, D, G, Tq)) return PFD_ERR_CUDA;
   } else {
@@ -224,7 +227,7 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
   if (W > 0) {
     WinScoreParams wp;
     std::memset(&wp, 0, sizeof(wp));
-    wp.tm_k = ap.tm_k128[0];
+    wp.tm_k = ap.tm_k[kBoxLevels - 1][0];
     if (!make_map(&wp.tm_qwin, q_win, W, Hq, D, G, W)) return PFD_ERR_CUDA;
     wp.q_win = ap.q_win;
     wp.win_m = ap.win_m;
@@ -368,20 +371,18 @@ pfd_status pfd_decode_attention(const pfd_bf16* q, const pfd_bf16* k_self,
   const int Tq = kBlockM / G;
   AttnParams ap;
   std::memset(&ap, 0, sizeof(ap));
-  if (!make_kv_maps(&ap.tm_k16[1], &ap.tm_k128[1], k_self, total_lq, Hkv, D) ||
-      !make_kv_maps(&ap.tm_v16[1], &ap.tm_v128[1], v_self, total_lq, Hkv, D) ||
+  if (!make_kv_maps(ap.tm_k, 1, k_self, total_lq, Hkv, D) ||
+      !make_kv_maps(ap.tm_v, 1, v_self, total_lq, Hkv, D) ||
       !make_map(&ap.tm_q[0], q, total_lq, Hq, D, G, Tq))
     return PFD_ERR_CUDA;
   ap.tm_q[1] = ap.tm_q[0];
   if (total_sel > 0) {
-    if (!make_kv_maps(&ap.tm_k16[0], &ap.tm_k128[0], pool_k, pool_rows, Hkv, D) ||
-        !make_kv_maps(&ap.tm_v16[0], &ap.tm_v128[0], pool_v, pool_rows, Hkv, D))
+    if (!make_kv_maps(ap.tm_k, 0, pool_k, pool_rows, Hkv, D) ||
+        !make_kv_maps(ap.tm_v, 0, pool_v, pool_rows, Hkv, D))
       return PFD_ERR_CUDA;
   } else {
-    ap.tm_k16[0] = ap.tm_k16[1];
-    ap.tm_v16[0] = ap.tm_v16[1];
-    ap.tm_k128[0] = ap.tm_k128[1];
-    ap.tm_v128[0] = ap.tm_v128[1];
+    copy_kv_maps(ap.tm_k, 0, 1);
+    copy_kv_maps(ap.tm_v, 0, 1);
   }
   ap.Tq = Tq;
   int mt_max = 0;

@@ -28,6 +28,7 @@ constexpr int kBlockM = 128;
 constexpr int kGroupRows = 16;
 constexpr int kGroupsPerTile = 8;
 constexpr int kBlockN = kGroupRows * kGroupsPerTile;
+constexpr int kBoxLevels = 4;      // K/V box heights 16, 32, 64, 128 rows
 constexpr int kMaxSegments = 512;   // selected chunks per sequence + the live block
 
 enum AttnMode : int { kModePrefill = 0, kModeDecode = 1 };
@@ -37,13 +38,13 @@ struct AttnParams {
   // live rows, index 1 = prefill window rows.  3-D maps over [tokens, Hq, D],
   // box = Tq tokens x G heads x 64 columns, 128-byte swizzle.
   CUtensorMap tm_q[2];
-  // Key/value tensors: index 0 = prefill K/V or the decode pool, index 1 =
-  // the decode live block.  3-D maps over [rows, Hkv, D], 128-byte swizzle,
-  // box = 16 rows (one group) or 128 rows (one tile) x 1 head x 64 columns.
-  CUtensorMap tm_k16[2];
-  CUtensorMap tm_v16[2];
-  CUtensorMap tm_k128[2];
-  CUtensorMap tm_v128[2];
+  // Key/value tensors: [box level][tensor], tensor 0 = prefill K/V or the
+  // decode pool, tensor 1 = the decode live block.  3-D maps over
+  // [rows, Hkv, D], 128-byte swizzle, box = (16 << level) rows x 1 head x 64
+  // columns: a run of consecutive 16-row groups is loaded with one box per
+  // set bit of its length.
+  CUtensorMap tm_k[kBoxLevels][2];
+  CUtensorMap tm_v[kBoxLevels][2];
 
   const bf16* q;        // prefill: chunk rows; decode: live rows
   const bf16* q_win;    // prefill: window rows
@@ -86,7 +87,7 @@ size_t attention_smem_bytes(int D);
 
 // ------------------------------------------------------- window scores --
 struct WinScoreParams {
-  CUtensorMap tm_k;         // prefill K, 128-row box (as AttnParams::tm_k128)
+  CUtensorMap tm_k;         // prefill K, 128-row box (as AttnParams::tm_k[3][0])
   CUtensorMap tm_qwin;      // q_win [W, Hq, D], box = W tokens x G heads x 64 columns
   const bf16* q_win;        // [W, Hq, D]
   const float* win_m;       // [N, Hq, W]
