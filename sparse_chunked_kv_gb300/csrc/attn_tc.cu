@@ -649,9 +649,10 @@ attention_kernel(const __grid_constant__ AttnParams p) {
             reg_fence(sr[1]);
             if (!full) mask_half(sr, half);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(sr[0][i]));
-              mx[(i + 2) & 3] = fmaxf(mx[(i + 2) & 3], __uint_as_float(sr[1][i]));
+            for (int i = 0; i < 32; i += 2) {
+              const int a = (i >> 1) & 1;
+              mx[a] = max3(mx[a], __uint_as_float(sr[0][i]), __uint_as_float(sr[0][i + 1]));
+              mx[2 + a] = max3(mx[2 + a], __uint_as_float(sr[1][i]), __uint_as_float(sr[1][i + 1]));
             }
           }
         }
@@ -688,7 +689,8 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         // Pass 2: probabilities relative to m_used -> bf16 pairs in TMEM
         // columns [0, 64) of S_x (over logits already read), fp32 row sum.
         const float neg_m = -m_used;
-        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint64_t scale2 = f2_pack(scale, scale), neg_m2 = f2_pack(neg_m, neg_m);
+        uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           if (half * 64 < ncol) {
@@ -701,20 +703,24 @@ attention_kernel(const __grid_constant__ AttnParams p) {
             uint32_t packed[32];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-              const float a0 = ex2_approx(fmaf(__uint_as_float(sr[0][i]), scale, neg_m));
-              const float a1 = ex2_approx(fmaf(__uint_as_float(sr[0][i + 1]), scale, neg_m));
-              const float b0 = ex2_approx(fmaf(__uint_as_float(sr[1][i]), scale, neg_m));
-              const float b1 = ex2_approx(fmaf(__uint_as_float(sr[1][i + 1]), scale, neg_m));
-              sum[0] += a0;
-              sum[1] += a1;
-              sum[2] += b0;
-              sum[3] += b1;
+              float xa0, xa1, xb0, xb1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[0][i]), __uint_as_float(sr[0][i + 1])),
+                               scale2, neg_m2), xa0, xa1);
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[1][i]), __uint_as_float(sr[1][i + 1])),
+                               scale2, neg_m2), xb0, xb1);
+              const float a0 = ex2_approx(xa0), a1 = ex2_approx(xa1);
+              const float b0 = ex2_approx(xb0), b1 = ex2_approx(xb1);
+              sum2[0] = f2_add(sum2[0], f2_pack(a0, a1));
+              sum2[1] = f2_add(sum2[1], f2_pack(b0, b1));
               packed[i >> 1] = pack_bf16x2(a0, a1);
               packed[16 + (i >> 1)] = pack_bf16x2(b0, b1);
             }
             if (with_pv) tmem_st32(lane_base + s_col + half * 32, packed);
           }
         }
+        float sum[4];
+        f2_unpack(sum2[0], sum[0], sum[1]);
+        f2_unpack(sum2[1], sum[2], sum[3]);
         l_sum += (sum[0] + sum[1]) + (sum[2] + sum[3]);
         if (with_pv) tmem_st_wait();
         tc_fence_before_sync();
