@@ -241,6 +241,11 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
     wp.G = G;
     wp.D = D;
     wp.k_tiles = ceil_div(C + 1, 128);
+    wp.concat = (C + 1 >= 128) ? 1 : 0;
+    const long long ws_items =
+        wp.concat ? (static_cast<long long>(N) * (C + 1) + 127) / 128 : static_cast<long long>(N) * wp.k_tiles;
+    if (ws_items >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
+    wp.n_items = static_cast<int>(ws_items);
     wp.scale_log2 = ap.scale_log2;
     wp.dev_err = dev_err;
     s = from_cuda(launch_window_scores(wp, st));

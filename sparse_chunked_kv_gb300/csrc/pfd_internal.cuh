@@ -95,6 +95,8 @@ struct WinScoreParams {
   float* part_scores;       // [N, Hkv, C+1]
   int n_chunks, chunk_rows, n_win, Hq, Hkv, G, D;
   int k_tiles;              // ceil((C+1) / 128)
+  int concat;               // 1: 128-row tiles over the chunks laid end to end (C+1 >= 128)
+  int n_items;              // tiles per KV group
   float scale_log2;
   int32_t* dev_err;
 };

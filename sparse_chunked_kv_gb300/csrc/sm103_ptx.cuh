@@ -244,6 +244,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Barrier `id` (1..15) over `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Packed fp32 pairs (one 64-bit register pair): two fp32 lanes per
 // instruction for fused multiply-add and add (round to nearest even).
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {

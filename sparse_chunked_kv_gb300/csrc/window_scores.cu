@@ -10,153 +10,257 @@
 // recomputes the logits transposed -- S^T = K Q_win^T with the 128 key rows of
 // one tile on the TMEM lanes and the W*G window rows of one KV group on the
 // TMEM columns -- so each thread owns one key and sums exp2(scale*s - b_n)
-// over its TMEM row with no cross-thread reduction.  One CTA = (chunk, KV
-// head, 128-key tile); it writes that head group's partial score, and the
-// top-B kernel adds the Hkv partials in a fixed order.
+// along its TMEM row with no cross-thread reduction.  The result is one
+// partial score per KV group; the top-B kernel adds the Hkv partials in a
+// fixed order.
+//
+// The kernel is persistent: CTA c serves KV group c % Hkv, loads that group's
+// window rows once and streams 128-row K tiles through a two-slot ring.  When
+// a chunk has at least 128 rows the tiles run over the chunks' rows laid end to
+// end (a tile then spans at most two chunks, so no tile is mostly padding);
+// otherwise each tile is a piece of one chunk.  S^T is split into two column
+// halves in TMEM so the tensor core computes one half while the warps
+// exponentiate the other.
+//   warp 0      TMA loads and the single-thread MMA issuer;
+//   warps 1..8  two warps per TMEM lane quarter (one thread per key row), each
+//               taking alternate 32-column pieces of every half.
 #include "pfd_internal.cuh"
 #include "sm103_ptx.cuh"
 
 namespace pfd {
 namespace {
 
-constexpr int kThreads = 160;       // warp 0: TMA + MMA; warps 1..4: one key row each thread
-constexpr uint32_t kPanelBytes = 128u * 128u;
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (1 + kConsumerWarps);
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr uint32_t kPanelBytes = 128u * 128u;   // a 128-row, 64-column K panel
 constexpr int kMaxWindowRows = 512;
+constexpr uint32_t kConsumerBarrier = 1;         // named barrier of warps 1..8
+
+// Rows [row0, row0 + nrows) of the concatenated chunks, starting in chunk c0.
+struct Tile {
+  long long row0;
+  int nrows;
+  int c0;
+};
+
+__device__ __forceinline__ Tile tile_of(const WinScoreParams& p, int i) {
+  Tile t;
+  const long long total = static_cast<long long>(p.n_chunks) * p.chunk_rows;
+  if (p.concat) {
+    t.row0 = static_cast<long long>(i) * 128;
+    t.nrows = static_cast<int>(min(128ll, total - t.row0));
+    t.c0 = static_cast<int>(t.row0 / p.chunk_rows);
+  } else {
+    const int chunk = i / p.k_tiles, kt = i % p.k_tiles;
+    t.row0 = static_cast<long long>(chunk) * p.chunk_rows + kt * 128;
+    t.nrows = min(128, p.chunk_rows - kt * 128);
+    t.c0 = chunk;
+  }
+  return t;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 window_score_kernel(const __grid_constant__ WinScoreParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_k;
-  __shared__ uint64_t bar_mma[2];
+  __shared__ uint64_t q_full, k_full[2], k_empty[2], s_full[2], s_free[2];
   __shared__ uint32_t tmem_base;
   __shared__ int failed;
-  __shared__ __align__(16) float b_sh[kMaxWindowRows];   // per column: m_n + log2(l_n)
+  __shared__ __align__(16) float b_sh[2][2][kMaxWindowRows];   // [item parity][chunk of tile][column]
+  __shared__ float red[2][128];                                // second warp's partial per key row
 
   grid_dependency_wait();
-  grid_dependents_launch();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int bid = blockIdx.x;
-  const int kt = bid % p.k_tiles;
-  bid /= p.k_tiles;
-  const int g = bid % p.Hkv;
-  const int chunk = bid / p.Hkv;
-  const int nw = p.n_win * p.G;                         // window rows of this group
-  const int nwp = (nw + 15) & ~15;                      // padded to the MMA N granule
+  const int g = blockIdx.x % p.Hkv;
+  const int cta_g = blockIdx.x / p.Hkv, n_cta_g = gridDim.x / p.Hkv;
+  const int nw = p.n_win * p.G;          // window rows of this group (TMEM columns)
+  const int nwp = (nw + 31) & ~31;       // padded: two halves of a multiple of 16
+  const int half = nwp / 2;
   uint32_t tmem_cols = 32;
   while (tmem_cols < static_cast<uint32_t>(nwp)) tmem_cols <<= 1;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* k_tile = smem;                               // [128 keys x D], D/64 panels
-  uint8_t* q_tile = smem + 128 * D * 2;                 // [nwp rows x D], panels of nwp*128 B
+  uint8_t* q_tile = smem;                                   // [nwp rows x D], panels of nwp*128 B
   const uint32_t q_panel = static_cast<uint32_t>(nwp) * 128u;
+  uint8_t* k_ring = smem + ((static_cast<uint32_t>(nwp) * D * 2 + 1023) & ~1023u);   // 2 x [128 x D]
+  constexpr uint32_t kKBytes = 128u * D * 2u;
 
-  if (warp >= 1) {
+  // Window statistics of chunk c as b values for columns n = w*G + j.
+  auto load_b = [&](int c, int n) -> float {
+    if (c >= p.n_chunks || n >= nw) return INFINITY;   // 2^(s - inf) = 0
+    const int w = n / p.G, jj = n - w * p.G;
+    const long long idx = (static_cast<long long>(c) * p.Hq + g * p.G + jj) * p.n_win + w;
+    const float l = p.win_l[idx];
+    return l > 0.0f ? p.win_m[idx] + log2f(l) : INFINITY;
+  };
+  const int n_items = p.n_items;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_init(&q_full, 1);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&k_full[i], 1);
+        mbar_init(&k_empty[i], 1);
+        mbar_init(&s_full[i], 1);
+        mbar_init(&s_free[i], kConsumerWarps);
+      }
+      fence_barrier_init();
+      failed = 0;
+    }
+    tmem_alloc(&tmem_base, tmem_cols);
+    tmem_relinquish();
+  } else {
     // Padding rows of the window tile are never loaded: keep them zero.
     const int ts = tid - 32;
-    for (int idx = ts; idx < (nwp - nw) * (D / 8); idx += 128) {
+    for (int idx = ts; idx < (nwp - nw) * (D / 8); idx += kConsumers) {
       const int n = nw + idx / (D / 8), c = idx % (D / 8);
       *reinterpret_cast<uint4*>(q_tile + sw128_offset(n, c * 8, nwp)) = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
-    for (int n = ts; n < nwp; n += 128) {
-      float b = INFINITY;  // padding columns contribute exp2(-inf) = 0
-      if (n < nw) {
-        const int w = n / p.G, jj = n - w * p.G;
-        const long long idx = (static_cast<long long>(chunk) * p.Hq + g * p.G + jj) * p.n_win + w;
-        const float l = p.win_l[idx];
-        b = l > 0.0f ? p.win_m[idx] + log2f(l) : INFINITY;
-      }
-      b_sh[n] = b;
+    // Statistics of the first tile.
+    if (cta_g < n_items) {
+      const Tile t0 = tile_of(p, cta_g);
+      for (int idx = ts; idx < 2 * nwp; idx += kConsumers)
+        b_sh[0][idx / nwp][idx % nwp] = load_b(t0.c0 + idx / nwp, idx % nwp);
     }
-  } else if (lane == 0) {
-    mbar_init(&bar_k, 1);
-    mbar_init(&bar_mma[0], 1);
-    mbar_init(&bar_mma[1], 1);
-    fence_barrier_init();
-    failed = 0;
-  }
-  if (warp == 0) {
-    tmem_alloc(&tmem_base, tmem_cols);
-    tmem_relinquish();
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const int n_chunks_n = (nwp + 255) / 256;
 
   if (warp == 0) {
     if (lane == 0) {
-      // K rows of this tile (rows past the chunk are loaded but never written
-      // out) and the group's window rows, one box per 64-column panel each.
-      const uint32_t bytes = 128u * D * 2u + static_cast<uint32_t>(nw) * D * 2u;
-      mbar_arrive_expect_tx(&bar_k, bytes);
-      const int row0 = chunk * p.chunk_rows + kt * 128;
-      for (int pn = 0; pn < D / 64; ++pn) {
-        tma_load_3d(k_tile + pn * kPanelBytes, &p.tm_k, &bar_k, pn * 64, g, row0);
-        tma_load_3d(q_tile + pn * q_panel, &p.tm_qwin, &bar_k, pn * 64, g * p.G, 0);
-      }
-      bool ok = mbar_wait(&bar_k, 0);
+      bool ok = true;
+      mbar_arrive_expect_tx(&q_full, static_cast<uint32_t>(nw) * D * 2u);
+      for (int pn = 0; pn < D / 64; ++pn)
+        tma_load_3d(q_tile + pn * q_panel, &p.tm_qwin, &q_full, pn * 64, g * p.G, 0);
+      auto load_k = [&](int k, int i) {
+        const int slot = k & 1;
+        mbar_arrive_expect_tx(&k_full[slot], kKBytes);
+        const Tile t = tile_of(p, i);
+        for (int pn = 0; pn < D / 64; ++pn)
+          tma_load_3d(k_ring + slot * kKBytes + pn * kPanelBytes, &p.tm_k, &k_full[slot], pn * 64, g,
+                      static_cast<int>(t.row0));
+      };
+      int k = 0;
+      if (cta_g < n_items) load_k(0, cta_g);
+      if (cta_g + n_cta_g < n_items) load_k(1, cta_g + n_cta_g);
+      ok = mbar_wait(&q_full, 0);
       tc_fence_after_sync();
-      const uint32_t ka = smem_u32(k_tile), qa = smem_u32(q_tile);
-      for (int nc = 0; ok && nc < n_chunks_n; ++nc) {
-        const int n0 = nc * 256;
-        const int nn = min(256, nwp - n0);
-        const uint32_t idesc = idesc_bf16(128, nn, false, false);
+      const uint32_t qa = smem_u32(q_tile);
+      for (int i = cta_g; ok && i < n_items; i += n_cta_g, ++k) {
+        const int slot = k & 1;
+        if (!mbar_wait(&k_full[slot], (k >> 1) & 1)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t ka = smem_u32(k_ring + slot * kKBytes);
+        for (int hf = 0; hf < 2; ++hf) {
+          // The warps have finished this half of the previous tile.
+          if (k > 0 && !mbar_wait(&s_free[hf], (k - 1) & 1)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t idesc = idesc_bf16(128, half, false, false);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = sw128_desc(ka + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t b =
-              sw128_desc(qa + (kk >> 2) * q_panel + n0 * 128 + (kk & 3) * 32, 16, 1024);
-          mma_bf16_ss(tmem + n0, a, b, idesc, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = sw128_desc(ka + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
+            const uint64_t b =
+                sw128_desc(qa + (kk >> 2) * q_panel + hf * half * 128 + (kk & 3) * 32, 16, 1024);
+            mma_bf16_ss(tmem + hf * half, a, b, idesc, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&s_full[hf]);
         }
-        mma_commit(&bar_mma[nc]);
+        if (!ok) break;
+        mma_commit(&k_empty[slot]);
+        // The slot is refilled with the tile two ahead once these MMAs are done.
+        const int i2 = i + 2 * n_cta_g;
+        if (i2 < n_items) {
+          if (!mbar_wait(&k_empty[slot], (k >> 1) & 1)) { ok = false; break; }
+          load_k(k + 2, i2);
+        }
       }
-      if (!ok) {
-        atomicOr(&failed, 1);
-        // Nothing was issued; release the consumers.
-        mbar_arrive(&bar_mma[0]);
-        mbar_arrive(&bar_mma[1]);
-      }
+      if (!ok) atomicOr(&failed, 1);
+      // Loads still in flight land before the CTA exits.
+      const int n_mine = cta_g < n_items ? (n_items - 1 - cta_g) / n_cta_g + 1 : 0;
+      for (int kk = max(0, n_mine - 2); kk < n_mine; ++kk) mbar_wait(&k_full[kk & 1], (kk >> 1) & 1);
     }
   } else {
     const int quarter = warp & 3;
+    const int sub = (warp - 1) >> 2;   // 0 for warps 1..4, 1 for warps 5..8
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
+    const int pieces = (half + 31) / 32;
     bool ok = true;
-    for (int nc = 0; nc < n_chunks_n; ++nc) {
-      if (!mbar_wait_warp(&bar_mma[nc], 0)) { ok = false; break; }
-      tc_fence_after_sync();
-      const int n0 = nc * 256;
-      const int nn = min(256, nwp - n0);
-      for (int cc = 0; cc < nn; cc += 32) {
-        uint32_t s[32];
-        tmem_ld32(lane_base + n0 + cc, s);
-        tmem_ld_wait(s);
-        const float4* b4 = reinterpret_cast<const float4*>(b_sh + n0 + cc);
+    int k = 0;
+    for (int i = cta_g; i < n_items; i += n_cta_g, ++k) {
+      const Tile t = tile_of(p, i);
+      const long long r = t.row0 + row;
+      const int c_row = static_cast<int>(r / p.chunk_rows);
+      const float* bv = b_sh[k & 1][min(c_row - t.c0, 1)];
+      // Statistics of the next tile, loaded now and stored after this tile.
+      const int i_next = i + n_cta_g;
+      constexpr int kPer = (2 * kMaxWindowRows + kConsumers - 1) / kConsumers;
+      float b_next[kPer];
+      if (i_next < n_items) {
+        const Tile tn = tile_of(p, i_next);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (n0 + cc + 4 * i < nwp) {
-            const float4 b = b4[i];
-            acc[0] += ex2_approx(fmaf(__uint_as_float(s[4 * i + 0]), p.scale_log2, -b.x));
-            acc[1] += ex2_approx(fmaf(__uint_as_float(s[4 * i + 1]), p.scale_log2, -b.y));
-            acc[2] += ex2_approx(fmaf(__uint_as_float(s[4 * i + 2]), p.scale_log2, -b.z));
-            acc[3] += ex2_approx(fmaf(__uint_as_float(s[4 * i + 3]), p.scale_log2, -b.w));
+        for (int u = 0; u < kPer; ++u) {
+          const int idx = tid - 32 + u * kConsumers;
+          b_next[u] = idx < 2 * nwp ? load_b(tn.c0 + idx / nwp, idx % nwp) : 0.0f;
+        }
+      }
+      uint64_t acc2 = f2_pack(0.f, 0.f);
+      for (int hf = 0; hf < 2; ++hf) {
+        if (ok && !mbar_wait_warp(&s_full[hf], k & 1)) ok = false;
+        tc_fence_after_sync();
+        if (ok) {
+          for (int pc = sub; pc < pieces; pc += 2) {
+            const int c0 = hf * half + pc * 32;
+            uint32_t s[32];
+            tmem_ld32(lane_base + c0, s);
+            tmem_ld_wait(s);
+            const int ncols = min(32, (hf + 1) * half - c0);
+#pragma unroll
+            for (int q = 0; q < 32; q += 2) {
+              if (q < ncols) {
+                const float2 b = *reinterpret_cast<const float2*>(bv + c0 + q);
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[q]), __uint_as_float(s[q + 1])), scale2,
+                                 f2_pack(-b.x, -b.y)),
+                          x0, x1);
+                acc2 = f2_add(acc2, f2_pack(ex2_approx(x0), ex2_approx(x1)));
+              }
+            }
           }
         }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[hf]);
+      }
+      float a0, a1;
+      f2_unpack(acc2, a0, a1);
+      const float acc = a0 + a1;
+      if (i_next < n_items) {
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int idx = tid - 32 + u * kConsumers;
+          if (idx < 2 * nwp) b_sh[(k + 1) & 1][idx / nwp][idx % nwp] = b_next[u];
+        }
+      }
+      if (sub == 1) red[k & 1][row] = acc;
+      named_barrier_sync(kConsumerBarrier, kConsumers);
+      if (sub == 0 && row < t.nrows && c_row < p.n_chunks) {
+        const int tt = static_cast<int>(r - static_cast<long long>(c_row) * p.chunk_rows);
+        p.part_scores[(static_cast<long long>(c_row) * p.Hkv + g) * p.chunk_rows + tt] =
+            acc + red[k & 1][row];
       }
     }
     if (!ok) atomicOr(&failed, 2);
-    const int t = kt * 128 + row;
-    if (t < p.chunk_rows)
-      p.part_scores[(static_cast<long long>(chunk) * p.Hkv + g) * p.chunk_rows + t] =
-          (acc[0] + acc[1]) + (acc[2] + acc[3]);
   }
   tc_fence_before_sync();
   __syncthreads();
+  grid_dependents_launch();
   if (tid == 0 && failed) raise_dev_err(p.dev_err, PFD_DEVERR_TIMEOUT);
   if (warp == 0) {
     tc_fence_after_sync();
@@ -167,21 +271,27 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
 }  // namespace
 
 cudaError_t launch_window_scores(const WinScoreParams& p, cudaStream_t stream) {
-  const int grid = p.n_chunks * p.Hkv * p.k_tiles;
-  if (grid <= 0 || p.n_win <= 0) return cudaSuccess;
-  const int nwp = (p.n_win * p.G + 15) & ~15;
-  const size_t smem = 1024 + static_cast<size_t>(128 + nwp) * p.D * 2;
-  cudaError_t err;
+  if (p.n_items <= 0 || p.n_win <= 0) return cudaSuccess;
+  const int nwp = (p.n_win * p.G + 31) & ~31;
+  if (nwp > kMaxWindowRows) return cudaErrorInvalidValue;
+  int sms = 0, dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  const int per_g = std::max(1, std::min(sms / p.Hkv, p.n_items));
+  const int grid = per_g * p.Hkv;
+  const size_t smem =
+      1024 + ((static_cast<size_t>(nwp) * p.D * 2 + 1023) & ~static_cast<size_t>(1023)) +
+      2 * 128 * static_cast<size_t>(p.D) * 2;
   if (p.D == 64) {
     err = ensure_smem_limit(reinterpret_cast<const void*>(window_score_kernel<64>), static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     return launch_pdl(window_score_kernel<64>, dim3(grid), dim3(kThreads), smem, stream, p);
-  } else {
-    err = ensure_smem_limit(reinterpret_cast<const void*>(window_score_kernel<128>), static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    return launch_pdl(window_score_kernel<128>, dim3(grid), dim3(kThreads), smem, stream, p);
   }
-  return cudaGetLastError();
+  err = ensure_smem_limit(reinterpret_cast<const void*>(window_score_kernel<128>), static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  return launch_pdl(window_score_kernel<128>, dim3(grid), dim3(kThreads), smem, stream, p);
 }
 
 }  // namespace pfd
