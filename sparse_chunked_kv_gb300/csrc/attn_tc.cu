@@ -739,11 +739,11 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         const bool row_ok = row < q_rows && t < it.n_t;
         const int head = it.g * G + jj;
         if (it.kind == kWindow) {
-          if (row_ok) {
-            const long long idx2 = (static_cast<long long>(it.chunk) * p.Hq + head) * p.n_win + t;
-            p.win_m[idx2] = m_used;
-            p.win_l[idx2] = l_sum;
-          }
+          // The window-score kernel's per-column constant b = m + log2(l)
+          // (+inf when the row saw no key, so its probabilities are 0).
+          if (row_ok)
+            p.win_b[(static_cast<long long>(it.chunk) * p.Hkv + it.g) * p.win_stride + t * G + jj] =
+                l_sum > 0.0f ? m_used + log2f(l_sum) : INFINITY;
         } else {
           const long long tok = it.q_row0 + t;
           const bool final_out = it.kind == kChunk || p.n_splits == 1;

@@ -80,15 +80,18 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct PrefillWs {
-  size_t win_m, win_l, part_scores, total;
+  size_t win_b, part_scores, total;
+  int win_stride;
 };
 
+// Window statistics [N, Hkv, W*G rounded up to 32] and per-KV-group partial
+// scores [N, Hkv, C+1].
 PrefillWs prefill_ws_layout(int N, int C, int W, int Hq, int Hkv) {
   PrefillWs w;
-  const size_t stats = static_cast<size_t>(N) * Hq * W * sizeof(float);
-  w.win_m = 0;
-  w.win_l = align256(stats);
-  w.part_scores = w.win_l + align256(stats);
+  w.win_stride = (W * (Hq / Hkv) + 31) & ~31;
+  const size_t stats = static_cast<size_t>(N) * Hkv * w.win_stride * sizeof(float);
+  w.win_b = 0;
+  w.part_scores = align256(stats);
   const size_t ps = W > 0 ? static_cast<size_t>(N) * Hkv * (C + 1) * sizeof(float) : 0;
   w.total = w.part_scores + align256(ps);
   return w;
@@ -200,8 +203,8 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
   ap.q_win = reinterpret_cast<const bf16*>(q_win);
   ap.out = reinterpret_cast<bf16*>(out);
   ap.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
-  ap.win_m = reinterpret_cast<float*>(wsb + ws.win_m);
-  ap.win_l = reinterpret_cast<float*>(wsb + ws.win_l);
+  ap.win_b = reinterpret_cast<float*>(wsb + ws.win_b);
+  ap.win_stride = ws.win_stride;
   ap.dev_err = dev_err;
   ap.mode = kModePrefill;
   ap.Hq = Hq;
@@ -230,8 +233,8 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
     wp.tm_k = ap.tm_k[kBoxLevels - 1][0];
     if (!make_map(&wp.tm_qwin, q_win, W, Hq, D, G, W)) return PFD_ERR_CUDA;
     wp.q_win = ap.q_win;
-    wp.win_m = ap.win_m;
-    wp.win_l = ap.win_l;
+    wp.win_b = ap.win_b;
+    wp.win_stride = ap.win_stride;
     wp.part_scores = reinterpret_cast<float*>(wsb + ws.part_scores);
     wp.n_chunks = N;
     wp.chunk_rows = C + 1;

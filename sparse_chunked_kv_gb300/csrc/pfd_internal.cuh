@@ -53,8 +53,9 @@ struct AttnParams {
   float* part_m;        // decode, several splits: [S, total_lq, Hq] (log2 units)
   float* part_l;        // [S, total_lq, Hq]
   float* part_acc;      // [S, total_lq, Hq, D]
-  float* win_m;         // prefill: [N, Hq, W] running max (log2 units)
-  float* win_l;         // prefill: [N, Hq, W] softmax denominators
+  float* win_b;         // prefill: [N, Hkv, win_stride] per window row n = w*G + j of
+                        // each KV group: m + log2(l) of its softmax over the chunk
+  int win_stride;       // (W*G rounded up to 32)
 
   const pfd_chunk_entry* table;
   const int32_t* sel;
@@ -90,8 +91,8 @@ struct WinScoreParams {
   CUtensorMap tm_k;         // prefill K, 128-row box (as AttnParams::tm_k[3][0])
   CUtensorMap tm_qwin;      // q_win [W, Hq, D], box = W tokens x G heads x 64 columns
   const bf16* q_win;        // [W, Hq, D]
-  const float* win_m;       // [N, Hq, W]
-  const float* win_l;       // [N, Hq, W]
+  const float* win_b;       // [N, Hkv, win_stride], as AttnParams::win_b
+  int win_stride;
   float* part_scores;       // [N, Hkv, C+1]
   int n_chunks, chunk_rows, n_win, Hq, Hkv, G, D;
   int k_tiles;              // ceil((C+1) / 128)

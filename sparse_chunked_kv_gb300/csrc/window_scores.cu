@@ -5,8 +5,8 @@
 //               softmax over the C+1 rows of chunk j of (scale * q_win[w,h] . k[t,g]).
 //
 // The attention kernel has already produced, for every (chunk, head, window
-// row), the row maximum m (log2 units) and the denominator l, folded here into
-// one constant b = m + log2(l) per window row (p = 2^(s*scale - b)).  This kernel
+// row), the constant b = m + log2(l) of that row's softmax over the chunk (m
+// the row maximum in log2 units, l the denominator), so p = 2^(s*scale - b).  This kernel
 // recomputes the logits transposed -- S^T = K Q_win^T with the 128 key rows of
 // one tile on the TMEM lanes and the W*G window rows of one KV group on the
 // TMEM columns -- so each thread owns one key and sums exp2(scale*s - b_n)
@@ -87,13 +87,11 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
   uint8_t* k_ring = smem + ((static_cast<uint32_t>(nwp) * D * 2 + 1023) & ~1023u);   // 2 x [128 x D]
   constexpr uint32_t kKBytes = 128u * D * 2u;
 
-  // Window statistics of chunk c as b values for columns n = w*G + j.
-  auto load_b = [&](int c, int n) -> float {
-    if (c >= p.n_chunks || n >= nw) return INFINITY;   // 2^(s - inf) = 0
-    const int w = n / p.G, jj = n - w * p.G;
-    const long long idx = (static_cast<long long>(c) * p.Hq + g * p.G + jj) * p.n_win + w;
-    const float l = p.win_l[idx];
-    return l > 0.0f ? p.win_m[idx] + log2f(l) : INFINITY;
+  // b of chunk c, column n (n = w*G + j); padding and missing chunks get +inf
+  // (2^(s - inf) = 0).
+  auto b_src = [&](int c, int n) -> const float* {
+    if (c >= p.n_chunks || n >= nw) return nullptr;
+    return p.win_b + (static_cast<long long>(c) * p.Hkv + g) * p.win_stride + n;
   };
   const int n_items = p.n_items;
 
@@ -122,8 +120,10 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
     // Statistics of the first tile.
     if (cta_g < n_items) {
       const Tile t0 = tile_of(p, cta_g);
-      for (int idx = ts; idx < 2 * nwp; idx += kConsumers)
-        b_sh[0][idx / nwp][idx % nwp] = load_b(t0.c0 + idx / nwp, idx % nwp);
+      for (int idx = ts; idx < 2 * nwp; idx += kConsumers) {
+        const float* src = b_src(t0.c0 + idx / nwp, idx % nwp);
+        b_sh[0][idx / nwp][idx % nwp] = src != nullptr ? *src : INFINITY;
+      }
     }
   }
   tc_fence_before_sync();
@@ -198,17 +198,19 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
       const long long r = t.row0 + row;
       const int c_row = static_cast<int>(r / p.chunk_rows);
       const float* bv = b_sh[k & 1][min(c_row - t.c0, 1)];
-      // Statistics of the next tile, loaded now and stored after this tile.
+      // Statistics of the next tile, copied asynchronously into the other
+      // buffer while this tile is processed (the buffer's last reader was the
+      // tile before this one, which every consumer has finished).
       const int i_next = i + n_cta_g;
-      constexpr int kPer = (2 * kMaxWindowRows + kConsumers - 1) / kConsumers;
-      float b_next[kPer];
       if (i_next < n_items) {
         const Tile tn = tile_of(p, i_next);
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-          const int idx = tid - 32 + u * kConsumers;
-          b_next[u] = idx < 2 * nwp ? load_b(tn.c0 + idx / nwp, idx % nwp) : 0.0f;
+        for (int idx = tid - 32; idx < 2 * nwp; idx += kConsumers) {
+          float* dst = &b_sh[(k + 1) & 1][idx / nwp][idx % nwp];
+          const float* src = b_src(tn.c0 + idx / nwp, idx % nwp);
+          if (src != nullptr) cp_async_4(dst, src);
+          else *dst = INFINITY;
         }
+        cp_async_commit();
       }
       uint64_t acc2 = f2_pack(0.f, 0.f);
       for (int hf = 0; hf < 2; ++hf) {
@@ -241,13 +243,7 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
       float a0, a1;
       f2_unpack(acc2, a0, a1);
       const float acc = a0 + a1;
-      if (i_next < n_items) {
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-          const int idx = tid - 32 + u * kConsumers;
-          if (idx < 2 * nwp) b_sh[(k + 1) & 1][idx / nwp][idx % nwp] = b_next[u];
-        }
-      }
+      if (i_next < n_items) cp_async_wait_all();
       if (sub == 1) red[k & 1][row] = acc;
       named_barrier_sync(kConsumerBarrier, kConsumers);
       if (sub == 0 && row < t.nrows && c_row < p.n_chunks) {
