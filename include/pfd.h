@@ -18,8 +18,10 @@
  *   - bf16 values are passed as raw 16-bit patterns (pfd_bf16).
  *   - Every pointer named as device memory must be CUDA device memory on the
  *     current device; the caller owns all memory.  The library allocates
- *     nothing and keeps no state between calls other than process-wide,
- *     read-only caches (the device's SM count, the TMA encoder entry point).
+ *     nothing and keeps no state between calls other than process-wide
+ *     caches: the device's SM count, the TMA encoder entry point, and a
+ *     bounded table of encoded TMA tensor maps keyed by (address, shape, box),
+ *     so repeated calls on the same buffers do not re-encode them.
  *   - Every call is asynchronous on `stream` (NULL = the legacy default
  *     stream).  The return value reports only what the host can check:
  *     invalid arguments (PFD_ERR_INVALID_ARG), shapes outside the supported

@@ -45,8 +45,8 @@ int device_sm_count() {
 // 3-D map over a [rows, heads, D] bf16 tensor with a box of box_rows rows x
 // box_heads heads x 64 columns (128 B), 128-byte swizzle; out-of-range rows
 // read as zero.
-bool make_map(CUtensorMap* map, const void* base, long long rows, int heads, int D, int box_heads,
-              int box_rows) {
+bool encode_map(CUtensorMap* map, const void* base, long long rows, int heads, int D, int box_heads,
+                int box_rows) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr || base == nullptr || rows <= 0) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads),
@@ -60,6 +60,44 @@ bool make_map(CUtensorMap* map, const void* base, long long rows, int heads, int
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// A tensor map depends only on (base, rows, heads, D, box), so encoded maps
+// are kept in a small process-wide table: a decode loop that calls with the
+// same buffers step after step encodes each map once.  Round-robin
+// replacement; the table is guarded by a mutex.
+struct MapKey {
+  const void* base;
+  long long rows;
+  int heads, D, box_heads, box_rows;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && rows == o.rows && heads == o.heads && D == o.D &&
+           box_heads == o.box_heads && box_rows == o.box_rows;
+  }
+};
+
+bool make_map(CUtensorMap* map, const void* base, long long rows, int heads, int D, int box_heads,
+              int box_rows) {
+  constexpr int kEntries = 128;
+  static std::mutex mu;
+  static MapKey keys[kEntries];
+  static CUtensorMap maps[kEntries];
+  static int used = 0, next = 0;
+  const MapKey key{base, rows, heads, D, box_heads, box_rows};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (keys[i] == key) {
+        *map = maps[i];
+        return true;
+      }
+  }
+  if (!encode_map(map, base, rows, heads, D, box_heads, box_rows)) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  const int slot = used < kEntries ? used++ : (next++ % kEntries);
+  keys[slot] = key;
+  maps[slot] = *map;
+  return true;
 }
 
 // K or V maps of one tensor (slot t of maps[level][t]): boxes of 16, 32, 64
