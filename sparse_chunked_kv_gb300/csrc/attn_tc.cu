@@ -759,36 +759,31 @@ attention_kernel(const __grid_constant__ AttnParams p) {
               for (int i = 0; i < 32; ++i) o[i] = 0u;
             }
             if (!row_ok) continue;
-            // Each lane writes its own row; whole 32-byte sectors where the
-            // destination allows it (half the store instructions, no
-            // half-filled sectors).
-            if (final_out) {
-              uint32_t packed[16];
+            // Normalised bf16 row: the output, or one split's partial O / l
+            // (the merge weighs it by the split's l and max).  Each lane
+            // writes its own row; whole 32-byte sectors where the destination
+            // allows it (the workspace always does).
+            uint32_t packed[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                packed[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
-                                        __uint_as_float(o[2 * i + 1]) * inv_l);
-              bf16* dst = p.out + (tok * p.Hq + head) * D + ch * 32;
-              if (p.out_v8) {
+            for (int i = 0; i < 16; ++i)
+              packed[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                      __uint_as_float(o[2 * i + 1]) * inv_l);
+            bf16* dst = final_out
+                ? p.out + (tok * p.Hq + head) * D + ch * 32
+                : p.part_acc +
+                      ((static_cast<long long>(it.split) * p.total_lq + tok) * p.Hq + head) * D +
+                      ch * 32;
+            if (!final_out || p.out_v8) {
 #pragma unroll
-                for (int q8 = 0; q8 < 2; ++q8)
-                  st_global_v8(dst + q8 * 16, packed[8 * q8], packed[8 * q8 + 1], packed[8 * q8 + 2],
-                               packed[8 * q8 + 3], packed[8 * q8 + 4], packed[8 * q8 + 5],
-                               packed[8 * q8 + 6], packed[8 * q8 + 7]);
-              } else {
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                  reinterpret_cast<uint4*>(dst)[q4] = make_uint4(
-                      packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2], packed[4 * q4 + 3]);
-              }
+              for (int q8 = 0; q8 < 2; ++q8)
+                st_global_v8(dst + q8 * 16, packed[8 * q8], packed[8 * q8 + 1], packed[8 * q8 + 2],
+                             packed[8 * q8 + 3], packed[8 * q8 + 4], packed[8 * q8 + 5],
+                             packed[8 * q8 + 6], packed[8 * q8 + 7]);
             } else {
-              // Workspace partials: 256-byte aligned base, 128-byte row chunks.
-              float* dst = p.part_acc +
-                  ((static_cast<long long>(it.split) * p.total_lq + tok) * p.Hq + head) * D + ch * 32;
 #pragma unroll
-              for (int q8 = 0; q8 < 4; ++q8)
-                st_global_v8(dst + q8 * 8, o[8 * q8], o[8 * q8 + 1], o[8 * q8 + 2], o[8 * q8 + 3],
-                             o[8 * q8 + 4], o[8 * q8 + 5], o[8 * q8 + 6], o[8 * q8 + 7]);
+              for (int q4 = 0; q4 < 4; ++q4)
+                reinterpret_cast<uint4*>(dst)[q4] = make_uint4(
+                    packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2], packed[4 * q4 + 3]);
             }
           }
           if (row_ok && it.kind == kDecode) {

@@ -2,9 +2,9 @@
 // Optimization" of the Prefilling-dLLM summary: chunks are processed
 // independently and the results are merged by a log-sum-exp reduction).
 //
-// For one (row, head) with partials (m_s, l_s, acc_s), m in log2 units:
-//   M = max_s m_s,  w_s = 2^(m_s - M),  L = sum_s w_s l_s,
-//   out = sum_s w_s acc_s / L,  lse = (M + log2 L) * ln 2.
+// For one (row, head) with partials (m_s, l_s, O_s = acc_s / l_s), m in log2
+// units:  M = max_s m_s,  w_s = 2^(m_s - M) l_s,  L = sum_s w_s,
+//         out = sum_s w_s O_s / L,  lse = (M + log2 L) * ln 2.
 // One warp per (row, head); each lane owns 4 consecutive columns of D.
 #include "pfd_internal.cuh"
 #include "sm103_ptx.cuh"
@@ -13,13 +13,17 @@ namespace pfd {
 namespace {
 
 constexpr int kMergeThreads = 256;
-constexpr int kAccBatch = 8;   // split partials of acc loaded per round trip
+constexpr int kAccBatch = 8;   // split partials of O loaded per round trip
 constexpr float kLn2 = 0.69314718055994530942f;
 
+__device__ __forceinline__ float4 bf16x4_to_float4(uint2 v) {
+  return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                     __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+}
+
 // One warp per (row, head).  Lane s loads split s's (m, l) (lanes loop when
-// S > 32), so the statistics of every split arrive in one round trip; the
-// acc rows of up to kAccBatch splits are loaded in the same round trip, each
-// lane holding 4 consecutive columns of D.
+// S > 32), so the statistics of every split arrive in one round trip; the O
+// rows of up to kAccBatch splits are loaded in the same round trip.
 __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergeParams p) {
   grid_dependency_wait();
   const long long pair = static_cast<long long>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
@@ -28,15 +32,14 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergePar
   const int lane = threadIdx.x & 31;
   const int S = p.n_splits;
   const bool active = lane * 4 < p.D;
-  const float* acc_base = p.part_acc + pair * p.D + lane * 4;
-  const long long acc_stride = n_pairs * p.D;
+  const bf16* o_base = p.part_acc + pair * p.D + lane * 4;
+  const long long o_stride = n_pairs * p.D;
 
-  float4 a[kAccBatch];
+  uint2 a[kAccBatch];
 #pragma unroll
   for (int s = 0; s < kAccBatch; ++s)
-    if (active && s < S) a[s] = __ldg(reinterpret_cast<const float4*>(acc_base + s * acc_stride));
+    if (active && s < S) a[s] = __ldg(reinterpret_cast<const uint2*>(o_base + s * o_stride));
 
-  // Running max over the splits, then each split's weight 2^(m_s - M).
   float m_lane = -INFINITY, l_lane = 0.0f;   // lane's own splits s = lane, lane + 32
   float m_hi = -INFINITY, l_hi = 0.0f;
   if (lane < S) {
@@ -50,9 +53,10 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergePar
   float big_m = fmaxf(m_lane, m_hi);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) big_m = fmaxf(big_m, __shfl_xor_sync(0xFFFFFFFFu, big_m, o));
-  const float w_lane = (m_lane == -INFINITY) ? 0.0f : ex2_approx(m_lane - big_m);
-  const float w_hi = (m_hi == -INFINITY) ? 0.0f : ex2_approx(m_hi - big_m);
-  float big_l = w_lane * l_lane + w_hi * l_hi;
+  // Weight of each split: 2^(m_s - M) * l_s (0 for a split that saw no key).
+  const float w_lane = (m_lane == -INFINITY) ? 0.0f : ex2_approx(m_lane - big_m) * l_lane;
+  const float w_hi = (m_hi == -INFINITY) ? 0.0f : ex2_approx(m_hi - big_m) * l_hi;
+  float big_l = w_lane + w_hi;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) big_l += __shfl_xor_sync(0xFFFFFFFFu, big_l, o);
 
@@ -61,8 +65,7 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergePar
     if (s0 > 0) {
 #pragma unroll
       for (int s = 0; s < kAccBatch; ++s)
-        if (active && s0 + s < S)
-          a[s] = __ldg(reinterpret_cast<const float4*>(acc_base + (s0 + s) * acc_stride));
+        if (active && s0 + s < S) a[s] = __ldg(reinterpret_cast<const uint2*>(o_base + (s0 + s) * o_stride));
     }
 #pragma unroll
     for (int s = 0; s < kAccBatch; ++s) {
@@ -71,10 +74,11 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergePar
       const float wh = __shfl_sync(0xFFFFFFFFu, w_hi, src);
       const float w = (s0 + s) < 32 ? wl : wh;
       if (active && s0 + s < S && w != 0.0f) {
-        acc.x = fmaf(w, a[s].x, acc.x);
-        acc.y = fmaf(w, a[s].y, acc.y);
-        acc.z = fmaf(w, a[s].z, acc.z);
-        acc.w = fmaf(w, a[s].w, acc.w);
+        const float4 v = bf16x4_to_float4(a[s]);
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
       }
     }
   }

@@ -152,7 +152,7 @@ DecodeWs decode_ws_layout(int n_splits, long long total_lq, int Hq, int D) {
   w.part_m = 0;
   w.part_l = align256(ml);
   w.part_acc = w.part_l + align256(ml);
-  w.total = w.part_acc + align256(ml * D);
+  w.total = w.part_acc + align256(ml / sizeof(float) * D * 2);   // bf16 partials
   return w;
 }
 
@@ -440,7 +440,7 @@ pfd_status pfd_decode_attention(const pfd_bf16* q, const pfd_bf16* k_self,
   ap.lse = lse;
   ap.part_m = S > 1 ? reinterpret_cast<float*>(wsb + ws.part_m) : nullptr;
   ap.part_l = S > 1 ? reinterpret_cast<float*>(wsb + ws.part_l) : nullptr;
-  ap.part_acc = S > 1 ? reinterpret_cast<float*>(wsb + ws.part_acc) : nullptr;
+  ap.part_acc = S > 1 ? reinterpret_cast<bf16*>(wsb + ws.part_acc) : nullptr;
   ap.table = table;
   ap.sel = sel;
   ap.cu_k = cu_k;

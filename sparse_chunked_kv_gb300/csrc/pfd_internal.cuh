@@ -52,7 +52,7 @@ struct AttnParams {
   float* lse;           // decode, one split: [total_lq, Hq] (may be null)
   float* part_m;        // decode, several splits: [S, total_lq, Hq] (log2 units)
   float* part_l;        // [S, total_lq, Hq]
-  float* part_acc;      // [S, total_lq, Hq, D]
+  bf16* part_acc;       // [S, total_lq, Hq, D] normalised (acc / l) bf16
   float* win_b;         // prefill: [N, Hkv, win_stride] per window row n = w*G + j of
                         // each KV group: m + log2(l) of its softmax over the chunk
   int win_stride;       // (W*G rounded up to 32)
@@ -132,7 +132,7 @@ cudaError_t launch_select(const float* s_i, const float* s_p, const int32_t* cu_
 struct MergeParams {
   const float* part_m;
   const float* part_l;
-  const float* part_acc;
+  const bf16* part_acc;     // normalised (acc / l) bf16
   bf16* out;
   float* lse;
   int n_splits, total_lq, Hq, D;

@@ -115,4 +115,4 @@ def test_decode_host_checks_and_plan(lib):
     assert 1 <= s <= 64
     assert _abi.pfd_decode_workspace(1, [0, 320], [0, 4], 28, 4, 128, 257, 1) == 0
     ws2 = _abi.pfd_decode_workspace(1, [0, 320], [0, 4], 28, 4, 128, 257, 2)
-    assert ws2 >= 2 * 320 * 28 * (2 + 128) * 4
+    assert ws2 >= 2 * 320 * 28 * (2 * 4 + 128 * 2)   # fp32 (m, l) and bf16 O per row and split
