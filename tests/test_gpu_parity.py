@@ -116,7 +116,9 @@ def _decode_inputs(cfg, seq=0, step=0, pad=0, fill=0.0):
     return req, pk, pv, table, sel, ql, kl, vl
 
 
-@pytest.mark.parametrize("n_splits", [0, 1, 2, 3, 5])
+# 12 splits cut the tiny case's ~190 keys into splits of one or two 16-row
+# key groups, far below one 128-key tile each.
+@pytest.mark.parametrize("n_splits", [0, 1, 2, 3, 4, 5, 7, 8, 12])
 @pytest.mark.parametrize("cfg_name", ["tiny", "gqa7"])
 def test_decode_parity(cfg_name, n_splits):
     cfg = wl.TINY if cfg_name == "tiny" else wl.scaled(wl.CTX_8K, n_chunks=6, n_select=3, n_resp=100)
