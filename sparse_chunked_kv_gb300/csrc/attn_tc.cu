@@ -748,31 +748,21 @@ attention_kernel(const __grid_constant__ AttnParams p) {
           const long long tok = it.q_row0 + t;
           const bool final_out = it.kind == kChunk || p.n_splits == 1;
           const float inv_l = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
-#pragma unroll 1
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t o[32];
-            if (n_seen > 0) {
-              tmem_ld32(lane_base + o_col + ch * 32, o);
-              tmem_ld_wait(o);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = 0u;
-            }
-            if (!row_ok) continue;
-            // Normalised bf16 row: the output, or one split's partial O / l
-            // (the merge weighs it by the split's l and max).  Each lane
-            // writes its own row; whole 32-byte sectors where the destination
-            // allows it (the workspace always does).
+          bf16* const row_dst =
+              final_out ? p.out + (tok * p.Hq + head) * D
+                        : p.part_acc +
+                              ((static_cast<long long>(it.split) * p.total_lq + tok) * p.Hq + head) * D;
+          // Normalised bf16 row: the output, or one split's partial O / l
+          // (the merge weighs it by the split's l and max).  Each lane
+          // writes its own row; whole 32-byte sectors where the destination
+          // allows it (the workspace always does).
+          auto emit32 = [&](int ch, const uint32_t (&o)[32]) {
             uint32_t packed[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
               packed[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
                                       __uint_as_float(o[2 * i + 1]) * inv_l);
-            bf16* dst = final_out
-                ? p.out + (tok * p.Hq + head) * D + ch * 32
-                : p.part_acc +
-                      ((static_cast<long long>(it.split) * p.total_lq + tok) * p.Hq + head) * D +
-                      ch * 32;
+            bf16* dst = row_dst + ch * 32;
             if (!final_out || p.out_v8) {
 #pragma unroll
               for (int q8 = 0; q8 < 2; ++q8)
@@ -785,6 +775,23 @@ attention_kernel(const __grid_constant__ AttnParams p) {
                 reinterpret_cast<uint4*>(dst)[q4] = make_uint4(
                     packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2], packed[4 * q4 + 3]);
             }
+          };
+          // 64 columns of O per TMEM round trip.
+#pragma unroll 1
+          for (int ch = 0; ch < D / 32; ch += 2) {
+            uint32_t o0[32], o1[32];
+            if (n_seen > 0) {
+              tmem_ld32(lane_base + o_col + ch * 32, o0);
+              tmem_ld32(lane_base + o_col + ch * 32 + 32, o1);
+              tmem_ld_wait(o0);
+              reg_fence(o1);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0u;
+            }
+            if (!row_ok) continue;
+            emit32(ch, o0);
+            emit32(ch + 1, o1);
           }
           if (row_ok && it.kind == kDecode) {
             if (p.n_splits == 1) {

@@ -6,6 +6,9 @@
 // units:  M = max_s m_s,  w_s = 2^(m_s - M) l_s,  L = sum_s w_s,
 //         out = sum_s w_s O_s / L,  lse = (M + log2 L) * ln 2.
 // One warp per (row, head); each lane owns 4 consecutive columns of D.
+#include <algorithm>
+#include <atomic>
+
 #include "pfd_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -26,6 +29,12 @@ __device__ __forceinline__ float4 bf16x4_to_float4(uint2 v) {
 // rows of up to kAccBatch splits are loaded in the same round trip.
 __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergeParams p) {
   grid_dependency_wait();
+  // With p.early_trigger (a grid of at most two waves of resident CTAs) the
+  // next kernel on the stream may be scheduled once every CTA has started:
+  // its CTAs take the SMs as this grid's last wave leaves them.  A longer
+  // grid signals only at its end, as an early next grid slowed its later
+  // waves down.
+  if (p.early_trigger) grid_dependents_launch();
   const long long pair = static_cast<long long>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
   const long long n_pairs = static_cast<long long>(p.total_lq) * p.Hq;
   if (pair >= n_pairs) return;
@@ -91,17 +100,36 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergePar
   }
   if (lane == 0 && p.lse != nullptr)
     p.lse[pair] = big_l > 0.0f ? (big_m + log2f(big_l)) * kLn2 : -INFINITY;
-  // Late trigger: a next attention grid scheduled early would hold registers
-  // that the merge's later waves need.
   grid_dependents_launch();
+}
+
+
+// Merge CTAs resident on one SM at once (cached per device; 1 if the query
+// fails).
+int merge_ctas_per_sm() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 1;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, lse_merge_kernel, kMergeThreads, 0) !=
+          cudaSuccess ||
+      n < 1)
+    n = 1;
+  cache[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 }  // namespace
 
-cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream) {
+cudaError_t launch_lse_merge(const MergeParams& params, int sm_count, cudaStream_t stream) {
+  MergeParams p = params;
   const long long n_pairs = static_cast<long long>(p.total_lq) * p.Hq;
   const long long blocks = (n_pairs + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
   if (blocks <= 0) return cudaSuccess;
+  const long long wave = static_cast<long long>(std::max(sm_count, 1)) * merge_ctas_per_sm();
+  p.early_trigger = blocks <= 2 * wave ? 1 : 0;
   return launch_pdl(lse_merge_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kMergeThreads), 0,
                     stream, p);
 }

@@ -475,7 +475,7 @@ pfd_status pfd_decode_attention(const pfd_bf16* q, const pfd_bf16* k_self,
   mp.total_lq = total_lq;
   mp.Hq = Hq;
   mp.D = D;
-  return from_cuda(launch_lse_merge(mp, st));
+  return from_cuda(launch_lse_merge(mp, device_sm_count(), st));
 }
 
 }  // extern "C"

@@ -136,9 +136,11 @@ struct MergeParams {
   bf16* out;
   float* lse;
   int n_splits, total_lq, Hq, D;
+  int early_trigger;        // set by launch_lse_merge
 };
 
-cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream);
+// sm_count: SMs of the current device (the grid is one wave of resident CTAs).
+cudaError_t launch_lse_merge(const MergeParams& p, int sm_count, cudaStream_t stream);
 
 // ------------------------------------------------------------- helpers --
 // Raises a kernel's dynamic shared-memory limit once per (kernel, device), so
