@@ -39,6 +39,15 @@
 //               O rescale in TMEM only when the running max grows by more than
 //               2^8, and the epilogue of the item.
 // TMEM (512 columns): S_a [0,128), S_b [128,256), O_a [256,..), O_b [384,..).
+//
+// A prefill chunk has C + 1 keys: its BOS row and C content rows.  The tensor
+// cores take only the content rows (C = 256, 512, 1024 fill whole 128-key
+// tiles, where the BOS row would add a tile of one key); the BOS key enters
+// analytically.  The Q loader brings its K and V rows to shared memory with
+// the item's Q, each softmax thread computes its BOS logit from the Q tile
+// during the first key tile, and the epilogue folds it into the row's max,
+// denominator and output: M = max(m, s0), l' = l 2^(m - M) + 2^(s0 - M),
+// O' = O 2^(m - M) + 2^(s0 - M) v0.
 #include "pfd_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -170,7 +179,12 @@ struct Layout {
   static constexpr uint32_t kSegRow = kRing0 + kRing * kTileBytes;   // int32 [kMaxSegments]
   static constexpr uint32_t kSegLen = kSegRow + 4u * kMaxSegments;
   static constexpr uint32_t kSegG0 = kSegLen + 4u * kMaxSegments;    // [kMaxSegments + 1]
-  static constexpr uint32_t kTotal = kSegG0 + 4u * (kMaxSegments + 1);
+  static constexpr uint32_t kTotalDecode = kSegG0 + 4u * (kMaxSegments + 1);
+  // Prefill only: the BOS rows of the item's chunk, double-buffered by item
+  // parity: one 16-row TMA box of K, then one of V (row 0 is the BOS row).
+  static constexpr uint32_t kBosBox = (D / 64) * 16u * 128u;
+  static constexpr uint32_t kBos0 = (kTotalDecode + 1023u) & ~1023u;
+  static constexpr uint32_t kTotalPrefill = kBos0 + 2u * 2u * kBosBox;
 };
 
 __device__ __forceinline__ int groups_of(int len) { return (len + kGroupRows - 1) / kGroupRows; }
@@ -185,8 +199,8 @@ __device__ __forceinline__ int load_segments(const AttnParams& p, const Item& it
   if (it.kind != kDecode) {
     nseg = 1;
     if (lane == 0) {
-      seg_row[0] = it.chunk * p.chunk_rows;
-      seg_len[0] = p.chunk_rows;
+      seg_row[0] = it.chunk * p.chunk_rows + 1;   // the content rows; BOS enters analytically
+      seg_len[0] = p.chunk_rows - 1;
     }
   } else {
     const int nsel = it.k1 - it.k0;
@@ -238,7 +252,9 @@ struct RowState {
   float l_sum;
 };
 
-template <int D>
+// kPrefill: a prefill launch (chunk and window items, with the analytic BOS
+// key); else a decode launch, compiled without that code.
+template <int D, bool kPrefill>
 __global__ void __launch_bounds__(kThreads, 1)
 attention_kernel(const __grid_constant__ AttnParams p) {
   using L = Layout<D>;
@@ -423,13 +439,22 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         Item it;
         if (!resolve_item(p, idx, it)) continue;
         // The Q buffers are free once the previous item's last QK has run.
+        // Its MMAs include PVs that needed the softmax of this item's
+        // predecessor done, so the BOS buffer of this parity (last read by the
+        // epilogue two items back) is free as well.
         if (items_done > 0 && !mbar_wait(&sh.q_empty, (items_done - 1) & 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(&sh.q_full, it.has_b ? 2 * q_bytes : q_bytes);
+        const int n_bos = !kPrefill ? 0 : it.kind == kChunk ? 2 : 1;   // K (and V) rows
+        mbar_arrive_expect_tx(&sh.q_full, (it.has_b ? 2 * q_bytes : q_bytes) + n_bos * L::kBosBox);
         for (int x = 0; x < (it.has_b ? 2 : 1); ++x)
           for (int pn = 0; pn < D / 64; ++pn)
             tma_load_3d(smem + (x ? L::kQ1 : L::kQ0) + pn * kPanelBytes, &p.tm_q[it.q_map],
                         &sh.q_full, pn * 64, it.g * G,
                         static_cast<int>(it.q_row0) + (it.ta + x) * p.Tq);
+        uint8_t* bos = smem + L::kBos0 + (items_done & 1) * 2 * L::kBosBox;
+        for (int kv = 0; kv < n_bos; ++kv)
+          for (int pn = 0; pn < D / 64; ++pn)
+            tma_load_3d(bos + kv * L::kBosBox + pn * 2048, kv ? &p.tm_v[0][0] : &p.tm_k[0][0],
+                        &sh.q_full, pn * 64, it.g, it.chunk * p.chunk_rows);
         ++items_done;
       }
       if (!ok) atomicOr(&sh.failed, 8);
@@ -593,7 +618,29 @@ attention_kernel(const __grid_constant__ AttnParams p) {
       const bool with_pv = it.kind != kWindow;
       const bool active = x == 0 || it.has_b;
       float m_used = -INFINITY, l_sum = 0.0f;
+      float s_bos = 0.0f;   // prefill: this row's BOS logit q . k0 (unscaled)
       int n_seen = 0;
+      const uint8_t* bos = smem + L::kBos0 + (items_done & 1) * 2 * L::kBosBox;
+      // q . k0 from the Q tile in shared memory and the BOS K row, in fp32.
+      // Both arrived by TMA on q_full (phase items_done, complete since the
+      // first QK ran; the next phase needs this item's last P first).
+      auto bos_logit = [&]() -> float {
+        if (!mbar_wait_warp(&sh.q_full, items_done & 1)) ok = false;
+        const uint8_t* qt = smem + (x ? L::kQ1 : L::kQ0);
+        float acc0 = 0.0f, acc1 = 0.0f;
+#pragma unroll 4
+        for (int c8 = 0; c8 < D / 8; ++c8) {
+          const uint4 qv = *reinterpret_cast<const uint4*>(qt + sw128_offset(row, c8 * 8, kBlockM));
+          const uint4 kv = *reinterpret_cast<const uint4*>(bos + sw128_offset(0, c8 * 8, 16));
+          const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc0 = fmaf(__uint_as_float(qw[i] << 16), __uint_as_float(kw[i] << 16), acc0);
+            acc1 = fmaf(__uint_as_float(qw[i] & 0xFFFF0000u), __uint_as_float(kw[i] & 0xFFFF0000u), acc1);
+          }
+        }
+        return acc0 + acc1;
+      };
       for (;;) {
         const int ms = tile_ctr % kRing;
         if (!mbar_wait_warp(&sh.meta_full[ms], (tile_ctr / kRing) & 1)) { ok = false; break; }
@@ -723,8 +770,14 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         f2_unpack(sum2[1], sum[2], sum[3]);
         l_sum += (sum[0] + sum[1]) + (sum[2] + sum[3]);
         if (with_pv) tmem_st_wait();
+        // The BOS logit, while the Q tile is certainly resident: before the
+        // item's last P is handed over (after it the last PV may complete and
+        // the next item's Q arrive), else right after the first tile's P.
+        const bool bos_now = kPrefill && n_seen == 1;
+        if (bos_now && meta.last) s_bos = bos_logit();
         tc_fence_before_sync();
         mbar_arrive(&sh.p_full[x]);
+        if (bos_now && !meta.last) s_bos = bos_logit();
         if (meta.last) break;
       }
       if (!ok) break;
@@ -732,6 +785,18 @@ attention_kernel(const __grid_constant__ AttnParams p) {
       // ---------------------------------------------------------- epilogue --
       if (!mbar_wait_warp(&sh.o_full[x], items_done & 1)) { ok = false; break; }
       tc_fence_after_sync();
+      // Prefill: fold the BOS key into (m, l) and, through o_alpha / o_bos,
+      // into the output row (every prefill item has content keys, so s_bos
+      // was computed).
+      float o_alpha = 1.0f, o_bos = 0.0f;
+      if constexpr (kPrefill) {
+        const float sb = s_bos * scale;
+        const float m_new = fmaxf(m_used, sb);
+        o_alpha = ex2_approx(m_used - m_new);
+        o_bos = ex2_approx(sb - m_new);
+        l_sum = l_sum * o_alpha + o_bos;
+        m_used = m_new;
+      }
       if (active) {
         const int t_local = row / G;
         const int jj = row - t_local * G;
@@ -756,12 +821,30 @@ attention_kernel(const __grid_constant__ AttnParams p) {
           // (the merge weighs it by the split's l and max).  Each lane
           // writes its own row; whole 32-byte sectors where the destination
           // allows it (the workspace always does).
+          const uint8_t* v_bos = bos + L::kBosBox;
           auto emit32 = [&](int ch, const uint32_t (&o)[32]) {
             uint32_t packed[16];
+            if (kPrefill && it.kind == kChunk) {
+              // (O 2^(m - M) + 2^(s0 - M) v0) / l' over these 32 columns.
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              packed[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
-                                      __uint_as_float(o[2 * i + 1]) * inv_l);
+              for (int q4 = 0; q4 < 4; ++q4) {
+                const uint4 vv = *reinterpret_cast<const uint4*>(v_bos + sw128_offset(0, ch * 32 + q4 * 8, 16));
+                const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int e = 8 * q4 + 2 * i;
+                  const float lo = fmaf(__uint_as_float(o[e]), o_alpha, o_bos * __uint_as_float(vw[i] << 16));
+                  const float hi = fmaf(__uint_as_float(o[e + 1]), o_alpha,
+                                        o_bos * __uint_as_float(vw[i] & 0xFFFF0000u));
+                  packed[4 * q4 + i] = pack_bf16x2(lo * inv_l, hi * inv_l);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                packed[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                        __uint_as_float(o[2 * i + 1]) * inv_l);
+            }
             bf16* dst = row_dst + ch * 32;
             if (!final_out || p.out_v8) {
 #pragma unroll
@@ -828,24 +911,28 @@ attention_kernel(const __grid_constant__ AttnParams p) {
 
 }  // namespace
 
-size_t attention_smem_bytes(int D) {
-  return 1024 + (D == 64 ? Layout<64>::kTotal : Layout<128>::kTotal);
+size_t attention_smem_bytes(int D, bool prefill) {
+  if (D == 64) return 1024 + (prefill ? Layout<64>::kTotalPrefill : Layout<64>::kTotalDecode);
+  return 1024 + (prefill ? Layout<128>::kTotalPrefill : Layout<128>::kTotalDecode);
+}
+
+template <int D, bool kPrefill>
+cudaError_t launch_attention_t(const AttnParams& p, int grid, size_t smem, cudaStream_t stream) {
+  const cudaError_t err = ensure_smem_limit(
+      reinterpret_cast<const void*>(attention_kernel<D, kPrefill>), static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  return launch_pdl(attention_kernel<D, kPrefill>, dim3(grid), dim3(kThreads), smem, stream, p);
 }
 
 cudaError_t launch_attention(const AttnParams& p, int grid, cudaStream_t stream) {
   if (grid <= 0 || p.n_items <= 0) return cudaSuccess;
-  const size_t smem = attention_smem_bytes(p.D);
-  cudaError_t err;
-  if (p.D == 64) {
-    err = ensure_smem_limit(reinterpret_cast<const void*>(attention_kernel<64>), static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    return launch_pdl(attention_kernel<64>, dim3(grid), dim3(kThreads), smem, stream, p);
-  } else {
-    err = ensure_smem_limit(reinterpret_cast<const void*>(attention_kernel<128>), static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    return launch_pdl(attention_kernel<128>, dim3(grid), dim3(kThreads), smem, stream, p);
-  }
-  return cudaGetLastError();
+  const bool prefill = p.mode == kModePrefill;
+  const size_t smem = attention_smem_bytes(p.D, prefill);
+  if (p.D == 64)
+    return prefill ? launch_attention_t<64, true>(p, grid, smem, stream)
+                   : launch_attention_t<64, false>(p, grid, smem, stream);
+  return prefill ? launch_attention_t<128, true>(p, grid, smem, stream)
+                 : launch_attention_t<128, false>(p, grid, smem, stream);
 }
 
 }  // namespace pfd

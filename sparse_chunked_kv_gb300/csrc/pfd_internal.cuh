@@ -84,7 +84,7 @@ struct AttnParams {
 };
 
 cudaError_t launch_attention(const AttnParams& p, int grid, cudaStream_t stream);
-size_t attention_smem_bytes(int D);
+size_t attention_smem_bytes(int D, bool prefill);
 
 // ------------------------------------------------------- window scores --
 struct WinScoreParams {
