@@ -170,6 +170,44 @@ __device__ __forceinline__ bool item_shape_error(const AttnParams& p, int idx) {
          k1 - k0 >= kMaxSegments;
 }
 
+// Prefill item of cost rank r: first the pairs of two query tiles, then the
+// pairs of one (the last pair of an odd tile count), first of chunk rows,
+// then of window rows; returns the item index resolve_item decodes.
+__device__ __forceinline__ int prefill_item_of_rank(const AttnParams& p, int r) {
+  const int pairs_c = (p.mt_chunk + 1) / 2, pairs_w = (p.mt_win + 1) / 2;
+  const int half_c = p.mt_chunk & 1, half_w = p.mt_win & 1;
+  const int full_c = pairs_c - half_c, full_w = pairs_w - half_w;
+  const int groups = p.n_chunks * p.Hkv;   // (chunk, KV head); all counts below n_items < 2^31
+  int n = groups * full_c;
+  if (r < n) return (r / full_c) * pairs_c + r % full_c;
+  r -= n;
+  if (half_c) {
+    if (r < groups) return r * pairs_c + pairs_c - 1;
+    r -= groups;
+  }
+  n = groups * full_w;
+  if (r < n) return p.n_chunk_items + (r / full_w) * pairs_w + r % full_w;
+  r -= n;
+  return p.n_chunk_items + r * pairs_w + pairs_w - 1;
+}
+
+// The k-th work item of this CTA, or -1 past its last.  Decode: the items
+// strided over the grid.  Prefill: the items in cost order dealt back and
+// forth over the CTAs (rank k G + b on even rounds, k G + G - 1 - b on odd
+// ones), which evens out the CTAs' totals.
+template <bool kPrefill>
+__device__ __forceinline__ int nth_item(const AttnParams& p, int k) {
+  const int grid = static_cast<int>(gridDim.x);
+  if constexpr (!kPrefill) {
+    const int idx = static_cast<int>(blockIdx.x) + k * grid;   // n_items < 2^31
+    return idx < p.n_items ? idx : -1;
+  } else {
+    const int b = static_cast<int>(blockIdx.x);
+    const int r = k * grid + ((k & 1) ? grid - 1 - b : b);
+    return r < p.n_items ? prefill_item_of_rank(p, r) : -1;
+  }
+}
+
 template <int D>
 struct Layout {
   static constexpr uint32_t kTileBytes = 128u * D * 2u;   // Q, K or V tile
@@ -316,7 +354,6 @@ attention_kernel(const __grid_constant__ AttnParams p) {
   // inputs may come from the previous kernel on the stream.
   grid_dependency_wait();
   const uint32_t tmem = sh.tmem_base;
-  const int n_items = p.n_items;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------ TMA producer --
@@ -324,7 +361,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
     uint32_t tile_ctr = 0;   // tiles published
     int items_done = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+    for (int kk = 0, idx; ok && (idx = nth_item<kPrefill>(p, kk)) >= 0; ++kk) {
       Item it;
       if (!resolve_item(p, idx, it)) {
         if (lane == 0 && item_shape_error(p, idx)) raise_dev_err(p.dev_err, PFD_DEVERR_SHAPE);
@@ -435,7 +472,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
       int items_done = 0;
       bool ok = true;
       const uint32_t q_bytes = static_cast<uint32_t>(q_rows) * D * 2;
-      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+      for (int kk = 0, idx; ok && (idx = nth_item<kPrefill>(p, kk)) >= 0; ++kk) {
         Item it;
         if (!resolve_item(p, idx, it)) continue;
         // The Q buffers are free once the previous item's last QK has run.
@@ -468,7 +505,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
       int items_done = 0;
       bool ok = true;
       constexpr uint32_t idesc_o = idesc_bf16(kBlockM, D, false, true);
-      for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+      for (int kk = 0, idx; ok && (idx = nth_item<kPrefill>(p, kk)) >= 0; ++kk) {
         Item it;
         if (!resolve_item(p, idx, it)) continue;
         const bool with_pv = it.kind != kWindow;
@@ -612,7 +649,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
     uint32_t tile_ctr = 0, ring_ctr = 0, s_ph = 0;
     int items_done = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; ok && idx < n_items; idx += gridDim.x) {
+    for (int kk = 0, idx; ok && (idx = nth_item<kPrefill>(p, kk)) >= 0; ++kk) {
       Item it;
       if (!resolve_item(p, idx, it)) continue;
       const bool with_pv = it.kind != kWindow;
