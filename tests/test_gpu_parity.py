@@ -178,6 +178,61 @@ def test_running_max_jumps_between_tiles():
         assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= P.LSE_MAX_ABS
 
 
+def _spike(k, rows, u, size):
+    k = k.float().clone()
+    for r in rows:
+        k[r] = size * u
+    return k.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("size", [40.0, 100.0])
+def test_logit_spike_in_later_tile(size):
+    """A key far above every earlier logit of its row (about 2^72 above the
+    running max for size 100, 2^29 for size 40) in the first and in the
+    second 64-key half of later tiles, for some rows of a warp and not for
+    others: the O rescale and the per-row reference stay exact."""
+    cfg = wl.scaled(wl.TINY, n_chunks=2, chunk_size=700, n_keep=200, n_select=2, n_win=16,
+                    n_resp=48)
+    req = wl.make_request(cfg, 0)
+    gen = torch.Generator().manual_seed(11)
+    d = cfg.head_dim
+    u = torch.randn(d, generator=gen)
+    u = u / u.norm()
+    rows = cfg.chunk_size + 1
+    # content row r is key r - 1 of the tensor-core pipeline: tile (r-1)//128,
+    # column (r-1)%128 -> half 0 of tile 2 (row 1+256+10), half 1 of tile 4
+    # (row 1+512+100), and half 1 of chunk 1's tile 1 (row 1+128+70)
+    spikes = [1 + 256 + 10, 1 + 512 + 100, rows + 1 + 128 + 70]
+    req["k"] = torch.stack([_spike(req["k"][:, h], spikes, u, size)
+                            for h in range(cfg.n_kv_heads)], dim=1)
+    qf = req["q"].float() + 4.0 * u
+    req["q"] = qf.to(torch.bfloat16)
+    res = P.run_prefill(cfg, req)
+    assert int(res["dev_err"][0]) == 0
+    o_ref = orc.chunk_attention(f64(req["q"]), f64(req["k"]), f64(req["v"]), cfg.n_chunks,
+                                cfg.chunk_size, cfg.sm_scale)
+    P.assert_close_out(res["out"].double().numpy(), o_ref, f"prefill out (spike {size})")
+    s_ref = orc.window_scores(f64(req["q_win"]), f64(req["k"]), cfg.n_chunks, cfg.chunk_size,
+                              cfg.sm_scale)
+    s_gpu = res["scores"].double().numpy()
+    tol = P.SCORE_RTOL * np.abs(s_ref) + 1e-6 * cfg.n_win * cfg.n_q_heads
+    assert (np.abs(s_gpu - s_ref) <= tol).all(), f"scores: max diff {np.abs(s_gpu - s_ref).max()}"
+    # decode: spikes in the live keys (the last tiles of the single split)
+    pk, pv, table = P.oracle_pool(cfg, req, orc.top_b(s_ref, cfg.n_keep), res["slot_row"],
+                                  res["pool_rows"])
+    sel = np.array([1, 0], dtype=np.int32)
+    ql, kl, vl = wl.live_block(req, wl.make_step(cfg, 0, 0))
+    ql = (ql.float() + 4.0 * u).to(torch.bfloat16)
+    kl = torch.stack([_spike(kl[:, h], [5, 40], u, size) for h in range(cfg.n_kv_heads)], dim=1)
+    o_ref, lse_ref = orc.decode_attention(f64(ql), f64(kl), f64(vl), pk, pv, table, sel, cfg.sm_scale)
+    for n_splits in (1, 2):
+        out, lse = api.decode_attention(P.cuda(ql), P.cuda(kl), P.cuda(vl), P.cuda(P.bf16_of(pk)),
+                                        P.cuda(P.bf16_of(pv)), P.cuda(torch.from_numpy(table)),
+                                        P.cuda(torch.from_numpy(sel)), n_splits=n_splits)
+        P.assert_close_out(out.cpu().double().numpy(), o_ref, f"decode out (spike {size})")
+        assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= P.LSE_MAX_ABS
+
+
 def test_decode_batched_shared_pool():
     """Three sequences with different chunk sizes and live lengths in one pool."""
     cfgs = [wl.scaled(wl.TINY, chunk_size=c, n_keep=b, n_select=k, n_resp=r, n_chunks=n)
