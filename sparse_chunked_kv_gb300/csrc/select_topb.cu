@@ -58,6 +58,7 @@ topb_compact_kernel(const TopBParams p) {
   __shared__ int warp_sums[33];
   __shared__ uint32_t sel_prefix;
   __shared__ int sel_remaining;
+  __shared__ int sel_eq_total;   // keys equal to the threshold (last round)
 
   grid_dependency_wait();
   grid_dependents_launch();
@@ -124,6 +125,7 @@ topb_compact_kernel(const TopBParams p) {
             if (above + static_cast<int>(cnt[b]) >= remaining) {
               sel_prefix = prefix | (static_cast<uint32_t>(255 - 8 * lane - b) << shift);
               sel_remaining = remaining - above;
+              sel_eq_total = static_cast<int>(cnt[b]);
               break;
             }
             above += static_cast<int>(cnt[b]);
@@ -139,13 +141,19 @@ topb_compact_kernel(const TopBParams p) {
     need_eq = remaining;
   }
 
-  // 3. Kept flags in index order, then their positions.
-  int n_eq = 0;
-#pragma unroll
-  for (int u = 0; u < kMaxPerThread; ++u)
-    if (u < per && i0 + u < C && key[u] == thr) ++n_eq;
+  // 3. Kept flags in index order, then their positions.  Keys equal to the
+  // threshold are kept lowest index first; when all of them are kept (the
+  // B-th largest score is unique, say) their ranks are not needed.
+  const bool all_eq = !(B > 0 && B < C) || sel_eq_total == need_eq;
   int total;
-  const int eq_base = block_exclusive_scan(n_eq, warp_sums, total);
+  int eq_base = 0;
+  if (!all_eq) {
+    int n_eq = 0;
+#pragma unroll
+    for (int u = 0; u < kMaxPerThread; ++u)
+      if (u < per && i0 + u < C && key[u] == thr) ++n_eq;
+    eq_base = block_exclusive_scan(n_eq, warp_sums, total);
+  }
   uint32_t kept_mask = 0u;
   int n_kept = 0, eq_seen = 0;
 #pragma unroll
@@ -155,7 +163,7 @@ topb_compact_kernel(const TopBParams p) {
     if (B == 0) kept = false;
     else if (B >= C) kept = true;
     else if (key[u] > thr) kept = true;
-    else if (key[u] == thr) kept = (eq_base + eq_seen++) < need_eq;
+    else if (key[u] == thr) kept = all_eq || (eq_base + eq_seen++) < need_eq;
     else kept = false;
     if (kept) {
       kept_mask |= 1u << u;

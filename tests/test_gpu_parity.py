@@ -178,6 +178,36 @@ def test_running_max_jumps_between_tiles():
         assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= P.LSE_MAX_ABS
 
 
+def test_prefill_exact_ties_keep_lowest_indices():
+    """Exact score ties at the B-th place are broken towards the lower token
+    index.  Chunk 0: all C content keys identical, so every content score
+    ties and the kept tokens are 0..B-1.  Chunk 1: the key ranked B-th is
+    copied onto the key ranked B+1-th, two exactly equal scores; when they
+    straddle the B-th place, the lower index is kept."""
+    cfg = wl.scaled(wl.TINY, n_chunks=2, chunk_size=300, n_keep=77, n_win=8)
+    req = wl.make_request(cfg, 0)
+    rows = cfg.chunk_size + 1
+    k = req["k"].clone()
+    k[1:rows] = k[1]
+    s_ref = orc.window_scores(f64(req["q_win"]), f64(k), cfg.n_chunks, cfg.chunk_size,
+                              cfg.sm_scale)
+    order = np.argsort(-s_ref[1, 1:], kind="stable")
+    b_th, nxt = int(order[cfg.n_keep - 1]), int(order[cfg.n_keep])
+    k[rows + 1 + nxt] = k[rows + 1 + b_th]
+    res = P.run_prefill(cfg, {**req, "k": k})
+    assert int(res["dev_err"][0]) == 0
+    assert res["kept_idx"][0].tolist() == list(range(cfg.n_keep))
+    s2 = orc.window_scores(f64(req["q_win"]), f64(k), cfg.n_chunks, cfg.chunk_size,
+                           cfg.sm_scale)
+    assert s2[1, 1 + b_th] == s2[1, 1 + nxt]
+    P.check_kept(res["kept_idx"].numpy(), s2, cfg.n_keep)
+    lo, hi = min(b_th, nxt), max(b_th, nxt)
+    ref = set(orc.top_b(s2, cfg.n_keep)[1].tolist())
+    kept = set(res["kept_idx"][1].tolist())
+    if (lo in ref) != (hi in ref):                 # the tie straddles the B-th place
+        assert lo in kept and hi not in kept
+
+
 def _spike(k, rows, u, size):
     k = k.float().clone()
     for r in rows:
