@@ -318,21 +318,41 @@ def run_e2e(args, r, stream):
     h_q, h_k, h_v = pin(r.host["q"]), pin(r.host["k"]), pin(r.host["v"])
     h_qw, h_si, h_sp, h_slot = pin(r.host["q_win"]), pin(r.host["s_i"]), pin(r.host["s_p"]), \
         pin(r.host["slot_row"])
-    h_live = [tuple(pin(x.cpu()) for x in blk) for blk in r.live]
+    # Each step's live q, k, v travel as one pinned block (one copy a step)
+    # into one of N_LIVE device blocks, so the copies can run up to
+    # N_LIVE - 1 steps ahead of the kernels.
+    n_live = 4
+    shapes = [x.shape for x in r.live[0]]
+    sizes = [x.numel() for x in r.live[0]]
+
+    def views(flat):
+        out, off = [], 0
+        for shp, n in zip(shapes, sizes):
+            out.append(flat[off:off + n].view(shp))
+            off += n
+        return tuple(out)
+
+    h_live = []
+    for blk in r.live:
+        flat = torch.empty(sum(sizes), dtype=torch.bfloat16).pin_memory()
+        for dst, x in zip(views(flat), blk):
+            dst.copy_(x.cpu())
+        h_live.append(flat)
     h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in r.dec_out]
-    d_live = [tuple(torch.empty_like(x) for x in r.live[0]) for _ in range(2)]
+    d_flat = [torch.empty(sum(sizes), dtype=torch.bfloat16, device=r.q.device) for _ in range(n_live)]
+    d_live = [views(f) for f in d_flat]
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_qw, h_si, h_sp, h_slot))
-    h2d += sum(x.numel() * x.element_size() for blk in h_live for x in blk)
+    h2d += sum(x.numel() * x.element_size() for x in h_live)
     d2h = sum(o.numel() * o.element_size() for o in h_out)
 
     # Copies run on their own streams so that they overlap the kernels: the
-    # inputs of decode step t+1 go up while step t computes, and step t's
-    # output comes down while step t+1 computes.  Two device buffers hold the
-    # live inputs; every copy stays inside the timed region.
+    # inputs of the next decode steps go up while step t computes, and step
+    # t's output comes down while step t+1 computes.  Every copy stays inside
+    # the timed region.
     copy_s = torch.cuda.Stream(stream.device)
     d2h_s = torch.cuda.Stream(stream.device)
-    h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
-    dec_done = [torch.cuda.Event(), torch.cuda.Event()]
+    h2d_done = [torch.cuda.Event() for _ in range(n_live)]
+    dec_done = [torch.cuda.Event() for _ in range(n_live)]
 
     def step(ev):
         with torch.cuda.stream(stream):
@@ -352,15 +372,12 @@ def run_e2e(args, r, stream):
             ev[1].record(stream)
         copy_s.wait_stream(stream)          # decode copies start after the prefill
         for t in range(cfg.n_steps):
-            b = t & 1
+            b = t % n_live
             dq, dk, dv = d_live[b]
-            hq, hk, hv = h_live[t]
             with torch.cuda.stream(copy_s):
-                if t >= 2:
-                    copy_s.wait_event(dec_done[b])   # step t-2 is done with buffer b
-                dq.copy_(hq, non_blocking=True)
-                dk.copy_(hk, non_blocking=True)
-                dv.copy_(hv, non_blocking=True)
+                if t >= n_live:
+                    copy_s.wait_event(dec_done[b])   # step t - n_live is done with block b
+                d_flat[b].copy_(h_live[t], non_blocking=True)
                 h2d_done[b].record(copy_s)
             with torch.cuda.stream(stream):
                 stream.wait_event(h2d_done[b])
@@ -408,15 +425,12 @@ def run_e2e(args, r, stream):
         copy_s.wait_stream(stream)
         d2h_s.wait_stream(stream)
         for t in range(cfg.n_steps):
-            b = t & 1
+            b = t % n_live
             dq, dk, dv = d_live[b]
-            hq, hk, hv = h_live[t]
             with torch.cuda.stream(copy_s):
-                if t >= 2:
+                if t >= n_live:
                     copy_s.wait_event(dec_done[b])
-                dq.copy_(hq, non_blocking=True)
-                dk.copy_(hk, non_blocking=True)
-                dv.copy_(hv, non_blocking=True)
+                d_flat[b].copy_(h_live[t], non_blocking=True)
                 h2d_done[b].record(copy_s)
             with torch.cuda.stream(stream):
                 stream.wait_event(h2d_done[b])
