@@ -134,6 +134,24 @@ def test_decode_parity(cfg_name, n_splits):
     assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= P.LSE_MAX_ABS
 
 
+@pytest.mark.parametrize("n_splits", [2, 3, 4, 5])
+def test_decode_odd_pair_count(n_splits):
+    """3 query heads on 1 KV head over 37 live rows: 111 (row, head) pairs, so the
+    merge's last warp holds a single pair when it takes two per warp."""
+    cfg = wl.scaled(wl.TINY, n_q_heads=3, n_kv_heads=1, n_win=16, n_resp=21)
+    _, pk, pv, table, sel, ql, kl, vl = _decode_inputs(cfg)
+    assert ql.shape[0] * ql.shape[1] % 2 == 1
+    o_ref, lse_ref = orc.decode_attention(f64(ql), f64(kl), f64(vl), pk, pv, table, sel, cfg.sm_scale)
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = api.decode_attention(P.cuda(ql), P.cuda(kl), P.cuda(vl), P.cuda(P.bf16_of(pk)),
+                                    P.cuda(P.bf16_of(pv)), P.cuda(torch.from_numpy(table)),
+                                    P.cuda(torch.from_numpy(sel)), n_splits=n_splits, dev_err=dev_err)
+    torch.cuda.synchronize()
+    assert int(dev_err.item()) == 0
+    P.assert_close_out(out.cpu().double().numpy(), o_ref, "decode out (odd pairs)")
+    assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= P.LSE_MAX_ABS
+
+
 def test_decode_nan_padding_is_masked():
     cfg = wl.scaled(wl.TINY, n_keep=57, n_select=3)     # 58-row slots: ragged 16-row groups
     _, pk, pv, table, sel, ql, kl, vl = _decode_inputs(cfg, pad=7, fill=float("nan"))
