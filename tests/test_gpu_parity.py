@@ -51,6 +51,34 @@ def test_prefill_parity(name, cfg):
     P.check_pool(cfg, req, res)
 
 
+def test_prefill_by_chunk_ranges_matches_one_call():
+    """Chunks are independent up to selection: calling the prefill once per
+    range of chunks (as a caller overlapping input copies would) gives the
+    same bits as one call, into one shared pool."""
+    cfg = wl.scaled(wl.CTX_8K, n_chunks=5, chunk_size=100, n_keep=37, n_win=7)
+    req = wl.make_request(cfg, 2)
+    rows = cfg.chunk_size + 1
+    slot = req["slot_row"].to(torch.int32)
+    q, k, v, qw = (P.cuda(req[x]) for x in ("q", "k", "v", "q_win"))
+    whole = api.chunk_prefill(q, k, v, qw, cfg.n_chunks, cfg.chunk_size, cfg.n_keep, P.cuda(slot),
+                              cfg.pool_rows)
+    pk = torch.zeros_like(whole["pool_k"])
+    pv = torch.zeros_like(whole["pool_v"])
+    parts = []
+    for j0, j1 in ((0, 2), (2, 3), (3, 5)):
+        r0, r1 = j0 * rows, j1 * rows
+        parts.append(api.chunk_prefill(q[r0:r1], k[r0:r1], v[r0:r1], qw, j1 - j0, cfg.chunk_size,
+                                       cfg.n_keep, P.cuda(slot[j0:j1]), cfg.pool_rows,
+                                       pool_k=pk, pool_v=pv))
+    torch.cuda.synchronize()
+    bits = {torch.bfloat16: torch.int16, torch.float32: torch.int32, torch.int32: torch.int32}
+    for key in ("out", "scores", "kept_idx", "table"):
+        got = torch.cat([part[key] for part in parts])
+        assert torch.equal(got.view(bits[got.dtype]), whole[key].view(bits[got.dtype])), key
+    assert torch.equal(pk.view(torch.int16), whole["pool_k"].view(torch.int16))
+    assert torch.equal(pv.view(torch.int16), whole["pool_v"].view(torch.int16))
+
+
 def test_prefill_pool_padding_untouched():
     cfg = wl.scaled(wl.TINY, n_chunks=4, chunk_size=80, n_keep=20)
     req = wl.make_request(cfg, 3)
