@@ -311,9 +311,7 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
   tp.n_keep = B;
   tp.Hkv = Hkv;
   tp.D = D;
-  const int want = ceil_div(2 * device_sm_count(), N);
-  tp.copy_splits = std::max(1, std::min(want, std::max(1, (B + 1) / 16)));
-  return from_cuda(launch_topb_compact(tp, st));
+  return from_cuda(launch_topb_compact(tp, st));   // sets the copy splits
 }
 
 pfd_status pfd_select_chunks(const float* s_I, const float* s_P, int N, int K, int32_t* sel,

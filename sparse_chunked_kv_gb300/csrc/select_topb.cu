@@ -51,6 +51,35 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int& 
   return res;
 }
 
+// 4. Chunk table and the copy of BOS + kept rows (kept_src, slot order) into
+// chunk j's pool slot; CTA `part` of copy_splits copies its share of the rows.
+__device__ __forceinline__ void copy_kept_rows(const TopBParams& p, int j, int part, int rows,
+                                               const int* kept_src, int tid) {
+  const int B = p.n_keep;
+  const long long slot = p.slot_row[j];
+  const bool slot_ok = slot >= 0 && slot + B + 1 <= p.pool_rows;
+  if (part == 0 && tid == 0) {
+    pfd_chunk_entry e;
+    e.row = slot_ok ? static_cast<int32_t>(slot) : 0;
+    e.len = slot_ok ? B + 1 : 0;
+    p.table[j] = e;
+    if (!slot_ok) raise_dev_err(p.dev_err, PFD_DEVERR_SLOT);
+  }
+  if (!slot_ok) return;
+  const int n_rows_out = B + 1;
+  const int r0 = static_cast<int>(static_cast<long long>(n_rows_out) * part / p.copy_splits);
+  const int r1 = static_cast<int>(static_cast<long long>(n_rows_out) * (part + 1) / p.copy_splits);
+  const int units = p.Hkv * p.D / 8;  // 16-byte units per token row
+  const long long chunk_row0 = static_cast<long long>(j) * rows;
+  for (int idx = tid; idx < (r1 - r0) * units; idx += kTopBThreads) {
+    const int r = r0 + idx / units, u = idx % units;
+    const long long src = (chunk_row0 + kept_src[r]) * units + u;
+    const long long dst = (slot + r) * units + u;
+    reinterpret_cast<uint4*>(p.pool_k)[dst] = __ldg(reinterpret_cast<const uint4*>(p.k) + src);
+    reinterpret_cast<uint4*>(p.pool_v)[dst] = __ldg(reinterpret_cast<const uint4*>(p.v) + src);
+  }
+}
+
 __global__ void __launch_bounds__(kTopBThreads)
 topb_compact_kernel(const TopBParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -181,29 +210,7 @@ topb_compact_kernel(const TopBParams p) {
   }
   __syncthreads();
 
-  // 4. Chunk table and the copy of BOS + kept rows into the slot.
-  const long long slot = p.slot_row[j];
-  const bool slot_ok = slot >= 0 && slot + B + 1 <= p.pool_rows;
-  if (part == 0 && tid == 0) {
-    pfd_chunk_entry e;
-    e.row = slot_ok ? static_cast<int32_t>(slot) : 0;
-    e.len = slot_ok ? B + 1 : 0;
-    p.table[j] = e;
-    if (!slot_ok) raise_dev_err(p.dev_err, PFD_DEVERR_SLOT);
-  }
-  if (!slot_ok) return;
-  const int n_rows_out = B + 1;
-  const int r0 = static_cast<int>(static_cast<long long>(n_rows_out) * part / p.copy_splits);
-  const int r1 = static_cast<int>(static_cast<long long>(n_rows_out) * (part + 1) / p.copy_splits);
-  const int units = p.Hkv * p.D / 8;  // 16-byte units per token row
-  const long long chunk_row0 = static_cast<long long>(j) * rows;
-  for (int idx = tid; idx < (r1 - r0) * units; idx += kTopBThreads) {
-    const int r = r0 + idx / units, u = idx % units;
-    const long long src = (chunk_row0 + kept_src[r]) * units + u;
-    const long long dst = (slot + r) * units + u;
-    reinterpret_cast<uint4*>(p.pool_k)[dst] = __ldg(reinterpret_cast<const uint4*>(p.k) + src);
-    reinterpret_cast<uint4*>(p.pool_v)[dst] = __ldg(reinterpret_cast<const uint4*>(p.v) + src);
-  }
+  copy_kept_rows(p, j, part, rows, kept_src, tid);
 }
 
 constexpr int kSelectThreads = 1024;
@@ -240,11 +247,26 @@ select_kernel(const float* __restrict__ s_i, const float* __restrict__ s_p,
 
 }  // namespace
 
-cudaError_t launch_topb_compact(const TopBParams& p, cudaStream_t stream) {
+// Launches (n_chunks x copy_splits) CTAs, with copy_splits chosen here from
+// the kernel's occupancy so that the grid is about one resident wave.
+cudaError_t launch_topb_compact(const TopBParams& params, cudaStream_t stream) {
+  TopBParams p = params;
+  int dev = 0, sm_count = 1;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sm_count = 1;
   const int rows = p.chunk_size + 1;
   const size_t smem = static_cast<size_t>((rows * 4 + 15) & ~15) + static_cast<size_t>(p.n_keep + 1) * 4;
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(topb_compact_kernel), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
+  // Every CTA of a chunk redoes the selection and copies a share of its rows
+  // (at least 16 rows each): as many CTAs per chunk as one resident wave holds.
+  int per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topb_compact_kernel, kTopBThreads,
+                                                    smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const int wave = std::max(sm_count, 1) * per_sm;
+  p.copy_splits = std::max(1, std::min(wave / std::max(p.n_chunks, 1), std::max(1, (p.n_keep + 1) / 16)));
   dim3 grid(p.n_chunks, p.copy_splits);
   return launch_pdl(topb_compact_kernel, grid, dim3(kTopBThreads), smem, stream, p);
 }

@@ -24,6 +24,8 @@ PREFILL_CASES = [
     ("keep_none", wl.scaled(wl.TINY, n_chunks=3, chunk_size=48, n_keep=0, n_select=2)),
     ("no_window", wl.scaled(wl.TINY, n_chunks=2, chunk_size=64, n_keep=10, n_win=0, n_resp=17)),
     ("one_token_chunks", wl.scaled(wl.TINY, n_chunks=5, chunk_size=1, n_keep=1, n_win=3)),
+    ("d64_c1500", wl.scaled(wl.TINY, n_chunks=2, chunk_size=1500, n_keep=400, n_win=5)),
+    ("c1024_keep_all_but_one", wl.scaled(wl.TINY, n_chunks=2, chunk_size=1024, n_keep=1023, n_win=4)),
 ]
 
 
@@ -224,13 +226,15 @@ def test_running_max_jumps_between_tiles():
         assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= P.LSE_MAX_ABS
 
 
-def test_prefill_exact_ties_keep_lowest_indices():
+# Chunks of one and of two keys per selecting thread.
+@pytest.mark.parametrize("chunk_size,n_keep", [(300, 77), (1200, 301)])
+def test_prefill_exact_ties_keep_lowest_indices(chunk_size, n_keep):
     """Exact score ties at the B-th place are broken towards the lower token
     index.  Chunk 0: all C content keys identical, so every content score
     ties and the kept tokens are 0..B-1.  Chunk 1: the key ranked B-th is
     copied onto the key ranked B+1-th, two exactly equal scores; when they
     straddle the B-th place, the lower index is kept."""
-    cfg = wl.scaled(wl.TINY, n_chunks=2, chunk_size=300, n_keep=77, n_win=8)
+    cfg = wl.scaled(wl.TINY, n_chunks=2, chunk_size=chunk_size, n_keep=n_keep, n_win=8)
     req = wl.make_request(cfg, 0)
     rows = cfg.chunk_size + 1
     k = req["k"].clone()
