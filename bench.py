@@ -559,6 +559,21 @@ def run_reference(args, cfg, rank):
 METRIC = "decode-step attention µs & TFLOP/s vs BF16 peak; chunk-prefill GB/s vs HBM peak"
 
 
+def max_over_ranks(values, device):
+    """Each timing's maximum over all ranks of the default process group
+    (every rank receives the result): the job is as slow as its slowest rank."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_tflops(world, flops_per_call, calls, ms):
+    """Whole-job throughput: every rank ran `calls` calls of `flops_per_call`
+    in at most `ms` milliseconds (weak scaling: fixed work per rank)."""
+    return world * flops_per_call * calls / (ms * 1e-3) / 1e12
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -576,9 +591,8 @@ def main():
     device = torch.device("cuda", local if world > 1 else 0)
     res = run_gpu(args, cfg, rank, world, device)
     if world > 1:
-        t = torch.tensor([res["dec_ms"], res["pre_ms"], res["step_ms"]], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        res["dec_ms"], res["pre_ms"], res["step_ms"] = [float(x) for x in t.tolist()]
+        res["dec_ms"], res["pre_ms"], res["step_ms"] = max_over_ranks(
+            [res["dec_ms"], res["pre_ms"], res["step_ms"]], device)
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -587,7 +601,7 @@ def main():
     T = cfg.n_steps
     dec_us = res["dec_ms"] * 1e3 / T                       # one decode call (attention + merge)
     dflops = decode_flops(cfg)
-    value = world * dflops * T / (res["dec_ms"] * 1e-3) / 1e12
+    value = job_tflops(world, dflops, T, res["dec_ms"])
     per_launch_tflops = dflops / (dec_us * 1e-6) / 1e12
     sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     pre_gbs = prefill_bytes(cfg) / (res["pre_ms"] * 1e-3) / 1e9
@@ -628,14 +642,14 @@ def main():
     }
     if "e2e" in res:
         e = res["e2e"]
-        line["e2e"] = {"value": world * dflops * T / (e["dec_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+        line["e2e"] = {"value": job_tflops(world, dflops, T, e["dec_ms"]), "unit": "TFLOP/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                        "prefill_ms": e["pre_ms"], "decode_ms": e["dec_ms"],
                        "path": ("C ABI calls (prefill + select, then one decode call per step) "
                                 "captured in CUDA graphs with every step's H2D copies from pinned "
                                 "host memory and D2H of its output as graph nodes on copy "
                                 "streams that overlap the kernels"),
-                       "eager_value": world * dflops * T / (e["eager_dec_ms"] * 1e-3) / 1e12,
+                       "eager_value": job_tflops(world, dflops, T, e["eager_dec_ms"]),
                        "eager_decode_ms": e["eager_dec_ms"],
                        "eager_path": "the same calls and copies issued from Python every step"}
     if world == 1 and not args.no_cpu_baseline:
