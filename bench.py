@@ -145,10 +145,15 @@ class ClockSampler:
 # ------------------------------------------------------- traffic record --
 
 def kernel_source_hash():
+    """Hash of the decode kernels' source with comments and whitespace removed,
+    so that a profile stays matched to its code across comment edits."""
     h = hashlib.sha256()
     for name in ("attn_tc.cu", "sm103_ptx.cuh", "pfd_internal.cuh", "lse_merge.cu"):
-        with open(os.path.join(ROOT, "sparse_chunked_kv_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "sparse_chunked_kv_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

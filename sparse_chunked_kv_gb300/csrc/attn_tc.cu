@@ -27,8 +27,8 @@
 //   warp 0      TMA producer of K and V tiles into a 4-slot ring (K(j), V(j),
 //               K(j+1), ...), so loads run two tiles ahead, also across item
 //               boundaries; it also publishes each tile's group metadata;
-//   warp 10     TMA loader of the item's two Q tiles (once the previous
-//               item's last QK has read the Q buffers);
+//   warp 10     TMA loader of the item's two Q tiles (once every MMA of the
+//               previous item, the last QK included, has completed);
 //   warp 1      TMEM owner and single-thread MMA issuer, ping-ponging the two
 //               query tiles:  QK_a(0) QK_b(0) | PV_a(j) QK_a(j+1) PV_b(j)
 //               QK_b(j+1) | ...  so the tensor core works on one tile while
@@ -475,10 +475,11 @@ attention_kernel(const __grid_constant__ AttnParams p) {
       for (int kk = 0, idx; ok && (idx = nth_item<kPrefill>(p, kk)) >= 0; ++kk) {
         Item it;
         if (!resolve_item(p, idx, it)) continue;
-        // The Q buffers are free once the previous item's last QK has run.
-        // Its MMAs include PVs that needed the softmax of this item's
-        // predecessor done, so the BOS buffer of this parity (last read by the
-        // epilogue two items back) is free as well.
+        // The Q buffers are free once every MMA of the previous item has
+        // completed (q_empty), its last QK included.  Its first PV was issued
+        // only after the epilogue two items back had released O (o_free), so
+        // the BOS buffer of this parity, last read by that epilogue, is free
+        // as well.
         if (items_done > 0 && !mbar_wait(&sh.q_empty, (items_done - 1) & 1)) { ok = false; break; }
         const int n_bos = !kPrefill ? 0 : it.kind == kChunk ? 2 : 1;   // K (and V) rows
         mbar_arrive_expect_tx(&sh.q_full, (it.has_b ? 2 * q_bytes : q_bytes) + n_bos * L::kBosBox);
