@@ -5,7 +5,8 @@
 // For one (row, head) with partials (m_s, l_s, O_s = acc_s / l_s), m in log2
 // units:  M = max_s m_s,  w_s = 2^(m_s - M) l_s,  L = sum_s w_s,
 //         out = sum_s w_s O_s / L,  lse = (M + log2 L) * ln 2.
-// One warp per (row, head); each lane owns 4 consecutive columns of D.
+// Up to four splits, a warp merges two (row, head) pairs; more, one pair.  Each
+// lane owns 4 consecutive columns of D.
 #include <algorithm>
 #include <atomic>
 
