@@ -144,12 +144,13 @@ class ClockSampler:
 
 # ------------------------------------------------------- traffic record --
 
-def kernel_source_hash():
+def kernel_source_hash(csrc=None):
     """Hash of the decode kernels' source with comments and whitespace removed,
     so that a profile stays matched to its code across comment edits."""
+    csrc = csrc or os.path.join(ROOT, "sparse_chunked_kv_gb300", "csrc")
     h = hashlib.sha256()
     for name in ("attn_tc.cu", "sm103_ptx.cuh", "pfd_internal.cuh", "lse_merge.cu"):
-        with open(os.path.join(ROOT, "sparse_chunked_kv_gb300", "csrc", name)) as f:
+        with open(os.path.join(csrc, name)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
         text = re.sub(r"//[^\n]*", " ", text)

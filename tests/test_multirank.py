@@ -71,3 +71,4 @@ def test_job_throughput_counts_every_rank():
     one = bench.job_tflops(1, 6.0e9, 64, 2.0)
     assert abs(one - 6.0e9 * 64 / 2.0e-3 / 1e12) < 1e-9
     assert abs(bench.job_tflops(2, 6.0e9, 64, 2.0) - 2 * one) < 1e-9
+
