@@ -25,8 +25,11 @@
  *   - Every call is asynchronous on `stream` (NULL = the legacy default
  *     stream).  The return value reports only what the host can check:
  *     invalid arguments (PFD_ERR_INVALID_ARG), shapes outside the supported
- *     set (PFD_ERR_UNSUPPORTED) and launch failures (PFD_ERR_CUDA).  Nothing
- *     is launched when the return value is not PFD_OK.
+ *     set (PFD_ERR_UNSUPPORTED) and CUDA failures (PFD_ERR_CUDA).  Nothing is
+ *     launched when a call returns PFD_ERR_INVALID_ARG or PFD_ERR_UNSUPPORTED,
+ *     or fails to encode a TMA tensor map.  A call made of several kernels
+ *     that returns PFD_ERR_CUDA from a later launch may have queued the
+ *     earlier ones; its outputs are then undefined.
  *   - Errors found in device-resident data (a chunk-table entry, a selected
  *     index or a pool slot out of range) never trap: the offending item is
  *     skipped and a PFD_DEVERR_* bit is OR-ed into *dev_err when dev_err is

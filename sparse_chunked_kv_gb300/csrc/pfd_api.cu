@@ -261,15 +261,22 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
       static_cast<long long>(ap.n_chunk_items) + static_cast<long long>(N) * Hkv * ceil_div(ap.mt_win, 2);
   if (items >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
   ap.n_items = static_cast<int>(items);
+  // Every tensor map is encoded before the first launch, so that a failure
+  // to encode one launches nothing.
+  WinScoreParams wp;
+  std::memset(&wp, 0, sizeof(wp));
+  wp.k_tiles = ceil_div(C + 1, 128);
+  wp.concat = (C + 1 >= 128) ? 1 : 0;
+  const long long ws_items =
+      wp.concat ? (rows + 127) / 128 : static_cast<long long>(N) * wp.k_tiles;
+  if (ws_items >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
+  if (W > 0 && !make_map(&wp.tm_qwin, q_win, W, Hq, D, G, W)) return PFD_ERR_CUDA;
   const int grid = static_cast<int>(std::min<long long>(items, device_sm_count()));
   pfd_status s = from_cuda(launch_attention(ap, grid, st));
   if (s != PFD_OK) return s;
 
   if (W > 0) {
-    WinScoreParams wp;
-    std::memset(&wp, 0, sizeof(wp));
     wp.tm_k = ap.tm_k[kBoxLevels - 1][0];
-    if (!make_map(&wp.tm_qwin, q_win, W, Hq, D, G, W)) return PFD_ERR_CUDA;
     wp.q_win = ap.q_win;
     wp.win_b = ap.win_b;
     wp.win_stride = ap.win_stride;
@@ -281,11 +288,6 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
     wp.Hkv = Hkv;
     wp.G = G;
     wp.D = D;
-    wp.k_tiles = ceil_div(C + 1, 128);
-    wp.concat = (C + 1 >= 128) ? 1 : 0;
-    const long long ws_items =
-        wp.concat ? (static_cast<long long>(N) * (C + 1) + 127) / 128 : static_cast<long long>(N) * wp.k_tiles;
-    if (ws_items >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
     wp.n_items = static_cast<int>(ws_items);
     wp.scale_log2 = ap.scale_log2;
     wp.dev_err = dev_err;
