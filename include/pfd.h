@@ -118,6 +118,11 @@ size_t pfd_chunk_prefill_workspace(int N, int C, int W, int Hq, int Hkv, int D, 
  *   table        [N] pfd_chunk_entry (written)
  *   dev_err      one int32, or NULL
  *   workspace    >= pfd_chunk_prefill_workspace(...) bytes
+ *
+ * Chunks are independent: calling this once per range of chunks, with q, k,
+ * v, out, scores, kept_idx, slot_row and table offset to the range, and the
+ * same q_win and pool, gives the bits of one call.  A caller may use this to
+ * overlap the upload of later chunks with the prefill of earlier ones.
  */
 pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
                              const pfd_bf16* q_win, int N, int C, int W, int Hq, int Hkv, int D,
