@@ -1,19 +1,23 @@
 #!/usr/bin/env python
-"""Benchmark of the sparse chunked-KV hot path (one request = one step).
+"""Benchmark of the sparse chunked-KV hot path.
 
-One step runs the whole path over one synthetic request of the chosen
-workload: chunked prefill (chunk attention, window scores, top-B, compaction
-into the pool), top-K chunk selection, then T static-KV decode steps
-(split-KV attention + LSE merge).  Inputs are resident in HBM before the timed
+One step runs the whole path over one synthetic job of the chosen workload:
+chunked prefill of every sequence (chunk attention, window scores, top-B,
+compaction into one shared pool), top-K chunk selection, then T static-KV
+decode steps (split-KV attention + LSE merge), each one batched call over
+every sequence.  The default workload is the batched serving mix: eight
+sequences of a 32K prefix with chunk sizes C in {256, 1024, 4096}, the
+largest single-GPU workload.  Inputs are resident in HBM before the timed
 region; the prefill+selection and the T-step decode loop are each one CUDA
 graph replay, bracketed by CUDA events on the launching stream.  L2 is
 flushed (256 MiB write) between steps, outside the timed events.
 
 value = decode-step attention throughput (algorithmic TFLOP/s, whole job);
 extra keys give the decode step in microseconds and the chunked prefill in
-GB/s and as a fraction of the HBM roofline.  Multi-GPU (torchrun): every rank
-runs its own request (independent problems, no collective on the data path),
-value = work of all ranks / slowest rank's time.
+GB/s and as a fraction of its roofline.  `per_config` times the 8K, 32K and
+128K single-request workloads in the same run.  Multi-GPU (torchrun): every
+rank runs its own job (independent problems, no collective on the data
+path), value = work of all ranks / slowest rank's time.
 
 --impl reference times the CPU oracle on the same workload (bounded sample).
 """
@@ -34,19 +38,28 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOADS = ["tiny", "8k", "32k", "128k", "mix"]
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="pfd", choices=["pfd", "reference"])
-    ap.add_argument("--config", default="8k", choices=["tiny", "8k", "32k", "128k"])
+    ap.add_argument("--config", default="mix", choices=WORKLOADS)
+    ap.add_argument("--per-config", default="8k,32k,128k",
+                    help="other workloads timed in the same run ('' for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    return ap.parse_args()
+    return ap.parse_args(argv)
+
+
+def job_configs(name):
+    """The sequences of a workload: the mix is eight, the others one."""
+    from sparse_chunked_kv_gb300 import workloads as wl
+    return wl.mix_configs() if name == "mix" else [wl.CONFIGS[name]]
 
 
 def load_peaks():
@@ -59,6 +72,8 @@ def load_peaks():
 
 
 # ------------------------------------------------------------- cost model --
+# Algorithmic work of the method (re-reads, padding and split partials are
+# not counted).  Each takes one Config; the job totals sum over sequences.
 
 def decode_flops(cfg):
     keys = cfg.n_select * (cfg.n_keep + 1) + cfg.n_live
@@ -84,33 +99,65 @@ def prefill_bytes(cfg):
             + n * c * 4 + n * b * 4 + n * (b + 1) * 2 * hkv * d * 2 + 8 * n)
 
 
-def workload_name(cfg):
-    return (f"{cfg.name}: one layer, N={cfg.n_chunks} chunks x C={cfg.chunk_size} (+BOS), "
-            f"Hq={cfg.n_q_heads}/Hkv={cfg.n_kv_heads}, D={cfg.head_dim}, B={cfg.n_keep}, "
-            f"K={cfg.n_select}, W={cfg.n_win}, L_d={cfg.n_resp}, T={cfg.n_steps}")
+def total(fn, cfgs):
+    return sum(fn(c) for c in cfgs)
+
+
+def workload_name(name, cfgs):
+    if len(cfgs) == 1:
+        cfg = cfgs[0]
+        return (f"{cfg.name}: one layer, N={cfg.n_chunks} chunks x C={cfg.chunk_size} (+BOS), "
+                f"Hq={cfg.n_q_heads}/Hkv={cfg.n_kv_heads}, D={cfg.head_dim}, B={cfg.n_keep}, "
+                f"K={cfg.n_select}, W={cfg.n_win}, L_d={cfg.n_resp}, T={cfg.n_steps}")
+    c0 = cfgs[0]
+    per = ", ".join(f"C={c.chunk_size}: N={c.n_chunks}, B={c.n_keep}, K={c.n_select}"
+                    for c in cfgs[:3])
+    return (f"{name}: batched serving mix of {len(cfgs)} sequences x "
+            f"{c0.n_chunks * c0.chunk_size // 1024}K prefix, one layer, C cycling "
+            f"256/1024/4096 ({per}), Hq={c0.n_q_heads}/Hkv={c0.n_kv_heads}, D={c0.head_dim}, "
+            f"W={c0.n_win}, L_d={c0.n_resp}, T={c0.n_steps}; one shared permuted pool, batched "
+            f"selection, one batched decode call per step")
 
 
 # ---------------------------------------------------------------- clocks --
 
 class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons every 20 ms; only
+    the samples taken between mark_start() and mark_end() (the timed region)
+    are reported."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, interval_ms=20):
         self.index = index
+        self.interval_ms = interval_ms
         self.proc = None
         self.path = os.path.join("/tmp", f"pfd_clocks_{os.getpid()}.csv")
+        self.marks = [0, None]
 
     def start(self):
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+
+    def _lines(self):
+        self.fh.flush()
+        with open(self.path) as f:
+            return f.read().count("\n")
+
+    def mark_start(self):
+        if self.proc is not None:
+            self.marks[0] = self._lines()
+
+    def mark_end(self):
+        if self.proc is not None:
+            self.marks[1] = self._lines()
 
     def stop(self):
         if self.proc is None:
@@ -121,25 +168,31 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
+        with open(self.path) as f:
+            lines = f.read().splitlines()
+        os.unlink(self.path)
+        lo, hi = self.marks[0], self.marks[1] if self.marks[1] is not None else len(lines)
+        window = "timed region"
+        if hi - lo < 1:
+            lo, hi, window = 0, len(lines), "whole run (no sample fell inside the timed region)"
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
-                except ValueError:
-                    continue
-                for name, val in zip(names, parts[5:9]):
-                    if val.lower() == "active":
-                        reasons.add(name)
-        os.unlink(self.path)
+        for line in lines[lo:hi]:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "interval_ms": self.interval_ms, "window": window,
+                "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------- traffic record --
@@ -174,162 +227,230 @@ def recorded_traffic(profile_name, key="traffic_bytes_per_launch"):
 
 # ------------------------------------------------------------ GPU path --
 
-class Request:
-    """Device-resident buffers of one request and the calls of one step."""
+class Job:
+    """Device-resident buffers of one job (one or more sequences sharing one
+    chunk pool and chunk table) and the library calls of one step."""
 
-    def __init__(self, cfg, seq, device):
+    def __init__(self, cfgs, seq0, device):
         import torch
 
         from sparse_chunked_kv_gb300 import _abi
         from sparse_chunked_kv_gb300 import workloads as wl
-        self.cfg, self.abi, self.torch = cfg, _abi, torch
-        req = wl.make_request(cfg, seq)
-        self.host = req
+        self.cfgs, self.abi, self.torch = list(cfgs), _abi, torch
+        c0 = self.cfgs[0]
+        hq, hkv, d = c0.n_q_heads, c0.n_kv_heads, c0.head_dim
+        assert all((c.n_q_heads, c.n_kv_heads, c.head_dim, c.n_steps) == (hq, hkv, d, c0.n_steps)
+                   for c in self.cfgs)
+        self.hq, self.hkv, self.d, self.T = hq, hkv, d, c0.n_steps
+        self.batch = len(self.cfgs)
         dev = device
         cu = lambda t: t.to(dev).contiguous()  # noqa: E731
-        self.q, self.k, self.v = cu(req["q"]), cu(req["k"]), cu(req["v"])
-        self.q_win = cu(req["q_win"])
-        self.s_i, self.s_p = cu(req["s_i"]), cu(req["s_p"])
-        self.slot_row = cu(req["slot_row"])
-        self.live = []
-        for t in range(cfg.n_steps):
-            ql, kl, vl = wl.live_block(req, wl.make_step(cfg, seq, t))
-            self.live.append((cu(ql), cu(kl), cu(vl)))
-        hq, hkv, d = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
-        self.out = torch.empty_like(self.q)
-        self.scores = torch.empty(cfg.n_chunks, cfg.chunk_size + 1, dtype=torch.float32, device=dev)
-        self.kept = torch.empty(cfg.n_chunks, max(cfg.n_keep, 1), dtype=torch.int32, device=dev)
-        self.pool_k = torch.zeros(cfg.pool_rows, hkv, d, dtype=torch.bfloat16, device=dev)
+        self.host, self.seqs = [], []
+        pool_base, cu_n, cu_k, cu_lq = [0], [0], [0], [0]
+        for c in self.cfgs:
+            pool_base.append(pool_base[-1] + c.pool_rows)
+            cu_n.append(cu_n[-1] + c.n_chunks)
+            cu_k.append(cu_k[-1] + c.n_select)
+            cu_lq.append(cu_lq[-1] + c.n_live)
+        self.pool_rows, self.table_len = pool_base[-1], cu_n[-1]
+        self.cu_n_host, self.cu_k_host, self.cu_lq_host = cu_n, cu_k, cu_lq
+        self.pool_k = torch.zeros(self.pool_rows, hkv, d, dtype=torch.bfloat16, device=dev)
         self.pool_v = torch.zeros_like(self.pool_k)
-        self.table = torch.empty(cfg.n_chunks, 2, dtype=torch.int32, device=dev)
+        self.table = torch.zeros(self.table_len, 2, dtype=torch.int32, device=dev)
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.ws_bytes = _abi.pfd_chunk_prefill_workspace(cfg.n_chunks, cfg.chunk_size, cfg.n_win,
-                                                         hq, hkv, d, cfg.n_keep)
-        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
-        self.sel = torch.empty(cfg.n_select, dtype=torch.int32, device=dev)
-        self.s_out = torch.empty(cfg.n_chunks, dtype=torch.float32, device=dev)
-        lq = cfg.n_live
-        self.cu_lq_host, self.cu_k_host = [0, lq], [0, cfg.n_select]
-        self.cu_lq = torch.tensor(self.cu_lq_host, dtype=torch.int32, device=dev)
-        self.cu_k = torch.tensor(self.cu_k_host, dtype=torch.int32, device=dev)
-        self.max_len = cfg.n_keep + 1
-        self.n_splits = _abi.pfd_decode_plan_splits(1, self.cu_lq_host, self.cu_k_host, hq, hkv, d,
+        ws = 0
+        live = [[] for _ in range(self.T)]
+        for i, c in enumerate(self.cfgs):
+            req = wl.make_request(c, seq0 + i)
+            req["slot_row"] = (req["slot_row"] + pool_base[i]).to(torch.int32)
+            self.host.append(req)
+            sq = dict(cfg=c, n0=cu_n[i])
+            sq["q"], sq["k"], sq["v"] = cu(req["q"]), cu(req["k"]), cu(req["v"])
+            sq["q_win"] = cu(req["q_win"])
+            sq["slot_row"] = cu(req["slot_row"])
+            sq["out"] = torch.empty_like(sq["q"])
+            sq["scores"] = torch.empty(c.n_chunks, c.chunk_size + 1, dtype=torch.float32,
+                                       device=dev)
+            sq["kept"] = torch.empty(c.n_chunks, max(c.n_keep, 1), dtype=torch.int32, device=dev)
+            sq["ws_bytes"] = _abi.pfd_chunk_prefill_workspace(c.n_chunks, c.chunk_size, c.n_win,
+                                                              hq, hkv, d, c.n_keep)
+            ws = max(ws, sq["ws_bytes"])
+            self.seqs.append(sq)
+            for t in range(self.T):
+                live[t].append(wl.live_block(req, wl.make_step(c, seq0 + i, t)))
+        self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+        self.s_i = cu(torch.cat([h["s_i"] for h in self.host]))
+        self.s_p = cu(torch.cat([h["s_p"] for h in self.host]))
+        self.s_out = torch.empty_like(self.s_i)
+        self.sel = torch.empty(cu_k[-1], dtype=torch.int32, device=dev)
+        self.cu_n = torch.tensor(cu_n, dtype=torch.int32, device=dev)
+        self.cu_k = torch.tensor(cu_k, dtype=torch.int32, device=dev)
+        self.cu_lq = torch.tensor(cu_lq, dtype=torch.int32, device=dev)
+        self.max_n = max(c.n_chunks for c in self.cfgs)
+        self.max_len = max(c.n_keep + 1 for c in self.cfgs)
+        # live q, k, v of step t, sequences concatenated
+        self.live = [tuple(cu(torch.cat([x[j] for x in live[t]])) for j in range(3))
+                     for t in range(self.T)]
+        self.n_splits = _abi.pfd_decode_plan_splits(self.batch, cu_lq, cu_k, hq, hkv, d,
                                                     self.max_len)
-        self.dws_bytes = _abi.pfd_decode_workspace(1, self.cu_lq_host, self.cu_k_host, hq, hkv, d,
+        self.dws_bytes = _abi.pfd_decode_workspace(self.batch, cu_lq, cu_k, hq, hkv, d,
                                                    self.max_len, self.n_splits)
         self.dws = torch.empty(max(self.dws_bytes, 256), dtype=torch.uint8, device=dev)
         self.dec_out = [torch.empty_like(ql) for ql, _, _ in self.live]
-        self.dec_lse = [torch.empty(lq, hq, dtype=torch.float32, device=dev) for _ in self.live]
+        self.dec_lse = [torch.empty(cu_lq[-1], hq, dtype=torch.float32, device=dev)
+                        for _ in self.live]
 
     def launches_per_step(self):
-        cfg = self.cfg
-        prefill = 2 + (1 if cfg.n_win > 0 else 0)
-        return prefill + 1 + cfg.n_steps * (1 + (1 if self.n_splits > 1 else 0))
+        prefill = sum(2 + (1 if c.n_win > 0 else 0) for c in self.cfgs)
+        return prefill + 1 + self.T * (1 + (1 if self.n_splits > 1 else 0))
 
     def prefill_select(self):
-        cfg, a = self.cfg, self.abi
-        a.pfd_chunk_prefill(self.q, self.k, self.v, self.q_win if cfg.n_win else None, cfg.n_chunks,
-                            cfg.chunk_size, cfg.n_win, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim,
-                            cfg.n_keep, 0.0, self.out, self.scores, self.kept, self.pool_k,
-                            self.pool_v, cfg.pool_rows, self.slot_row, self.table, self.dev_err,
-                            self.ws, self.ws_bytes)
-        a.pfd_select_chunks(self.s_i, self.s_p, cfg.n_chunks, cfg.n_select, self.sel, self.s_out)
+        a, hq, hkv, d = self.abi, self.hq, self.hkv, self.d
+        for sq in self.seqs:
+            c = sq["cfg"]
+            a.pfd_chunk_prefill(sq["q"], sq["k"], sq["v"], sq["q_win"] if c.n_win else None,
+                                c.n_chunks, c.chunk_size, c.n_win, hq, hkv, d, c.n_keep, 0.0,
+                                sq["out"], sq["scores"], sq["kept"], self.pool_k, self.pool_v,
+                                self.pool_rows, sq["slot_row"], self.table[sq["n0"]:],
+                                self.dev_err, self.ws, sq["ws_bytes"])
+        if self.batch == 1:
+            c = self.cfgs[0]
+            a.pfd_select_chunks(self.s_i, self.s_p, c.n_chunks, c.n_select, self.sel, self.s_out)
+        else:
+            a.pfd_select_chunks_batched(self.s_i, self.s_p, self.cu_n, self.cu_k, self.batch,
+                                        self.max_n, self.sel, self.s_out)
 
     def decode(self, t, q=None, k=None, v=None, out=None):
-        cfg = self.cfg
         ql, kl, vl = self.live[t]
         self.abi.pfd_decode_attention(
             q if q is not None else ql, k if k is not None else kl, v if v is not None else vl,
-            self.cu_lq, self.cu_lq_host, self.pool_k, self.pool_v, cfg.pool_rows, self.table,
-            cfg.n_chunks, self.sel, self.cu_k, self.cu_k_host, 1, cfg.n_q_heads, cfg.n_kv_heads,
-            cfg.head_dim, self.max_len, 0.0, self.n_splits,
+            self.cu_lq, self.cu_lq_host, self.pool_k, self.pool_v, self.pool_rows, self.table,
+            self.table_len, self.sel, self.cu_k, self.cu_k_host, self.batch, self.hq, self.hkv,
+            self.d, self.max_len, 0.0, self.n_splits,
             out if out is not None else self.dec_out[t], self.dec_lse[t], self.dev_err, self.dws,
             self.dws_bytes)
 
 
-def run_gpu(args, cfg, rank, world, device):
+def capture(job, stream):
+    """Warms the job once eagerly, then captures its prefill+selection and
+    its T-step decode loop as two CUDA graphs."""
+    import torch
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        job.prefill_select()
+        for t in range(job.T):
+            job.decode(t)
+    torch.cuda.synchronize()
+    if int(job.dev_err.item()) != 0:
+        raise RuntimeError(f"device error word {int(job.dev_err.item())}")
+    g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_pre, stream=stream):
+        job.prefill_select()
+    with torch.cuda.graph(g_dec, stream=stream):
+        for t in range(job.T):
+            job.decode(t)
+    torch.cuda.synchronize()
+    return g_pre, g_dec
+
+
+def replay_steps(g_pre, g_dec, stream, flush, n):
+    """n steps (prefill graph, decode graph), L2 flushed between steps
+    outside the events; returns the (prefill ms, decode ms) of each."""
+    import torch
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for ev in events:
+            ev[0].record(stream)
+            g_pre.replay()
+            ev[1].record(stream)
+            g_dec.replay()
+            ev[2].record(stream)
+            flush.zero_()
+    torch.cuda.synchronize()
+    return [(e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])) for e in events]
+
+
+def run_gpu(args, cfgs, rank, world, device):
     import torch
 
     from sparse_chunked_kv_gb300 import _abi
     _abi.load()
-    r = Request(cfg, rank, device)
+    job = Job(cfgs, rank * len(cfgs), device)
     stream = torch.cuda.Stream(device)
-    torch.cuda.synchronize()
-    # warm once eagerly (kernel attributes, module load), then capture graphs
-    with torch.cuda.stream(stream):
-        r.prefill_select()
-        for t in range(cfg.n_steps):
-            r.decode(t)
-    torch.cuda.synchronize()
-    if int(r.dev_err.item()) != 0:
-        raise RuntimeError(f"device error word {int(r.dev_err.item())}")
-    g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_pre, stream=stream):
-        r.prefill_select()
-    with torch.cuda.graph(g_dec, stream=stream):
-        for t in range(cfg.n_steps):
-            r.decode(t)
-    torch.cuda.synchronize()
+    g_pre, g_dec = capture(job, stream)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
-
-    def one_step(ev):
-        ev[0].record(stream)
-        g_pre.replay()
-        ev[1].record(stream)
-        g_dec.replay()
-        ev[2].record(stream)
-
-    for _ in range(args.warmup):
-        with torch.cuda.stream(stream):
-            one_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
-            flush.zero_()
-    torch.cuda.synchronize()
+    replay_steps(g_pre, g_dec, stream, flush, args.warmup)
 
     clocks = ClockSampler(device.index if device.index is not None else 0)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks.start()
+    time.sleep(0.5)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
+    clocks.mark_start()
     t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for s in range(args.steps):
-            one_step(events[s])
-            flush.zero_()
-    torch.cuda.synchronize()
+    times = replay_steps(g_pre, g_dec, stream, flush, args.steps)
     wall = time.perf_counter() - t0
+    clocks.mark_end()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    if int(r.dev_err.item()) != 0:
-        raise RuntimeError(f"device error word {int(r.dev_err.item())}")
-    pre_ms = [e[0].elapsed_time(e[1]) for e in events]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in events]
-    step_ms = [a + b for a, b in zip(pre_ms, dec_ms)]
+    if int(job.dev_err.item()) != 0:
+        raise RuntimeError(f"device error word {int(job.dev_err.item())}")
+    pre_ms = [a for a, _ in times]
+    dec_ms = [b for _, b in times]
     res = dict(pre_ms=statistics.mean(pre_ms), dec_ms=statistics.mean(dec_ms),
-               step_ms=statistics.mean(step_ms), wall=wall, clocks=clk,
-               launches=r.launches_per_step() * args.steps, n_splits=r.n_splits)
+               step_ms=statistics.mean(a + b for a, b in times), wall=wall, clocks=clk,
+               launches=job.launches_per_step() * args.steps, n_splits=job.n_splits)
     if not args.no_e2e:
-        res["e2e"] = run_e2e(args, r, stream)
+        res["e2e"] = run_e2e(args, job, stream)
+    del g_pre, g_dec, job
+    torch.cuda.empty_cache()
     return res
 
 
-def run_e2e(args, r, stream):
-    """Same path through the C ABI from pinned host buffers: every step copies
-    its inputs host->device and the decode outputs device->host."""
+def time_workload(name, rank, device, reps=5):
+    """Decode and prefill timings of another workload in the same run (its
+    own job, graphs replayed reps times after 3 warm-ups, L2 flushed between
+    replays)."""
     import torch
-    cfg = r.cfg
+    cfgs = job_configs(name)
+    job = Job(cfgs, rank * len(cfgs), device)
+    stream = torch.cuda.Stream(device)
+    g_pre, g_dec = capture(job, stream)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    replay_steps(g_pre, g_dec, stream, flush, 3)
+    times = replay_steps(g_pre, g_dec, stream, flush, reps)
+    if int(job.dev_err.item()) != 0:
+        raise RuntimeError(f"{name}: device error word {int(job.dev_err.item())}")
+    res = dict(cfgs=cfgs, pre_ms=statistics.median(a for a, _ in times),
+               dec_ms=statistics.median(b for _, b in times), n_splits=job.n_splits, T=job.T)
+    del g_pre, g_dec, job, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_e2e(args, job, stream):
+    """The same work through the C ABI from pinned host buffers.
+
+    Decode: every decode step copies its live q, k, v host -> device (one
+    pinned block per step into one of four rotating device blocks, on a copy
+    stream that runs up to three steps ahead) and its output device -> host;
+    the T calls and all their copies are one CUDA graph.  The decode value
+    and the byte counts of the line cover exactly this work.  The prefill's
+    own upload (every sequence's q, k, v, q_win, s_I, s_P, slot rows) is
+    timed separately and reported beside it."""
+    import torch
     pin = lambda t: t.pin_memory()  # noqa: E731
-    h_q, h_k, h_v = pin(r.host["q"]), pin(r.host["k"]), pin(r.host["v"])
-    h_qw, h_si, h_sp, h_slot = pin(r.host["q_win"]), pin(r.host["s_i"]), pin(r.host["s_p"]), \
-        pin(r.host["slot_row"])
-    # Each step's live q, k, v travel as one pinned block (one copy a step)
-    # into one of N_LIVE device blocks, so the copies can run up to
-    # N_LIVE - 1 steps ahead of the kernels.
+    pre_in = []
+    for sq, h in zip(job.seqs, job.host):
+        for key in ("q", "k", "v", "q_win", "slot_row"):
+            pre_in.append((sq[key], pin(h[key].contiguous())))
+    pre_in.append((job.s_i, pin(torch.cat([h["s_i"] for h in job.host]))))
+    pre_in.append((job.s_p, pin(torch.cat([h["s_p"] for h in job.host]))))
     n_live = 4
-    shapes = [x.shape for x in r.live[0]]
-    sizes = [x.numel() for x in r.live[0]]
+    shapes = [x.shape for x in job.live[0]]
+    sizes = [x.numel() for x in job.live[0]]
 
     def views(flat):
         out, off = [], 0
@@ -339,45 +460,37 @@ def run_e2e(args, r, stream):
         return tuple(out)
 
     h_live = []
-    for blk in r.live:
+    for blk in job.live:
         flat = torch.empty(sum(sizes), dtype=torch.bfloat16).pin_memory()
         for dst, x in zip(views(flat), blk):
             dst.copy_(x.cpu())
         h_live.append(flat)
-    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in r.dec_out]
-    d_flat = [torch.empty(sum(sizes), dtype=torch.bfloat16, device=r.q.device) for _ in range(n_live)]
+    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in job.dec_out]
+    d_flat = [torch.empty(sum(sizes), dtype=torch.bfloat16, device=job.pool_k.device)
+              for _ in range(n_live)]
     d_live = [views(f) for f in d_flat]
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_qw, h_si, h_sp, h_slot))
-    h2d += sum(x.numel() * x.element_size() for x in h_live)
-    d2h = sum(o.numel() * o.element_size() for o in h_out)
+    pre_h2d = sum(h.numel() * h.element_size() for _, h in pre_in)
+    dec_h2d = sum(x.numel() * x.element_size() for x in h_live)
+    dec_d2h = sum(o.numel() * o.element_size() for o in h_out)
 
-    # Copies run on their own streams so that they overlap the kernels: the
-    # inputs of the next decode steps go up while step t computes, and step
-    # t's output comes down while step t+1 computes.  Every copy stays inside
-    # the timed region.
     copy_s = torch.cuda.Stream(stream.device)
     d2h_s = torch.cuda.Stream(stream.device)
     h2d_done = [torch.cuda.Event() for _ in range(n_live)]
     dec_done = [torch.cuda.Event() for _ in range(n_live)]
 
-    def step(ev):
-        with torch.cuda.stream(stream):
-            ev[0].record(stream)
+    def prefill_part():
         copy_s.wait_stream(stream)
         with torch.cuda.stream(copy_s):
-            r.q.copy_(h_q, non_blocking=True)
-            r.k.copy_(h_k, non_blocking=True)
-            r.v.copy_(h_v, non_blocking=True)
-            r.q_win.copy_(h_qw, non_blocking=True)
-            r.s_i.copy_(h_si, non_blocking=True)
-            r.s_p.copy_(h_sp, non_blocking=True)
-            r.slot_row.copy_(h_slot, non_blocking=True)
+            for d, h in pre_in:
+                d.copy_(h, non_blocking=True)
         stream.wait_stream(copy_s)
         with torch.cuda.stream(stream):
-            r.prefill_select()
-            ev[1].record(stream)
-        copy_s.wait_stream(stream)          # decode copies start after the prefill
-        for t in range(cfg.n_steps):
+            job.prefill_select()
+
+    def decode_part():
+        copy_s.wait_stream(stream)
+        d2h_s.wait_stream(stream)
+        for t in range(job.T):
             b = t % n_live
             dq, dk, dv = d_live[b]
             with torch.cuda.stream(copy_s):
@@ -387,72 +500,28 @@ def run_e2e(args, r, stream):
                 h2d_done[b].record(copy_s)
             with torch.cuda.stream(stream):
                 stream.wait_event(h2d_done[b])
-                r.decode(t, dq, dk, dv, r.dec_out[t])
+                job.decode(t, dq, dk, dv, job.dec_out[t])
                 dec_done[b].record(stream)
             with torch.cuda.stream(d2h_s):
                 d2h_s.wait_event(dec_done[b])
-                h_out[t].copy_(r.dec_out[t], non_blocking=True)
+                h_out[t].copy_(job.dec_out[t], non_blocking=True)
         stream.wait_stream(d2h_s)
-        with torch.cuda.stream(stream):
-            ev[2].record(stream)
+        stream.wait_stream(copy_s)
 
-    # Eager: one public-API call per decode step, issued from Python.
-    for _ in range(max(1, args.warmup)):
-        step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    # Warm eagerly, then capture the calls and copies once, as a serving loop
+    # would run them; every copy is a node of a graph replayed every step
+    # inside the timed region.
+    for _ in range(2):
+        prefill_part()
+        decode_part()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    for s in range(args.steps):
-        step(evs[s])
-    torch.cuda.synchronize()
-    eager_pre = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    eager_dec = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-
-    # Graph: the same calls and copies captured once, as a serving loop would
-    # run them; every H2D from pinned memory and every D2H is a node of the
-    # graph, replayed every step inside the timed region.
     g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    marks = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-
-    def prefill_part():
-        copy_s.wait_stream(stream)
-        with torch.cuda.stream(copy_s):
-            r.q.copy_(h_q, non_blocking=True)
-            r.k.copy_(h_k, non_blocking=True)
-            r.v.copy_(h_v, non_blocking=True)
-            r.q_win.copy_(h_qw, non_blocking=True)
-            r.s_i.copy_(h_si, non_blocking=True)
-            r.s_p.copy_(h_sp, non_blocking=True)
-            r.slot_row.copy_(h_slot, non_blocking=True)
-        stream.wait_stream(copy_s)
-        with torch.cuda.stream(stream):
-            r.prefill_select()
-
-    def decode_part():
-        copy_s.wait_stream(stream)
-        d2h_s.wait_stream(stream)
-        for t in range(cfg.n_steps):
-            b = t % n_live
-            dq, dk, dv = d_live[b]
-            with torch.cuda.stream(copy_s):
-                if t >= n_live:
-                    copy_s.wait_event(dec_done[b])
-                d_flat[b].copy_(h_live[t], non_blocking=True)
-                h2d_done[b].record(copy_s)
-            with torch.cuda.stream(stream):
-                stream.wait_event(h2d_done[b])
-                r.decode(t, dq, dk, dv, r.dec_out[t])
-                dec_done[b].record(stream)
-            with torch.cuda.stream(d2h_s):
-                d2h_s.wait_event(dec_done[b])
-                h_out[t].copy_(r.dec_out[t], non_blocking=True)
-        stream.wait_stream(d2h_s)
-        stream.wait_stream(copy_s)
-
     with torch.cuda.graph(g_pre, stream=stream):
         prefill_part()
     with torch.cuda.graph(g_dec, stream=stream):
         decode_part()
     torch.cuda.synchronize()
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     pre_ms, dec_ms = [], []
     for it in range(max(1, args.warmup) + args.steps):
         with torch.cuda.stream(stream):
@@ -465,8 +534,8 @@ def run_e2e(args, r, stream):
         if it >= max(1, args.warmup):
             pre_ms.append(marks[0].elapsed_time(marks[1]))
             dec_ms.append(marks[1].elapsed_time(marks[2]))
-    return dict(pre_ms=statistics.mean(pre_ms), dec_ms=statistics.mean(dec_ms), h2d=h2d, d2h=d2h,
-                eager_pre_ms=eager_pre, eager_dec_ms=eager_dec)
+    return dict(pre_ms=statistics.mean(pre_ms), dec_ms=statistics.mean(dec_ms),
+                pre_h2d=pre_h2d, dec_h2d=dec_h2d, dec_d2h=dec_d2h)
 
 
 # ----------------------------------------------------------- CPU oracle --
@@ -482,24 +551,35 @@ def blas_threads():
     return len(os.sched_getaffinity(0))
 
 
-def oracle_decode_sample(cfg, seconds):
-    """Times full oracle decode steps of cfg (fp64 CPU) for about `seconds`."""
+def _oracle_decode_inputs(cfg, seq):
+    """One sequence's oracle decode inputs: its pool (kept = the first B
+    content rows; the decode cost does not depend on which), selection and
+    the live block of step 0."""
+    import numpy as np
+
     from oracle import pfd_oracle as orc
     from sparse_chunked_kv_gb300 import workloads as wl
-    req = wl.make_request(cfg, 0)
+    req = wl.make_request(cfg, seq)
     f = wl.to_f64
-    kept = [list(range(cfg.n_keep))] * cfg.n_chunks
-    import numpy as np
-    kept = np.array(kept, dtype=np.int32)
+    kept = np.array([list(range(cfg.n_keep))] * cfg.n_chunks, dtype=np.int32)
     pk = np.zeros((cfg.pool_rows, cfg.n_kv_heads, cfg.head_dim))
     pv = np.zeros_like(pk)
-    table = orc.compact(f(req["k"]), f(req["v"]), kept, req["slot_row"].numpy(), cfg.chunk_size, pk, pv)
+    table = orc.compact(f(req["k"]), f(req["v"]), kept, req["slot_row"].numpy(), cfg.chunk_size,
+                        pk, pv)
     sel, _ = orc.select_chunks(req["s_i"].numpy(), req["s_p"].numpy(), cfg.n_select)
-    ql, kl, vl = wl.live_block(req, wl.make_step(cfg, 0, 0))
-    ql, kl, vl = f(ql), f(kl), f(vl)
+    ql, kl, vl = wl.live_block(req, wl.make_step(cfg, seq, 0))
+    return (f(ql), f(kl), f(vl), pk, pv, table, sel, cfg.sm_scale)
+
+
+def oracle_decode_sample(cfgs, seconds):
+    """Times full oracle decode steps of the job (fp64 CPU, every sequence)
+    for about `seconds`; returns seconds per step."""
+    from oracle import pfd_oracle as orc
+    inputs = [_oracle_decode_inputs(c, i) for i, c in enumerate(cfgs)]
     n, t0 = 0, time.perf_counter()
     while True:
-        orc.decode_attention(ql, kl, vl, pk, pv, table, sel, cfg.sm_scale)
+        for x in inputs:
+            orc.decode_attention(*x)
         n += 1
         el = time.perf_counter() - t0
         if el >= seconds or n >= 1000:
@@ -507,56 +587,70 @@ def oracle_decode_sample(cfg, seconds):
     return el / n
 
 
-def oracle_prefill_sample(cfg, seconds):
-    """Times the oracle's prefill (chunk attention + window scores) on one chunk."""
+def oracle_prefill_sample(cfgs, seconds):
+    """Times the oracle's prefill (chunk attention + window scores) on one
+    chunk of each distinct chunk size, scaled to the job's chunk counts."""
     from oracle import pfd_oracle as orc
     from sparse_chunked_kv_gb300 import workloads as wl
-    req = wl.make_request(cfg, 0)
-    rows = cfg.chunk_size + 1
-    f = wl.to_f64
-    q, k, v, qw = f(req["q"][:rows]), f(req["k"][:rows]), f(req["v"][:rows]), f(req["q_win"])
-    n, t0 = 0, time.perf_counter()
-    while True:
-        orc.chunk_attention(q, k, v, 1, cfg.chunk_size, cfg.sm_scale)
-        orc.window_scores(qw, k, 1, cfg.chunk_size, cfg.sm_scale)
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or n >= 1000:
-            break
-    return (el / n) * cfg.n_chunks  # one chunk's time scaled to the workload's N chunks
+    distinct = {}
+    for c in cfgs:
+        distinct.setdefault(c.chunk_size, []).append(c)
+    per = max(seconds / len(distinct), 1e-3)
+    total_s = 0.0
+    for group in distinct.values():
+        cfg = group[0]
+        req = wl.make_request(cfg, 0)
+        rows = cfg.chunk_size + 1
+        f = wl.to_f64
+        q, k, v, qw = f(req["q"][:rows]), f(req["k"][:rows]), f(req["v"][:rows]), f(req["q_win"])
+        n, t0 = 0, time.perf_counter()
+        while True:
+            orc.chunk_attention(q, k, v, 1, cfg.chunk_size, cfg.sm_scale)
+            orc.window_scores(qw, k, 1, cfg.chunk_size, cfg.sm_scale)
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= per or n >= 1000:
+                break
+        total_s += (el / n) * sum(c.n_chunks for c in group)
+    return total_s
 
 
-def cpu_baseline(cfg, seconds):
-    dec_s = oracle_decode_sample(cfg, seconds * 0.7)
-    pre_s = oracle_prefill_sample(cfg, seconds * 0.3)
-    return {"value": decode_flops(cfg) / dec_s / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
-            "kind": "oracle",
-            "sample": (f"fp64 numpy oracle: full decode steps of the {cfg.name} workload repeated "
-                       f"for ~{0.7 * seconds:.0f} s ({dec_s * 1e3:.1f} ms each); prefill rate from "
-                       f"one chunk repeated for ~{0.3 * seconds:.0f} s, scaled to N chunks"),
+def cpu_baseline(name, cfgs, seconds):
+    dec_s = oracle_decode_sample(cfgs, seconds * 0.7)
+    pre_s = oracle_prefill_sample(cfgs, seconds * 0.3)
+    return {"value": total(decode_flops, cfgs) / dec_s / 1e12, "unit": "TFLOP/s",
+            "cores": blas_threads(), "kind": "oracle",
+            "sample": (f"fp64 numpy oracle: full decode steps of the {name} workload "
+                       f"({len(cfgs)} sequence(s)) repeated for ~{0.7 * seconds:.0f} s "
+                       f"({dec_s * 1e3:.1f} ms each); prefill rate from one chunk of each chunk "
+                       f"size repeated for ~{0.3 * seconds:.0f} s, scaled to the job's chunks"),
             "decode_ms_per_step": dec_s * 1e3, "prefill_ms": pre_s * 1e3,
-            "prefill_gbs": prefill_bytes(cfg) / pre_s / 1e9}
+            "prefill_gbs": total(prefill_bytes, cfgs) / pre_s / 1e9}
 
 
-def run_reference(args, cfg, rank):
+def run_reference(args, cfgs, rank, name=None):
+    if not isinstance(cfgs, (list, tuple)):
+        cfgs = [cfgs]
+    name = name or (cfgs[0].name if len(cfgs) == 1 else "mix")
     if rank != 0:
         return
-    from sparse_chunked_kv_gb300 import workloads as wl  # noqa: F401
     per_step = max(0.5, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        oracle_decode_sample(cfg, 0.0)
-    times = [oracle_decode_sample(cfg, per_step) for _ in range(args.steps)]
+        oracle_decode_sample(cfgs, 0.0)
+    times = [oracle_decode_sample(cfgs, per_step) for _ in range(args.steps)]
     dec_s = statistics.mean(times)
-    value = decode_flops(cfg) / dec_s / 1e12
+    value = total(decode_flops, cfgs) / dec_s / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dec_s * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_name(cfg), "timed": "one oracle decode step per step"},
+            "config": {"workload": workload_name(name, cfgs),
+                       "timed": "one oracle decode step of the whole job per step"},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
                              "kind": "oracle",
-                             "sample": f"fp64 numpy oracle, full decode steps of {cfg.name}, "
-                                       f"~{per_step:.1f} s per timed step"},
+                             "sample": f"fp64 numpy oracle, full decode steps of {name} "
+                                       f"({len(cfgs)} sequence(s)), ~{per_step:.1f} s per "
+                                       f"timed step"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -580,86 +674,117 @@ def job_tflops(world, flops_per_call, calls, ms):
     return world * flops_per_call * calls / (ms * 1e-3) / 1e12
 
 
+def roofline_fracs(cfgs, dec_ms_per_call, pre_ms, peaks):
+    """Decode and prefill against the measured peaks: decode against the
+    bf16 burst peak (a graph of back-to-back calls lasting milliseconds) and,
+    as a second figure, the sustained one; prefill against
+    max(bytes / HBM, flops / bf16 burst)."""
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    dflops = total(decode_flops, cfgs)
+    dec_tflops = dflops / (dec_ms_per_call * 1e-3) / 1e12
+    pflops, pbytes = total(prefill_flops, cfgs), total(prefill_bytes, cfgs)
+    pre_s = pre_ms * 1e-3
+    t_hbm, t_tc = pbytes / (hbm * 1e9), pflops / (burst * 1e12)
+    return dict(decode_us=dec_ms_per_call * 1e3, decode_tflops=dec_tflops,
+                decode_frac=dec_tflops / burst, decode_frac_sustained=dec_tflops / sustained,
+                prefill_us=pre_ms * 1e3, prefill_tflops=pflops / pre_s / 1e12,
+                prefill_gbs=pbytes / pre_s / 1e9, prefill_bound="tensor" if t_tc >= t_hbm else "hbm",
+                prefill_frac=max(t_hbm, t_tc) / pre_s)
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    from sparse_chunked_kv_gb300 import workloads as wl
-    cfg = wl.CONFIGS[args.config]
+    cfgs = job_configs(args.config)
     if args.impl == "reference":
-        run_reference(args, cfg, rank)
+        run_reference(args, cfgs, rank, args.config)
         return
     import torch
     if world > 1:
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl")
     device = torch.device("cuda", local if world > 1 else 0)
-    res = run_gpu(args, cfg, rank, world, device)
+    res = run_gpu(args, cfgs, rank, world, device)
     if world > 1:
         res["dec_ms"], res["pre_ms"], res["step_ms"] = max_over_ranks(
             [res["dec_ms"], res["pre_ms"], res["step_ms"]], device)
+    others = {}
+    if rank == 0:
+        for name in [x for x in args.per_config.split(",") if x and x != args.config]:
+            others[name] = time_workload(name, 0, device)
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
     peaks, peak_kind = load_peaks()
-    T = cfg.n_steps
-    dec_us = res["dec_ms"] * 1e3 / T                       # one decode call (attention + merge)
-    dflops = decode_flops(cfg)
+    T = cfgs[0].n_steps
+    dflops = total(decode_flops, cfgs)
     value = job_tflops(world, dflops, T, res["dec_ms"])
-    per_launch_tflops = dflops / (dec_us * 1e-6) / 1e12
-    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-    pre_gbs = prefill_bytes(cfg) / (res["pre_ms"] * 1e-3) / 1e9
-    pre_tflops = prefill_flops(cfg) / (res["pre_ms"] * 1e-3) / 1e12
-    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    fr = roofline_fracs(cfgs, res["dec_ms"] / T, res["pre_ms"], peaks)
     burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    pre_roof_s = max(prefill_bytes(cfg) / (hbm * 1e9), prefill_flops(cfg) / (burst * 1e12))
+    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["step_ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": workload_name(cfg), "global_batch": world,
-                   "seq_len": cfg.n_chunks * cfg.chunk_size,
+        "config": {"workload": workload_name(args.config, cfgs), "global_batch": world * len(cfgs),
+                   "seq_len": sum(c.n_chunks * c.chunk_size for c in cfgs) // len(cfgs),
                    "l2": "flushed between steps (256 MiB write), outside the timed events",
                    "decode_splits": res["n_splits"], "graphs": "prefill+select; T-step decode loop",
-                   "parallelism": f"replicas x{world} (independent requests)"},
-        "decode_us_per_step": dec_us,
-        "decode_tflops": per_launch_tflops,
-        "prefill_us": res["pre_ms"] * 1e3,
-        "prefill_gbs": pre_gbs,
-        "prefill_tflops": pre_tflops,
-        "prefill_roofline_frac": pre_roof_s / (res["pre_ms"] * 1e-3),
+                   "parallelism": f"replicas x{world} (independent jobs)"},
+        "decode_us_per_step": fr["decode_us"],
+        "decode_tflops": fr["decode_tflops"],
+        "prefill_us": fr["prefill_us"],
+        "prefill_gbs": fr["prefill_gbs"],
+        "prefill_tflops": fr["prefill_tflops"],
+        "prefill_roofline_frac": fr["prefill_frac"],
         "roofline": {"kernel": "decode attention call (attention_kernel + lse_merge_kernel)",
-                     "bound": "tensor", "achieved": per_launch_tflops, "peak": sustained,
-                     "peak_kind": f"{peak_kind} bf16 sustained", "unit": "TFLOP/s",
-                     "frac": per_launch_tflops / sustained,
-                     "traffic": recorded_traffic("decode_attention_8k.md")},
-        "prefill_roofline": {"bound": "tensor" if prefill_flops(cfg) / (burst * 1e12) >=
-                             prefill_bytes(cfg) / (hbm * 1e9) else "hbm",
-                             "achieved_gbs": pre_gbs, "hbm_peak_gbs": hbm,
-                             "achieved_tflops": pre_tflops, "tensor_peak_tflops": burst,
-                             "frac": pre_roof_s / (res["pre_ms"] * 1e-3),
-                             "peak_kind": peak_kind},
+                     "bound": "tensor", "achieved": fr["decode_tflops"], "peak": burst,
+                     "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s",
+                     "frac": fr["decode_frac"],
+                     "frac_of_sustained": fr["decode_frac_sustained"],
+                     "sustained_peak": sustained,
+                     "traffic": recorded_traffic(f"decode_attention_{args.config}.md")},
+        "prefill_roofline": {"bound": fr["prefill_bound"], "achieved_gbs": fr["prefill_gbs"],
+                             "hbm_peak_gbs": hbm, "achieved_tflops": fr["prefill_tflops"],
+                             "tensor_peak_tflops": burst, "frac": fr["prefill_frac"],
+                             "peak_kind": f"{peak_kind} (HBM copy; bf16 burst)"},
         "clocks": res["clocks"],
         "gpu_launches": res["launches"],
         "wall_s_timed_region": res["wall"],
     }
+    if others:
+        line["per_config"] = {}
+        for name, o in others.items():
+            f2 = roofline_fracs(o["cfgs"], o["dec_ms"] / o["T"], o["pre_ms"], peaks)
+            line["per_config"][name] = {
+                "decode_us_per_step": f2["decode_us"], "decode_tflops": f2["decode_tflops"],
+                "decode_frac": f2["decode_frac"], "decode_frac_sustained": f2["decode_frac_sustained"],
+                "decode_splits": o["n_splits"], "prefill_us": f2["prefill_us"],
+                "prefill_tflops": f2["prefill_tflops"], "prefill_gbs": f2["prefill_gbs"],
+                "prefill_bound": f2["prefill_bound"], "prefill_frac": f2["prefill_frac"],
+                "timing": "median of 5 graph replays after 3 warm-ups, L2 flushed between"}
     if "e2e" in res:
         e = res["e2e"]
         line["e2e"] = {"value": job_tflops(world, dflops, T, e["dec_ms"]), "unit": "TFLOP/s",
-                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
-                       "prefill_ms": e["pre_ms"], "decode_ms": e["dec_ms"],
-                       "path": ("C ABI calls (prefill + select, then one decode call per step) "
-                                "captured in CUDA graphs with every step's H2D copies from pinned "
-                                "host memory and D2H of its output as graph nodes on copy "
-                                "streams that overlap the kernels"),
-                       "eager_value": job_tflops(world, dflops, T, e["eager_dec_ms"]),
-                       "eager_decode_ms": e["eager_dec_ms"],
-                       "eager_path": "the same calls and copies issued from Python every step"}
+                       "h2d_bytes_per_step": e["dec_h2d"], "d2h_bytes_per_step": e["dec_d2h"],
+                       "decode_ms": e["dec_ms"],
+                       "path": ("the T decode calls of a step through the C ABI, captured in a "
+                                "CUDA graph with every call's live-block H2D copy from pinned "
+                                "host memory and its output's D2H as graph nodes on copy streams "
+                                "that overlap the kernels; value and byte counts cover exactly "
+                                "these calls and copies"),
+                       "prefill": {"ms": e["pre_ms"], "h2d_bytes": e["pre_h2d"],
+                                   "path": "every sequence's prefill inputs uploaded from pinned "
+                                           "memory, then the prefill and selection calls"}}
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.config, cfgs, args.cpu_seconds)
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

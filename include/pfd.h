@@ -35,6 +35,12 @@
  *     skipped and a PFD_DEVERR_* bit is OR-ed into *dev_err when dev_err is
  *     not NULL.  The kernels wait on nothing outside their own thread block,
  *     and every internal pipeline wait is bounded (PFD_DEVERR_TIMEOUT).
+ *   - PFD_DEVERR_TIMEOUT means a pipeline stage stopped making progress.  The
+ *     thread block that saw it leaves its loop without draining the tensor
+ *     copies and tensor-core operations it had in flight, so the outputs of
+ *     that call are undefined and the CUDA context must be treated as
+ *     unusable afterwards (destroy it); it only bounds how long a broken
+ *     launch can occupy the GPU.
  *   - Calls are thread-safe; calls on one stream run in order.
  */
 #ifndef PFD_H_
@@ -151,7 +157,10 @@ pfd_status pfd_select_chunks(const float* s_I, const float* s_P, int N, int K, i
  * entries cu_n[b] .. cu_n[b+1]-1 and selects K_b = cu_k[b+1]-cu_k[b] of them.
  * sel[cu_k[b] + i] receives the table index (cu_n[b] + chunk) of its i-th
  * best chunk.  cu_n, cu_k: [batch+1] int32 device, non-decreasing.
- * max_n bounds every sequence's chunk count (<= 16384).
+ * max_n bounds every sequence's chunk count (<= 16384).  A sequence whose
+ * device segment is malformed (no chunk, more than max_n chunks, K_b < 0 or
+ * K_b > its chunk count) gets -1 in its selection slots (when 0 < K_b <=
+ * max_n), which a later pfd_decode_attention reports as PFD_DEVERR_SEL.
  */
 pfd_status pfd_select_chunks_batched(const float* s_I, const float* s_P, const int32_t* cu_n,
                                      const int32_t* cu_k, int batch, int max_n, int32_t* sel,
@@ -182,8 +191,9 @@ size_t pfd_decode_workspace(int batch, const int32_t* cu_lq_host, const int32_t*
  *   lse = natural-log log-sum-exp of the same logits.
  * The key range is cut into n_splits contiguous splits (0 = automatic); each
  * split reads its chunks in place through the table (no gather) and keeps a
- * partial softmax state (max, sum, unnormalised output); the splits are
- * merged by a log-sum-exp reduction.  The pool is only read.
+ * partial softmax state: its max and denominator in fp32 and its output row
+ * normalised by that denominator in bf16.  The splits are merged by a
+ * log-sum-exp reduction.  The pool is only read.
  *
  * Arguments (device memory unless stated):
  *   q              [total_lq, Hq, D] bf16; k_self, v_self [total_lq, Hkv, D]
@@ -221,18 +231,23 @@ pfd_status pfd_decode_attention(const pfd_bf16* q, const pfd_bf16* k_self,
  *
  * The split-KV partials go to one statically allocated device buffer of
  * PFD_DECODE_STATIC_SCRATCH_BYTES per device instead of caller workspace;
- * nothing is allocated.  The first call made on a device, with that device
- * current, looks up that device's copy of the buffer (cudaGetSymbolAddress)
- * and caches the address; make that first call before any stream capture
- * begins.  Every call on a device shares the buffer, so calls whose work
- * overlaps on the GPU (streams with no ordering between them) race and give
- * undefined results; calls on one stream run in order and are safe.
+ * nothing is allocated.  Every call looks up the current device's copy of
+ * the buffer (cudaGetSymbolAddress, with that device current); nothing is
+ * cached, so calls after a device reset need no special care.  The first
+ * call on a device may make the CUDA runtime load this library's device code
+ * there; make it before any stream capture begins.  Every call on a device
+ * shares the buffer, so calls whose work overlaps on the GPU (streams with
+ * no ordering between them) race and give undefined results; calls on one
+ * stream run in order and are safe.
  *
- * Arguments, results and device-side errors are those of
- * pfd_decode_attention.  Returns PFD_ERR_UNSUPPORTED, with nothing launched,
- * when these sizes need more than PFD_DECODE_STATIC_SCRATCH_BYTES of
- * workspace (pfd_decode_workspace(...) reports the need), and PFD_ERR_CUDA
- * when the buffer's address cannot be found on the current device.
+ * With n_splits == 0 the call uses the split count pfd_decode_plan_splits
+ * reports, lowered to the largest count whose partials fit the buffer (one
+ * split needs no scratch, so every size runs).  An explicit n_splits whose
+ * partials need more than PFD_DECODE_STATIC_SCRATCH_BYTES
+ * (pfd_decode_workspace(...) reports the need) returns PFD_ERR_UNSUPPORTED
+ * with nothing launched.  Arguments, results and device-side errors are
+ * otherwise those of pfd_decode_attention; PFD_ERR_CUDA is returned when the
+ * buffer's address cannot be found on the current device.
  */
 pfd_status pfd_decode_attention_static_scratch(
     const pfd_bf16* q, const pfd_bf16* k_self, const pfd_bf16* v_self, const int32_t* cu_lq,

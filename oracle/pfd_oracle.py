@@ -77,11 +77,6 @@ def softmax_rows(x: np.ndarray) -> np.ndarray:
     return e / e.sum(axis=-1, keepdims=True)
 
 
-def default_scale(head_dim: int) -> float:
-    """R5: the standard 1/sqrt(D) attention scale."""
-    return 1.0 / math.sqrt(head_dim)
-
-
 # --------------------------------------------------------------- prefill --
 
 def chunk_attention(q, k, v, n_chunks, chunk_size, sm_scale, counter=None):
@@ -118,13 +113,16 @@ def chunk_attention_rows(q, k, v, chunk_size, rows, sm_scale):
     span = chunk_size + 1
     n_q_heads, head_dim = q.shape[1], q.shape[2]
     group = n_q_heads // k.shape[1]
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1)
     out = np.empty((len(rows), n_q_heads, head_dim), dtype=np.float64)
-    for i, r in enumerate(rows):
-        lo = (int(r) // span) * span
+    chunk_of = rows // span
+    for j in np.unique(chunk_of):
+        at = np.nonzero(chunk_of == j)[0]      # positions in `rows` of chunk j's rows
+        lo = int(j) * span
         for h in range(n_q_heads):
             g = h // group
-            logits = sm_scale * (q[r, h, :][None, :] @ k[lo:lo + span, g, :].T)
-            out[i, h, :] = (softmax_rows(logits) @ v[lo:lo + span, g, :])[0]
+            logits = sm_scale * (q[rows[at], h, :] @ k[lo:lo + span, g, :].T)
+            out[at, h, :] = softmax_rows(logits) @ v[lo:lo + span, g, :]
     return out
 
 

@@ -227,7 +227,14 @@ select_kernel(const float* __restrict__ s_i, const float* __restrict__ s_p,
   const int n = cu_n ? cu_n[b + 1] - off : n_scalar;
   const int koff = cu_k ? cu_k[b] : 0;
   const int k = cu_k ? cu_k[b + 1] - koff : k_scalar;
-  if (n <= 0 || n > max_n || k < 0 || k > n) return;
+  if (n <= 0 || n > max_n || k < 0 || k > n) {
+    // A malformed segment: its selection slots get -1, so that a decode
+    // call reading them reports PFD_DEVERR_SEL instead of using stale
+    // indices.  Only a range a valid cu_k could describe is written.
+    if (koff >= 0 && k > 0 && k <= max_n)
+      for (int t = threadIdx.x; t < k; t += kSelectThreads) sel[koff + t] = -1;
+    return;
+  }
   for (int t = threadIdx.x; t < n; t += kSelectThreads) {
     const float s = s_i[off + t] + s_p[off + t];
     if (s_out) s_out[off + t] = s;

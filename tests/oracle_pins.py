@@ -221,6 +221,35 @@ def check_split_equals_concat(orc, seed=8):
     assert np.max(np.abs(out1 - out2)) < 1e-12 and np.max(np.abs(lse1 - lse2)) < 1e-12
 
 
+def check_split_at_arbitrary_points(orc, seed=14):
+    """Split + LSE merge at arbitrary cut points of the concatenated keys
+    (inside chunk slots and across their edges, not only at chunk
+    boundaries) == one softmax over the concatenation (torch SDPA and
+    torch.logsumexp), for several random cut sets."""
+    gen = torch.Generator().manual_seed(seed)
+    hq, hkv, d, lq = 6, 2, 16, 7
+    pool_k, pool_v = rand(gen, 48, hkv, d), rand(gen, 48, hkv, d)
+    table = np.array([[0, 11], [13, 9], [30, 17]], dtype=np.int32)
+    sel = np.array([2, 0, 1], dtype=np.int32)
+    q, ks, vs = rand(gen, lq, hq, d), rand(gen, lq, hkv, d), rand(gen, lq, hkv, d)
+    kk = np.concatenate([orc.gather_selected(pool_k, table, sel), ks], axis=0)
+    vv = np.concatenate([orc.gather_selected(pool_v, table, sel), vs], axis=0)
+    n_keys = kk.shape[0]
+    for trial in range(6):
+        n_cuts = 1 + trial
+        cuts = sorted(torch.randperm(n_keys - 1, generator=gen)[:n_cuts].add(1).tolist())
+        edges = [0] + cuts + [n_keys]
+        parts = [orc.split_partials(q, kk[a:b], vv[a:b], hq // hkv, 0.4)
+                 for a, b in zip(edges[:-1], edges[1:])]
+        out, lse = orc.lse_merge(parts)
+        for h in range(hq):
+            g = h // (hq // hkv)
+            want = sdpa(q[:, h], kk[:, g], vv[:, g], None, 0.4)
+            assert np.max(np.abs(out[:, h] - want)) < 1e-12, f"split at {cuts} != one softmax"
+            lg = torch.from_numpy(0.4 * q[:, h] @ kk[:, g].T)
+            assert np.max(np.abs(lse[:, h] - torch.logsumexp(lg, dim=1).numpy())) < 1e-12
+
+
 def check_decode_vs_sdpa(orc, seed=9):
     """Decode == SDPA over [selected rows ; live rows]; lse == logsumexp."""
     gen = torch.Generator().manual_seed(seed)
@@ -316,5 +345,6 @@ def check_cost_model(orc):
 ALL_CHECKS = [
     check_chunk_attention, check_scores_vs_sdpa, check_scores_brute_force, check_scores_invariants,
     check_scores_single_row, check_top_b, check_select, check_split_equals_concat,
+    check_split_at_arbitrary_points,
     check_decode_vs_sdpa, check_dense_equivalence, check_compact, check_cost_model,
 ]

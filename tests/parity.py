@@ -6,7 +6,13 @@ tolerances:
     within 1e-5 (relative) of the chunk's B-th largest score;
   - attention outputs (bf16 in, fp32 accumulate): max-abs 2e-2, mean-abs 2e-3;
   - decode lse: max-abs 1e-3;
-  - window scores (fp32 sums of ~W*Hq probabilities): rel 1e-4.
+  - window scores: |gpu - oracle| <= 1e-4 * |oracle| + 1e-6 * W * Hq per
+    element (score_tol).  A score is an fp32 sum of W*Hq probabilities, each
+    carrying about 1e-6 of relative error from the fp32 exponent and
+    normaliser, so the absolute term grows with the number of terms: at
+    W = 64, Hq = 28 it is 1.8e-3, against scores of order 1..100.  The kept
+    indices stay bit-exact outside the 1e-5 tie band whatever this
+    tolerance is.
 """
 from __future__ import annotations
 
@@ -22,6 +28,12 @@ OUT_MEAN_ABS = 2e-3
 LSE_MAX_ABS = 1e-3
 TIE_REL = 1e-5
 SCORE_RTOL = 1e-4
+SCORE_ATOL_PER_TERM = 1e-6
+
+
+def score_tol(ref, n_win, n_q_heads):
+    """Per-element tolerance of the fp32 window scores against the oracle."""
+    return SCORE_RTOL * np.abs(ref) + SCORE_ATOL_PER_TERM * max(1, n_win * n_q_heads)
 
 f64 = wl.to_f64
 

@@ -109,6 +109,14 @@ def _decode_split_no_rescale(q, ks, vs, pk, pv, table, sel, scale):
     return acc / l[..., None], np.log(l)
 
 
+def _lse_merge_drops_max(parts):
+    # mistake: weighs each split by its denominator alone, ignoring its max
+    big_l = sum(p[1] for p in parts)
+    acc = sum(p[1][..., None] * (p[2] / p[1][..., None]) for p in parts)
+    m_all = np.stack([p[0] for p in parts]).max(axis=0)
+    return acc / big_l[..., None], m_all + np.log(big_l)
+
+
 MUTANTS = {
     "cross_chunk_attention": (Mutant(chunk_attention=_chunk_attention_global), pins.check_chunk_attention),
     "gqa_mapping": (Mutant(chunk_attention=_chunk_attention_bad_gqa), pins.check_chunk_attention),
@@ -121,6 +129,8 @@ MUTANTS = {
     "decode_drops_self_block": (Mutant(decode_attention=_decode_no_self), pins.check_decode_vs_sdpa),
     "merge_without_rescale": (Mutant(decode_attention_split=_decode_split_no_rescale),
                               pins.check_split_equals_concat),
+    "merge_drops_split_max": (Mutant(lse_merge=_lse_merge_drops_max),
+                              pins.check_split_at_arbitrary_points),
 }
 
 
