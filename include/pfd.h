@@ -10,7 +10,9 @@
  *                                                        pfd_chunk_prefill and
  *                                                        the top-K selection
  *   Methodology 3, "Decoding with Static KV Reuse" and
- *   "Attention Kernel Optimization" (split-KV, LSE merge) -> pfd_decode_attention
+ *   "Attention Kernel Optimization" (split-KV, LSE merge) -> pfd_decode_attention,
+ *                                                        pfd_decode_partial,
+ *                                                        pfd_lse_merge
  *
  * Conventions shared by every call:
  *   - Tensors are token-major and contiguous: a [rows, heads, D] tensor keeps
@@ -53,7 +55,7 @@
 extern "C" {
 #endif
 
-#define PFD_ABI_VERSION 1
+#define PFD_ABI_VERSION 2
 
 typedef enum {
   PFD_OK = 0,
@@ -217,6 +219,55 @@ pfd_status pfd_decode_attention(const pfd_bf16* q, const pfd_bf16* k_self,
                                 float sm_scale, int n_splits, pfd_bf16* out, float* lse,
                                 int32_t* dev_err, void* workspace, size_t workspace_bytes,
                                 pfd_stream_t stream);
+
+/*
+ * One device's share of a decode step split across devices ("Attention Kernel
+ * Optimization": the KV dimension is partitioned, the parts are processed
+ * independently and merged by a log-sum-exp reduction).
+ *
+ * Identical to pfd_decode_attention except for two things.  First, the
+ * keys are the selected chunks sel[cu_k[b]..cu_k[b+1]) followed by the live
+ * block only when self_keys == 1; with self_keys == 0 the live rows are
+ * queries only.  Second, the result is that subset's partial state:
+ *   part_o   [total_lq, Hq, D] bf16: softmax over the subset's keys applied
+ *            to their v rows (the subset's own normalised output);
+ *   part_lse [total_lq, Hq] fp32 (required): natural-log log-sum-exp of the
+ *            subset's logits.  A (row, head) that sees no key at all gets
+ *            part_o = 0 and part_lse = -inf.
+ * A step over the whole key set is the merge (pfd_lse_merge) of partials
+ * whose subsets partition it: e.g. each device passes its local selected
+ * chunks, one of them (the owner of the live block) with self_keys = 1, the
+ * partials are gathered, and the owner merges them.
+ * workspace >= pfd_decode_partial_workspace(...) bytes (the call's own
+ * internal splits).
+ */
+size_t pfd_decode_partial_workspace(int batch, const int32_t* cu_lq_host,
+                                    const int32_t* cu_k_host, int Hq, int Hkv, int D,
+                                    int max_chunk_len, int self_keys, int n_splits);
+
+pfd_status pfd_decode_partial(const pfd_bf16* q, const pfd_bf16* k_self, const pfd_bf16* v_self,
+                              const int32_t* cu_lq, const int32_t* cu_lq_host,
+                              const pfd_bf16* pool_k, const pfd_bf16* pool_v, int64_t pool_rows,
+                              const pfd_chunk_entry* table, int32_t table_len, const int32_t* sel,
+                              const int32_t* cu_k, const int32_t* cu_k_host, int batch, int Hq,
+                              int Hkv, int D, int max_chunk_len, float sm_scale, int self_keys,
+                              int n_splits, pfd_bf16* part_o, float* part_lse, int32_t* dev_err,
+                              void* workspace, size_t workspace_bytes, pfd_stream_t stream);
+
+/*
+ * Log-sum-exp merge of n_parts partial states from any source ("Attention
+ * Kernel Optimization"), for every (row, head) of rows x Hq:
+ *   M = max_s part_lse[s],  w_s = exp(part_lse[s] - M),
+ *   out = sum_s w_s part_o[s] / sum_s w_s,  lse = M + ln(sum_s w_s).
+ * A part with part_lse = -inf has weight 0; if every part has, out = 0 and
+ * lse = -inf.
+ *   part_o   [n_parts, rows, Hq, D] bf16 device (8-byte aligned)
+ *   part_lse [n_parts, rows, Hq] fp32 device
+ *   out      [rows, Hq, D] bf16 device (written);  lse [rows, Hq] fp32 or NULL
+ * 1 <= n_parts <= 64; D in {64, 128}.
+ */
+pfd_status pfd_lse_merge(const pfd_bf16* part_o, const float* part_lse, int n_parts, int rows,
+                         int Hq, int D, pfd_bf16* out, float* lse, pfd_stream_t stream);
 
 /* Bytes of the static device scratch used by
  * pfd_decode_attention_static_scratch (per device). */

@@ -38,6 +38,10 @@ SIGNATURES = {
     "pfd_decode_attention_static_scratch": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _P,
                                                  ctypes.c_int32, _P, _P, _P, _I, _I, _I, _I, _I,
                                                  _F, _I, _P, _P, _P, _P]),
+    "pfd_decode_partial_workspace": (_SZ, [_I, _P, _P, _I, _I, _I, _I, _I, _I]),
+    "pfd_decode_partial": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _P, ctypes.c_int32, _P, _P, _P,
+                                _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "pfd_lse_merge": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "pfd_status_string": (ctypes.c_char_p, [_I]),
     "pfd_abi_version": (_I, []),
 }
@@ -168,3 +172,28 @@ def pfd_decode_attention_static_scratch(q, k_self, v_self, cu_lq, cu_lq_host, po
             raise PfdError(f"PFD_ERR_UNSUPPORTED: these sizes need {need} bytes of decode scratch, "
                            f"more than the static {DECODE_STATIC_SCRATCH_BYTES} bytes")
     _check(status)
+
+
+def pfd_decode_partial_workspace(batch, cu_lq_host, cu_k_host, Hq, Hkv, D, max_chunk_len,
+                                 self_keys, n_splits):
+    a, b = _host_i32(cu_lq_host), _host_i32(cu_k_host)
+    return load().pfd_decode_partial_workspace(batch, ctypes.cast(a, _P), ctypes.cast(b, _P), Hq,
+                                               Hkv, D, max_chunk_len, int(self_keys), n_splits)
+
+
+def pfd_decode_partial(q, k_self, v_self, cu_lq, cu_lq_host, pool_k, pool_v, pool_rows, table,
+                       table_len, sel, cu_k, cu_k_host, batch, Hq, Hkv, D, max_chunk_len,
+                       sm_scale, self_keys, n_splits, part_o, part_lse, dev_err, workspace,
+                       workspace_bytes, stream=None):
+    a, b = _host_i32(cu_lq_host), _host_i32(cu_k_host)
+    _check(load().pfd_decode_partial(
+        _ptr(q), _ptr(k_self), _ptr(v_self), _ptr(cu_lq), ctypes.cast(a, _P), _ptr(pool_k),
+        _ptr(pool_v), int(pool_rows), _ptr(table), int(table_len), _ptr(sel), _ptr(cu_k),
+        ctypes.cast(b, _P), batch, Hq, Hkv, D, max_chunk_len, float(sm_scale), int(self_keys),
+        n_splits, _ptr(part_o), _ptr(part_lse), _ptr(dev_err), _ptr(workspace),
+        int(workspace_bytes), _stream(stream)))
+
+
+def pfd_lse_merge(part_o, part_lse, n_parts, rows, Hq, D, out, lse, stream=None):
+    _check(load().pfd_lse_merge(_ptr(part_o), _ptr(part_lse), n_parts, rows, Hq, D, _ptr(out),
+                                _ptr(lse), _stream(stream)))

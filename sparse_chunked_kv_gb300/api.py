@@ -100,3 +100,50 @@ def decode_attention(q, k_self, v_self, pool_k, pool_v, table, sel, cu_lq=None, 
                               batch, hq, hkv, d, max_chunk_len, sm_scale, n_splits, out, lse,
                               dev_err, workspace, ws_bytes, stream)
     return out, lse
+
+
+def decode_partial(q, k_self, v_self, pool_k, pool_v, table, sel, cu_lq, cu_k, self_keys,
+                   sm_scale=0.0, n_splits=0, max_chunk_len=None, part_o=None, part_lse=None,
+                   dev_err=None, stream=None):
+    """One device's share of a decode step (pfd_decode_partial): the partial
+    state over the given selected chunks, plus the live block's keys when
+    self_keys.  cu_lq, cu_k: host lists.  Returns (part_o, part_lse)."""
+    _need_cuda(q, k_self, v_self, pool_k, pool_v, table)
+    dev = q.device
+    total_lq, hq, d = q.shape
+    hkv = k_self.shape[1]
+    cu_lq_host, cu_k_host = [int(x) for x in cu_lq], [int(x) for x in cu_k]
+    batch = len(cu_lq_host) - 1
+    cu_lq_dev = torch.tensor(cu_lq_host, dtype=torch.int32).to(dev)
+    cu_k_dev = torch.tensor(cu_k_host, dtype=torch.int32).to(dev)
+    if sel is None or sel.numel() == 0:
+        sel = torch.zeros(1, dtype=torch.int32, device=dev)
+    if max_chunk_len is None:
+        max_chunk_len = int(table[:, 1].max().item()) if table.shape[0] > 0 else 0
+    if part_o is None:
+        part_o = torch.empty_like(q)
+    if part_lse is None:
+        part_lse = torch.empty(total_lq, hq, dtype=torch.float32, device=dev)
+    if dev_err is None:
+        dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_bytes = _abi.pfd_decode_partial_workspace(batch, cu_lq_host, cu_k_host, hq, hkv, d,
+                                                 max_chunk_len, self_keys, n_splits)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _abi.pfd_decode_partial(q, k_self, v_self, cu_lq_dev, cu_lq_host, pool_k, pool_v,
+                            pool_k.shape[0], table, table.shape[0], sel, cu_k_dev, cu_k_host,
+                            batch, hq, hkv, d, max_chunk_len, sm_scale, self_keys, n_splits,
+                            part_o, part_lse, dev_err, ws, ws_bytes, stream)
+    return part_o, part_lse
+
+
+def lse_merge(part_o, part_lse, out=None, lse=None, stream=None):
+    """Log-sum-exp merge of stacked partials (pfd_lse_merge):
+    part_o [S, rows, Hq, D], part_lse [S, rows, Hq].  Returns (out, lse)."""
+    _need_cuda(part_o, part_lse)
+    s, rows, hq, d = part_o.shape
+    if out is None:
+        out = torch.empty(rows, hq, d, dtype=part_o.dtype, device=part_o.device)
+    if lse is None:
+        lse = torch.empty(rows, hq, dtype=torch.float32, device=part_o.device)
+    _abi.pfd_lse_merge(part_o, part_lse, s, rows, hq, d, out, lse, stream)
+    return out, lse

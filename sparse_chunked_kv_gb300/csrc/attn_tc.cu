@@ -229,7 +229,8 @@ __device__ __forceinline__ int groups_of(int len) { return (len + kGroupRows - 1
 
 // Fills the item's segment list (row, length, first global group) in shared
 // memory; run by the whole producer warp.  Decode: the selected chunks' slots
-// through the table, then the live block (the last segment, tensor 1).
+// through the table, then (unless the call leaves it out) the live block,
+// the last segment, read from tensor 1.
 __device__ __forceinline__ int load_segments(const AttnParams& p, const Item& it, int32_t* seg_row,
                                              int32_t* seg_len, int32_t* seg_g0, int lane) {
   int nseg;
@@ -242,7 +243,7 @@ __device__ __forceinline__ int load_segments(const AttnParams& p, const Item& it
     }
   } else {
     const int nsel = it.k1 - it.k0;
-    nseg = nsel + 1;
+    nseg = nsel + (p.self_keys ? 1 : 0);
     for (int i = lane; i < nsel; i += 32) {
       const int c = p.sel[it.k0 + i];
       int row = 0, len = 0;
@@ -260,7 +261,7 @@ __device__ __forceinline__ int load_segments(const AttnParams& p, const Item& it
       seg_row[i] = row;
       seg_len[i] = len;
     }
-    if (lane == 0) {
+    if (lane == 0 && p.self_keys) {
       seg_row[nsel] = static_cast<int32_t>(it.q_row0);
       seg_len[nsel] = it.n_t;
     }
@@ -395,7 +396,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
           const int gofs = g - seg_g0[lo];
           const int nv = min(kGroupRows, len - gofs * kGroupRows);
           const bool shifted = nv < kGroupRows && len >= kGroupRows;
-          t = (it.kind == kDecode && lo == nseg - 1) ? 1 : 0;
+          t = (it.kind == kDecode && p.self_keys && lo == nseg - 1) ? 1 : 0;
           row = seg_row[lo] + (shifted ? len - kGroupRows : gofs * kGroupRows);
           code = static_cast<uint32_t>(nv) | (shifted ? kShifted : 0u);
         }

@@ -19,10 +19,25 @@ namespace {
 constexpr int kMergeThreads = 256;
 constexpr int kAccBatch = 8;   // split partials of O loaded per round trip (one-pair kernel)
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
 
 __device__ __forceinline__ float4 bf16x4_to_float4(uint2 v) {
   return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
                      __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+}
+
+// One split's (m, l) for a (row, head): stored as (max in log2 units,
+// denominator), or, without part_l, as a natural-log log-sum-exp, which is
+// the state (lse * log2(e), 1).  A split that saw no key has m = -inf.
+__device__ __forceinline__ void load_state(const MergeParams& p, long long idx, float& m, float& l) {
+  if (p.part_l != nullptr) {
+    m = __ldg(p.part_m + idx);
+    l = __ldg(p.part_l + idx);
+  } else {
+    const float lse = __ldg(p.part_m + idx);
+    m = lse * kLog2e;
+    l = lse == -INFINITY ? 0.0f : 1.0f;
+  }
 }
 
 // More than 4 splits: one warp per (row, head).  Lane s loads split s's (m, l) (lanes loop when
@@ -52,14 +67,8 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel_one(const Merg
 
   float m_lane = -INFINITY, l_lane = 0.0f;   // lane's own splits s = lane, lane + 32
   float m_hi = -INFINITY, l_hi = 0.0f;
-  if (lane < S) {
-    m_lane = __ldg(p.part_m + lane * n_pairs + pair);
-    l_lane = __ldg(p.part_l + lane * n_pairs + pair);
-  }
-  if (lane + 32 < S) {
-    m_hi = __ldg(p.part_m + (lane + 32) * n_pairs + pair);
-    l_hi = __ldg(p.part_l + (lane + 32) * n_pairs + pair);
-  }
+  if (lane < S) load_state(p, lane * n_pairs + pair, m_lane, l_lane);
+  if (lane + 32 < S) load_state(p, (lane + 32) * n_pairs + pair, m_hi, l_hi);
   float big_m = fmaxf(m_lane, m_hi);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) big_m = fmaxf(big_m, __shfl_xor_sync(0xFFFFFFFFu, big_m, o));
@@ -139,14 +148,8 @@ __global__ void __launch_bounds__(kMergeThreads, 4) lse_merge_kernel(const Merge
       if (valid && active && s < S) a[i][s] = __ldg(reinterpret_cast<const uint2*>(o_base + s * o_stride));
     m_lane[i] = m_hi[i] = -INFINITY;
     l_lane[i] = l_hi[i] = 0.0f;
-    if (valid && lane < S) {
-      m_lane[i] = __ldg(p.part_m + lane * n_pairs + pair);
-      l_lane[i] = __ldg(p.part_l + lane * n_pairs + pair);
-    }
-    if (valid && lane + 32 < S) {
-      m_hi[i] = __ldg(p.part_m + (lane + 32) * n_pairs + pair);
-      l_hi[i] = __ldg(p.part_l + (lane + 32) * n_pairs + pair);
-    }
+    if (valid && lane < S) load_state(p, lane * n_pairs + pair, m_lane[i], l_lane[i]);
+    if (valid && lane + 32 < S) load_state(p, (lane + 32) * n_pairs + pair, m_hi[i], l_hi[i]);
   }
 #pragma unroll
   for (int i = 0; i < kP; ++i) {

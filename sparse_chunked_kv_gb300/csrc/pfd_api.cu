@@ -166,6 +166,142 @@ bool decode_host_ok(int batch, const int32_t* cu_lq_host, const int32_t* cu_k_ho
 
 constexpr int kMaxSplits = 64;
 
+int plan_splits(int batch, const int32_t* cu_lq_host, const int32_t* cu_k_host, int Hq,
+                int Hkv, int D, int max_chunk_len, bool self_keys) {
+  (void)D;
+  if (!decode_host_ok(batch, cu_lq_host, cu_k_host) || !shapes_ok(Hq, Hkv, 128)) return 1;
+  const int G = Hq / Hkv;
+  if (G > kBlockM) return 1;
+  const int Tq = kBlockM / G;
+  long long items = 0, keys_max = 0;
+  for (int b = 0; b < batch; ++b) {
+    const long long lq = cu_lq_host[b + 1] - cu_lq_host[b];
+    const long long kb = cu_k_host[b + 1] - cu_k_host[b];
+    items += Hkv * (((lq + Tq - 1) / Tq + 1) / 2);   // two query tiles per item
+    keys_max = std::max(keys_max, kb * std::max(0, max_chunk_len) + (self_keys ? lq : 0));
+  }
+  if (items <= 0) return 1;
+  const long long sms = device_sm_count();   // one persistent CTA per SM
+  int best = 1;
+  double best_cost = 1e300;
+  const long long max_s = std::max<long long>(1, std::min<long long>(kMaxSplits, (keys_max + kBlockN - 1) / kBlockN));
+  for (int S = 1; S <= max_s; ++S) {
+    const long long waves = (items * S + sms - 1) / sms;
+    const long long tiles = (keys_max + static_cast<long long>(S) * kBlockN - 1) / (static_cast<long long>(S) * kBlockN);
+    // an item costs ~2 units per key tile (two query tiles) plus ~3 units of
+    // fixed cost (Q load, pipeline fill, epilogue); the merge ~ 2 units
+    const double cost = static_cast<double>(waves) * (2.0 * tiles + 3.0) + (S > 1 ? 2.0 : 0.0);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
+}
+
+// Decode attention of one step over [selected chunks ; live block when
+// self_keys]: pfd_decode_attention (self_keys) and pfd_decode_partial.
+pfd_status decode_impl(const pfd_bf16* q, const pfd_bf16* k_self, const pfd_bf16* v_self,
+                       const int32_t* cu_lq, const int32_t* cu_lq_host, const pfd_bf16* pool_k,
+                       const pfd_bf16* pool_v, int64_t pool_rows, const pfd_chunk_entry* table,
+                       int32_t table_len, const int32_t* sel, const int32_t* cu_k,
+                       const int32_t* cu_k_host, int batch, int Hq, int Hkv, int D,
+                       int max_chunk_len, float sm_scale, bool self_keys, int n_splits,
+                       pfd_bf16* out, float* lse, int32_t* dev_err, void* workspace,
+                       size_t workspace_bytes, pfd_stream_t stream) {
+  if (!decode_host_ok(batch, cu_lq_host, cu_k_host)) return PFD_ERR_INVALID_ARG;
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return PFD_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return PFD_ERR_UNSUPPORTED;
+  if (!q || !k_self || !v_self || !cu_lq || !cu_k || !out) return PFD_ERR_INVALID_ARG;
+  if (n_splits < 0 || n_splits > kMaxSplits) return PFD_ERR_INVALID_ARG;
+  if (Hq / Hkv > kBlockM) return PFD_ERR_UNSUPPORTED;
+  for (int b = 0; b < batch; ++b)
+    if (cu_k_host[b + 1] - cu_k_host[b] >= kMaxSegments) return PFD_ERR_UNSUPPORTED;
+  const int total_lq = cu_lq_host[batch];
+  const int total_sel = cu_k_host[batch];
+  if (total_sel > 0 && (!pool_k || !pool_v || !table || !sel || pool_rows < 1 || table_len < 1))
+    return PFD_ERR_INVALID_ARG;
+  if (pool_rows >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_self) || !aligned16(v_self) || !aligned16(out) ||
+      (total_sel > 0 && (!aligned16(pool_k) || !aligned16(pool_v))))
+    return PFD_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  const int S = n_splits > 0 ? n_splits
+                             : plan_splits(batch, cu_lq_host, cu_k_host, Hq, Hkv, D,
+                                           max_chunk_len, self_keys);
+  const DecodeWs ws = decode_ws_layout(S, total_lq, Hq, D);
+  if (workspace_bytes < ws.total || (ws.total > 0 && workspace == nullptr) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return PFD_ERR_INVALID_ARG;
+  const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+
+  const int Tq = kBlockM / G;
+  AttnParams ap;
+  std::memset(&ap, 0, sizeof(ap));
+  if (!make_kv_maps(ap.tm_k, 1, k_self, total_lq, Hkv, D) ||
+      !make_kv_maps(ap.tm_v, 1, v_self, total_lq, Hkv, D) ||
+      !make_map(&ap.tm_q[0], q, total_lq, Hq, D, G, Tq))
+    return PFD_ERR_CUDA;
+  ap.tm_q[1] = ap.tm_q[0];
+  if (total_sel > 0) {
+    if (!make_kv_maps(ap.tm_k, 0, pool_k, pool_rows, Hkv, D) ||
+        !make_kv_maps(ap.tm_v, 0, pool_v, pool_rows, Hkv, D))
+      return PFD_ERR_CUDA;
+  } else {
+    copy_kv_maps(ap.tm_k, 0, 1);
+    copy_kv_maps(ap.tm_v, 0, 1);
+  }
+  ap.Tq = Tq;
+  int mt_max = 0;
+  for (int b = 0; b < batch; ++b)
+    mt_max = std::max(mt_max, ceil_div(cu_lq_host[b + 1] - cu_lq_host[b], Tq));
+  ap.q = reinterpret_cast<const bf16*>(q);
+  ap.out = reinterpret_cast<bf16*>(out);
+  ap.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+  ap.lse = lse;
+  ap.part_m = S > 1 ? reinterpret_cast<float*>(wsb + ws.part_m) : nullptr;
+  ap.part_l = S > 1 ? reinterpret_cast<float*>(wsb + ws.part_l) : nullptr;
+  ap.part_acc = S > 1 ? reinterpret_cast<bf16*>(wsb + ws.part_acc) : nullptr;
+  ap.table = table;
+  ap.sel = sel;
+  ap.cu_k = cu_k;
+  ap.cu_lq = cu_lq;
+  ap.dev_err = dev_err;
+  ap.pool_rows = pool_rows;
+  ap.table_len = table_len;
+  ap.mode = kModeDecode;
+  ap.Hq = Hq;
+  ap.Hkv = Hkv;
+  ap.G = G;
+  ap.D = D;
+  ap.batch = batch;
+  ap.mt_max = mt_max;
+  ap.n_splits = S;
+  ap.total_lq = total_lq;
+  ap.total_sel = total_sel;
+  ap.self_keys = self_keys ? 1 : 0;
+  ap.scale_log2 = scale * kLog2e;
+  const long long items = static_cast<long long>(batch) * Hkv * S * ceil_div(mt_max, 2);
+  if (items >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
+  ap.n_items = static_cast<int>(items);
+  const int grid = static_cast<int>(std::min<long long>(items, device_sm_count()));
+  pfd_status s = from_cuda(launch_attention(ap, grid, st));
+  if (s != PFD_OK || S == 1) return s;
+  MergeParams mp;
+  mp.part_m = ap.part_m;
+  mp.part_l = ap.part_l;
+  mp.part_acc = ap.part_acc;
+  mp.out = ap.out;
+  mp.lse = lse;
+  mp.n_splits = S;
+  mp.total_lq = total_lq;
+  mp.Hq = Hq;
+  mp.D = D;
+  return from_cuda(launch_lse_merge(mp, device_sm_count(), st));
+}
+
 }  // namespace
 }  // namespace pfd
 
@@ -336,43 +472,25 @@ pfd_status pfd_select_chunks_batched(const float* s_I, const float* s_P, const i
 
 int pfd_decode_plan_splits(int batch, const int32_t* cu_lq_host, const int32_t* cu_k_host,
                            int Hq, int Hkv, int D, int max_chunk_len) {
-  (void)D;
-  if (!decode_host_ok(batch, cu_lq_host, cu_k_host) || !shapes_ok(Hq, Hkv, 128)) return 1;
-  const int G = Hq / Hkv;
-  if (G > kBlockM) return 1;
-  const int Tq = kBlockM / G;
-  long long items = 0, keys_max = 0;
-  for (int b = 0; b < batch; ++b) {
-    const long long lq = cu_lq_host[b + 1] - cu_lq_host[b];
-    const long long kb = cu_k_host[b + 1] - cu_k_host[b];
-    items += Hkv * (((lq + Tq - 1) / Tq + 1) / 2);   // two query tiles per item
-    keys_max = std::max(keys_max, kb * std::max(0, max_chunk_len) + lq);
-  }
-  if (items <= 0) return 1;
-  const long long sms = device_sm_count();   // one persistent CTA per SM
-  int best = 1;
-  double best_cost = 1e300;
-  const long long max_s = std::max<long long>(1, std::min<long long>(kMaxSplits, (keys_max + kBlockN - 1) / kBlockN));
-  for (int S = 1; S <= max_s; ++S) {
-    const long long waves = (items * S + sms - 1) / sms;
-    const long long tiles = (keys_max + static_cast<long long>(S) * kBlockN - 1) / (static_cast<long long>(S) * kBlockN);
-    // an item costs ~2 units per key tile (two query tiles) plus ~3 units of
-    // fixed cost (Q load, pipeline fill, epilogue); the merge ~ 2 units
-    const double cost = static_cast<double>(waves) * (2.0 * tiles + 3.0) + (S > 1 ? 2.0 : 0.0);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = S;
-    }
-  }
-  return best;
+  return plan_splits(batch, cu_lq_host, cu_k_host, Hq, Hkv, D, max_chunk_len, true);
 }
 
 size_t pfd_decode_workspace(int batch, const int32_t* cu_lq_host, const int32_t* cu_k_host,
                             int Hq, int Hkv, int D, int max_chunk_len, int n_splits) {
   if (!decode_host_ok(batch, cu_lq_host, cu_k_host)) return 0;
   const int S = n_splits > 0 ? n_splits
-                             : pfd_decode_plan_splits(batch, cu_lq_host, cu_k_host, Hq, Hkv, D,
-                                                      max_chunk_len);
+                             : plan_splits(batch, cu_lq_host, cu_k_host, Hq, Hkv, D,
+                                           max_chunk_len, true);
+  return decode_ws_layout(S, cu_lq_host[batch], Hq, D).total;
+}
+
+size_t pfd_decode_partial_workspace(int batch, const int32_t* cu_lq_host,
+                                    const int32_t* cu_k_host, int Hq, int Hkv, int D,
+                                    int max_chunk_len, int self_keys, int n_splits) {
+  if (!decode_host_ok(batch, cu_lq_host, cu_k_host)) return 0;
+  const int S = n_splits > 0 ? n_splits
+                             : plan_splits(batch, cu_lq_host, cu_k_host, Hq, Hkv, D,
+                                           max_chunk_len, self_keys != 0);
   return decode_ws_layout(S, cu_lq_host[batch], Hq, D).total;
 }
 
@@ -386,96 +504,47 @@ pfd_status pfd_decode_attention(const pfd_bf16* q, const pfd_bf16* k_self,
                                 float sm_scale, int n_splits, pfd_bf16* out, float* lse,
                                 int32_t* dev_err, void* workspace, size_t workspace_bytes,
                                 pfd_stream_t stream) {
-  if (!decode_host_ok(batch, cu_lq_host, cu_k_host)) return PFD_ERR_INVALID_ARG;
-  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return PFD_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return PFD_ERR_UNSUPPORTED;
-  if (!q || !k_self || !v_self || !cu_lq || !cu_k || !out) return PFD_ERR_INVALID_ARG;
-  if (n_splits < 0 || n_splits > kMaxSplits) return PFD_ERR_INVALID_ARG;
-  if (Hq / Hkv > kBlockM) return PFD_ERR_UNSUPPORTED;
-  for (int b = 0; b < batch; ++b)
-    if (cu_k_host[b + 1] - cu_k_host[b] >= kMaxSegments) return PFD_ERR_UNSUPPORTED;
-  const int total_lq = cu_lq_host[batch];
-  const int total_sel = cu_k_host[batch];
-  if (total_sel > 0 && (!pool_k || !pool_v || !table || !sel || pool_rows < 1 || table_len < 1))
-    return PFD_ERR_INVALID_ARG;
-  if (pool_rows >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k_self) || !aligned16(v_self) || !aligned16(out) ||
-      (total_sel > 0 && (!aligned16(pool_k) || !aligned16(pool_v))))
-    return PFD_ERR_INVALID_ARG;
-  const int G = Hq / Hkv;
-  const int S = n_splits > 0 ? n_splits
-                             : pfd_decode_plan_splits(batch, cu_lq_host, cu_k_host, Hq, Hkv, D,
-                                                      max_chunk_len);
-  const DecodeWs ws = decode_ws_layout(S, total_lq, Hq, D);
-  if (workspace_bytes < ws.total || (ws.total > 0 && workspace == nullptr) ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return PFD_ERR_INVALID_ARG;
-  const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  return decode_impl(q, k_self, v_self, cu_lq, cu_lq_host, pool_k, pool_v, pool_rows, table,
+                     table_len, sel, cu_k, cu_k_host, batch, Hq, Hkv, D, max_chunk_len, sm_scale,
+                     true, n_splits, out, lse, dev_err, workspace, workspace_bytes, stream);
+}
 
-  const int Tq = kBlockM / G;
-  AttnParams ap;
-  std::memset(&ap, 0, sizeof(ap));
-  if (!make_kv_maps(ap.tm_k, 1, k_self, total_lq, Hkv, D) ||
-      !make_kv_maps(ap.tm_v, 1, v_self, total_lq, Hkv, D) ||
-      !make_map(&ap.tm_q[0], q, total_lq, Hq, D, G, Tq))
-    return PFD_ERR_CUDA;
-  ap.tm_q[1] = ap.tm_q[0];
-  if (total_sel > 0) {
-    if (!make_kv_maps(ap.tm_k, 0, pool_k, pool_rows, Hkv, D) ||
-        !make_kv_maps(ap.tm_v, 0, pool_v, pool_rows, Hkv, D))
-      return PFD_ERR_CUDA;
-  } else {
-    copy_kv_maps(ap.tm_k, 0, 1);
-    copy_kv_maps(ap.tm_v, 0, 1);
-  }
-  ap.Tq = Tq;
-  int mt_max = 0;
-  for (int b = 0; b < batch; ++b)
-    mt_max = std::max(mt_max, ceil_div(cu_lq_host[b + 1] - cu_lq_host[b], Tq));
-  ap.q = reinterpret_cast<const bf16*>(q);
-  ap.out = reinterpret_cast<bf16*>(out);
-  ap.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
-  ap.lse = lse;
-  ap.part_m = S > 1 ? reinterpret_cast<float*>(wsb + ws.part_m) : nullptr;
-  ap.part_l = S > 1 ? reinterpret_cast<float*>(wsb + ws.part_l) : nullptr;
-  ap.part_acc = S > 1 ? reinterpret_cast<bf16*>(wsb + ws.part_acc) : nullptr;
-  ap.table = table;
-  ap.sel = sel;
-  ap.cu_k = cu_k;
-  ap.cu_lq = cu_lq;
-  ap.dev_err = dev_err;
-  ap.pool_rows = pool_rows;
-  ap.table_len = table_len;
-  ap.mode = kModeDecode;
-  ap.Hq = Hq;
-  ap.Hkv = Hkv;
-  ap.G = G;
-  ap.D = D;
-  ap.batch = batch;
-  ap.mt_max = mt_max;
-  ap.n_splits = S;
-  ap.total_lq = total_lq;
-  ap.total_sel = total_sel;
-  ap.scale_log2 = scale * kLog2e;
-  const long long items = static_cast<long long>(batch) * Hkv * S * ceil_div(mt_max, 2);
-  if (items >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
-  ap.n_items = static_cast<int>(items);
-  const int grid = static_cast<int>(std::min<long long>(items, device_sm_count()));
-  pfd_status s = from_cuda(launch_attention(ap, grid, st));
-  if (s != PFD_OK || S == 1) return s;
+pfd_status pfd_decode_partial(const pfd_bf16* q, const pfd_bf16* k_self, const pfd_bf16* v_self,
+                              const int32_t* cu_lq, const int32_t* cu_lq_host,
+                              const pfd_bf16* pool_k, const pfd_bf16* pool_v, int64_t pool_rows,
+                              const pfd_chunk_entry* table, int32_t table_len, const int32_t* sel,
+                              const int32_t* cu_k, const int32_t* cu_k_host, int batch, int Hq,
+                              int Hkv, int D, int max_chunk_len, float sm_scale, int self_keys,
+                              int n_splits, pfd_bf16* part_o, float* part_lse, int32_t* dev_err,
+                              void* workspace, size_t workspace_bytes, pfd_stream_t stream) {
+  if (part_lse == nullptr || (self_keys != 0 && self_keys != 1)) return PFD_ERR_INVALID_ARG;
+  return decode_impl(q, k_self, v_self, cu_lq, cu_lq_host, pool_k, pool_v, pool_rows, table,
+                     table_len, sel, cu_k, cu_k_host, batch, Hq, Hkv, D, max_chunk_len, sm_scale,
+                     self_keys != 0, n_splits, part_o, part_lse, dev_err, workspace,
+                     workspace_bytes, stream);
+}
+
+pfd_status pfd_lse_merge(const pfd_bf16* part_o, const float* part_lse, int n_parts, int rows,
+                         int Hq, int D, pfd_bf16* out, float* lse, pfd_stream_t stream) {
+  if (!part_o || !part_lse || !out || n_parts < 1 || rows < 1 || Hq < 1)
+    return PFD_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return PFD_ERR_UNSUPPORTED;
+  if (n_parts > kMaxSplits) return PFD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(n_parts) * rows * Hq * D >= (1ll << 40)) return PFD_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(part_o) & 7u) != 0 || (reinterpret_cast<uintptr_t>(out) & 7u) != 0)
+    return PFD_ERR_INVALID_ARG;
   MergeParams mp;
-  mp.part_m = ap.part_m;
-  mp.part_l = ap.part_l;
-  mp.part_acc = ap.part_acc;
-  mp.out = ap.out;
+  std::memset(&mp, 0, sizeof(mp));
+  mp.part_m = part_lse;
+  mp.part_l = nullptr;   // states given as log-sum-exp
+  mp.part_acc = reinterpret_cast<const bf16*>(part_o);
+  mp.out = reinterpret_cast<bf16*>(out);
   mp.lse = lse;
-  mp.n_splits = S;
-  mp.total_lq = total_lq;
+  mp.n_splits = n_parts;
+  mp.total_lq = rows;
   mp.Hq = Hq;
   mp.D = D;
-  return from_cuda(launch_lse_merge(mp, device_sm_count(), st));
+  return from_cuda(launch_lse_merge(mp, device_sm_count(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -78,6 +78,7 @@ struct AttnParams {
 
   // decode
   int batch, mt_max, n_splits, total_lq, total_sel;
+  int self_keys;        // 1: the live block is the last key segment; 0: selected chunks only
 
   float scale_log2;     // sm_scale * log2(e)
   int out_v8;           // out is 32-byte aligned: whole-sector (32-byte) stores
@@ -130,6 +131,9 @@ cudaError_t launch_select(const float* s_i, const float* s_p, const int32_t* cu_
 
 // ------------------------------------------------------------ LSE merge --
 struct MergeParams {
+  // Split states: part_m = max (log2 units) and part_l = denominator, or,
+  // when part_l is null, part_m = natural-log log-sum-exp of the split (its
+  // denominator relative to a max of 0: m = lse * log2(e), l = 1).
   const float* part_m;
   const float* part_l;
   const bf16* part_acc;     // normalised (acc / l) bf16

@@ -44,7 +44,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert _abi.pfd_abi_version() == 1
+    assert _abi.pfd_abi_version() == 2
     assert _abi.pfd_status_string(0) == "PFD_OK"
     assert _abi.pfd_status_string(1) == "PFD_ERR_INVALID_ARG"
     assert _abi.pfd_status_string(2) == "PFD_ERR_UNSUPPORTED"
@@ -116,3 +116,30 @@ def test_decode_host_checks_and_plan(lib):
     assert _abi.pfd_decode_workspace(1, [0, 320], [0, 4], 28, 4, 128, 257, 1) == 0
     ws2 = _abi.pfd_decode_workspace(1, [0, 320], [0, 4], 28, 4, 128, 257, 2)
     assert ws2 >= 2 * 320 * 28 * (2 * 4 + 128 * 2)   # fp32 (m, l) and bf16 O per row and split
+
+
+def test_partial_and_merge_host_checks(lib):
+    """pfd_decode_partial needs part_lse and self_keys in {0, 1};
+    pfd_lse_merge checks its counts, head dim and alignment on the host."""
+    cu_lq = (ctypes.c_int32 * 2)(0, 320)
+    cu_k = (ctypes.c_int32 * 2)(0, 4)
+    args = [256, 256, 256, 256, cu_lq, 256, 256, 100, 256, 16, 256, 256, cu_k, 1, 28, 4, 128, 257,
+            0.0, 1, 1, 256, 256, None, None, 0, None]
+    a = list(args)
+    a[22] = None                  # part_lse is required
+    assert lib.pfd_decode_partial(*a) == 1
+    a = list(args)
+    a[19] = 2                     # self_keys must be 0 or 1
+    assert lib.pfd_decode_partial(*a) == 1
+    a = list(args)
+    a[0] = 8                      # misaligned q
+    assert lib.pfd_decode_partial(*a) == 1
+    assert lib.pfd_lse_merge(256, 256, 0, 4, 4, 128, 256, None, None) == 1
+    assert lib.pfd_lse_merge(256, 256, 2, 4, 4, 96, 256, None, None) == 2
+    assert lib.pfd_lse_merge(256, 256, 65, 4, 4, 128, 256, None, None) == 2
+    assert lib.pfd_lse_merge(258, 256, 2, 4, 4, 128, 256, None, None) == 1
+    assert lib.pfd_lse_merge(None, 256, 2, 4, 4, 128, 256, None, None) == 1
+    # without the live block the planner sees fewer keys, never more splits
+    with_self = _abi.pfd_decode_partial_workspace(1, [0, 320], [0, 4], 28, 4, 128, 257, 1, 0)
+    assert with_self == _abi.pfd_decode_workspace(1, [0, 320], [0, 4], 28, 4, 128, 257, 0)
+    assert _abi.pfd_decode_partial_workspace(1, [0, 320], [0, 4], 28, 4, 128, 257, 0, 1) == 0
