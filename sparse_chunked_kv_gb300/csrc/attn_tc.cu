@@ -86,6 +86,8 @@ struct TileMeta {
   uint32_t nvalid_hi;  // groups 4..7
   int32_t ngroups;     // 0 only for the single tile of an empty item
   int32_t last;        // 1 on the last tile of an item
+  int32_t fix_v;       // 1 when a group is ragged and unshifted: its V rows
+                       // past the segment must be zeroed before PV
 };
 
 struct Shared {
@@ -324,9 +326,10 @@ attention_kernel(const __grid_constant__ AttnParams p) {
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&sh.s_full[x], 1);
-      mbar_init(&sh.p_full[x], kWgThreads);
+      // one arrival per softmax warp (after a warp sync), not per thread
+      mbar_init(&sh.p_full[x], kWgThreads / 32);
       mbar_init(&sh.o_full[x], 1);
-      mbar_init(&sh.o_free[x], kWgThreads);
+      mbar_init(&sh.o_free[x], kWgThreads / 32);
     }
     mbar_init(&sh.drain, 1);
     fence_barrier_init();
@@ -405,6 +408,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         packed |= __shfl_xor_sync(0xFFFFFFFFu, packed, 2);
         const uint32_t nv_lo = __shfl_sync(0xFFFFFFFFu, packed, 0);
         const uint32_t nv_hi = __shfl_sync(0xFFFFFFFFu, packed, 4);
+        const bool fix_v = __any_sync(0xFFFFFFFFu, lane < ng && code < kGroupRows);
         // Runs: group k continues group k-1's run when it is the next 16 rows
         // of the same tensor.  A lane that starts a run loads the whole run,
         // one box per set bit of its length (16..128 rows).
@@ -428,6 +432,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
           m.nvalid_hi = nv_hi;
           m.ngroups = ng;
           m.last = (j == tiles_to_publish - 1) ? 1 : 0;
+          m.fix_v = fix_v ? 1 : 0;
           mbar_arrive(&sh.meta_full[ms]);
         }
         ++tile_ctr;
@@ -507,6 +512,11 @@ attention_kernel(const __grid_constant__ AttnParams p) {
       int items_done = 0;
       bool ok = true;
       constexpr uint32_t idesc_o = idesc_bf16(kBlockM, D, false, true);
+      // Base descriptors: Q tile 0 and K in ring slot 0 (K-major), V in ring
+      // slot 0 (MN-major, 64-column panels kPanelBytes apart).
+      const uint64_t desc_q0 = sw128_desc(s_base + L::kQ0, 16, 1024);
+      const uint64_t desc_ring_k = sw128_desc(s_base + L::kRing0, 16, 1024);
+      const uint64_t desc_ring_v = sw128_desc(s_base + L::kRing0, kPanelBytes, 1024);
       for (int kk = 0, idx; ok && (idx = nth_item<kPrefill>(p, kk)) >= 0; ++kk) {
         Item it;
         if (!resolve_item(p, idx, it)) continue;
@@ -521,16 +531,22 @@ attention_kernel(const __grid_constant__ AttnParams p) {
           return r;
         };
         if (!mbar_wait(&sh.q_full, items_done & 1)) { ok = false; break; }
-        // QK of one tile into S_x from the K slot `ks`.
+        // QK of one tile into S_x from the K slot `ks`.  A descriptor's
+        // address field holds (address >> 4) in 14 bits and every operand
+        // here lies in this CTA's shared memory, so the descriptor of base +
+        // offset is the base descriptor plus offset >> 4: the loop adds
+        // constants to descriptors made once per kernel.
         auto issue_qk = [&](int x, int ng, uint32_t ks) {
-          const uint32_t q_addr = s_base + (x ? L::kQ1 : L::kQ0);
-          const uint32_t k_addr = s_base + L::kRing0 + ks * L::kTileBytes;
-          const uint32_t idesc_s = idesc_bf16(kBlockM, ng * kGroupRows, false, false);
+          const uint64_t a0 = desc_q0 + (x ? (L::kTileBytes >> 4) : 0u);
+          const uint64_t b0 = desc_ring_k + ks * (L::kTileBytes >> 4);
+          const uint32_t idesc_s = ng == kGroupsPerTile
+                                       ? idesc_bf16(kBlockM, kBlockN, false, false)
+                                       : idesc_bf16(kBlockM, ng * kGroupRows, false, false);
+          const uint32_t d_s = tmem + tmem_s_col(x);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = sw128_desc(q_addr + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = sw128_desc(k_addr + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
-            mma_bf16_ss(tmem + tmem_s_col(x), a, b, idesc_s, kk > 0 ? 1u : 0u);
+            const uint32_t off = ((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4;
+            mma_bf16_ss(d_s, a0 + off, b0 + off, idesc_s, kk > 0 ? 1u : 0u);
           }
           mma_commit(&sh.s_full[x]);
         };
@@ -555,11 +571,17 @@ attention_kernel(const __grid_constant__ AttnParams p) {
           if (wrote) fence_proxy_async_smem();
         };
         auto issue_pv = [&](int x, int ng, uint32_t vs, bool first) {
-          const uint32_t v_addr = s_base + L::kRing0 + vs * L::kTileBytes;
-          for (int kk = 0; kk < ng; ++kk) {
-            const uint64_t v = sw128_desc(v_addr + kk * 2048, kPanelBytes, 1024);
-            mma_bf16_ts(tmem + tmem_o_col(x), tmem + tmem_s_col(x) + kk * 8, v, idesc_o,
-                        (!first || kk > 0) ? 1u : 0u);
+          const uint64_t v0 = desc_ring_v + vs * (L::kTileBytes >> 4);
+          const uint32_t d_o = tmem + tmem_o_col(x), a_p = tmem + tmem_s_col(x);
+          if (ng == kGroupsPerTile) {
+#pragma unroll
+            for (int kk = 0; kk < kGroupsPerTile; ++kk)
+              mma_bf16_ts(d_o, a_p + kk * 8, v0 + kk * (2048 >> 4), idesc_o,
+                          (!first || kk > 0) ? 1u : 0u);
+          } else {
+            for (int kk = 0; kk < ng; ++kk)
+              mma_bf16_ts(d_o, a_p + kk * 8, v0 + kk * (2048 >> 4), idesc_o,
+                          (!first || kk > 0) ? 1u : 0u);
           }
         };
         // Tile 0.
@@ -583,9 +605,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
               vs = ring_ctr % kRing;
               if (!mbar_wait(&sh.ring_full[vs], (ring_ctr / kRing) & 1)) { ok = false; break; }
               ++ring_ctr;
-              const bool full_tile = mt.ngroups == kGroupsPerTile && mt.nvalid_lo == 0x10101010u &&
-                                     mt.nvalid_hi == 0x10101010u;
-              if (!full_tile) fix_v(mt, vs);
+              if (mt.fix_v) fix_v(mt, vs);
             }
             TileMeta mn = mt;
             uint32_t ks_next = 0;
@@ -708,20 +728,42 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         // Ragged tiles: logits of key rows outside a group's valid rows become
         // -inf (their exp2 is then 0): the rows past the count, or for a
         // shifted group the leading rows that repeat the previous group's keys.
-        auto mask_half = [&](uint32_t (&sr)[2][32], int half) {
+        // valid16(code): bit i set when row i of the group is one of its keys.
+        auto valid16 = [](int code) -> uint32_t {
+          if (code & kShifted) return (0xFFFFu << (kGroupRows - (code & 0x1f))) & 0xFFFFu;
+          return (1u << code) - 1u;   // code 16: all rows; 0: none
+        };
+        // Masks the groups of this half whose bit is set in `which` (a
+        // warp-uniform 4-bit set); each group is one uniform branch, so tiles
+        // with one ragged group pay for that group only.
+        auto mask_half = [&](uint32_t (&sr)[2][32], int half, uint32_t which) {
 #pragma unroll
           for (int gq = 0; gq < 4; ++gq) {
-            const int code = nv_of(half * 4 + gq);
-            if (code != kGroupRows) {   // warp-uniform: ragged, shifted or absent
-              const bool sh_grp = (code & kShifted) != 0;
-              const int lo = sh_grp ? kGroupRows - (code & 0x1f) : 0;
-              const int hi = sh_grp ? kGroupRows : code;
+            if (which & (1u << gq)) {
+              const uint32_t vm = valid16(nv_of(half * 4 + gq));
 #pragma unroll
               for (int i = 0; i < 16; ++i)
-                if (i < lo || i >= hi) sr[gq >> 1][(gq & 1) * 16 + i] = __float_as_uint(-INFINITY);
+                if (!((vm >> i) & 1u)) sr[gq >> 1][(gq & 1) * 16 + i] = __float_as_uint(-INFINITY);
             }
           }
         };
+        // Groups that need masking, per half: for the row sum and P every
+        // group that is not 16 keys (rag2); for the row max only those whose
+        // extra rows are not keys of this row at all (rag1: groups past the
+        // tile's end, and an unshifted ragged group, whose rows past its
+        // segment may hold another slot or padding).  A shifted group's
+        // repeated rows are keys of the same segment, harmless to the max.
+        uint32_t rag1 = 0, rag2 = 0;
+        if (!full) {
+#pragma unroll
+          for (int g = 0; g < kGroupsPerTile; ++g) {
+            const int code = nv_of(g);
+            if (code != kGroupRows) {
+              rag2 |= 1u << g;
+              if (!(code & kShifted)) rag1 |= 1u << g;
+            }
+          }
+        }
 
         // Pass 1: row max over the tile, 64 columns (two TMEM loads) at a time.
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -733,7 +775,8 @@ attention_kernel(const __grid_constant__ AttnParams p) {
             tmem_ld32(lane_base + s_col + half * 64 + 32, sr[1]);
             tmem_ld_wait(sr[0]);
             reg_fence(sr[1]);
-            if (!full) mask_half(sr, half);
+            const uint32_t m1 = (rag1 >> (4 * half)) & 0xFu;
+            if (m1) mask_half(sr, half, m1);
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
               const int a = (i >> 1) & 1;
@@ -785,7 +828,8 @@ attention_kernel(const __grid_constant__ AttnParams p) {
             tmem_ld32(lane_base + s_col + half * 64 + 32, sr[1]);
             tmem_ld_wait(sr[0]);
             reg_fence(sr[1]);
-            if (!full) mask_half(sr, half);
+            const uint32_t m2 = (rag2 >> (4 * half)) & 0xFu;
+            if (m2) mask_half(sr, half, m2);
             uint32_t packed[32];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
@@ -814,8 +858,11 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         // the next item's Q arrive), else right after the first tile's P.
         const bool bos_now = kPrefill && n_seen == 1;
         if (bos_now && meta.last) s_bos = bos_logit();
+        // Every lane's TMEM reads of S and stores of P are complete (waited
+        // above); the warp sync orders them before lane 0's arrival.
         tc_fence_before_sync();
-        mbar_arrive(&sh.p_full[x]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.p_full[x]);
         if (bos_now && !meta.last) s_bos = bos_logit();
         if (meta.last) break;
       }
@@ -930,7 +977,8 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         }
       }
       tc_fence_before_sync();
-      mbar_arrive(&sh.o_free[x]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.o_free[x]);
       ++items_done;
     }
     if (!ok) atomicOr(&sh.failed, 4);
