@@ -430,6 +430,44 @@ def time_workload(name, rank, device, reps=5):
     return res
 
 
+def time_scoring_head(device, reps=10):
+    """The chunk-score head on the 8K-prefix shape: 16 chunks x (64 window +
+    256 pseudo-label rows) x the 152,064-entry vocabulary, logits drawn on
+    the device from a seeded generator (N(0, 4), bf16).  One call reads
+    1.56 GB (> L2), so no flush is needed; median of reps after 3 warm-ups."""
+    import torch
+
+    from sparse_chunked_kv_gb300 import _abi
+    from sparse_chunked_kv_gb300 import workloads as wl
+    n, r, v = 16, 64 + 256, wl.SCORING_VOCAB
+    gen = torch.Generator(device=device).manual_seed(5)
+    logits = (2.0 * torch.randn(n, r, v, generator=gen, device=device)).to(torch.bfloat16)
+    labels = torch.randint(0, v, (r,), generator=gen, device=device, dtype=torch.int32)
+    row_ll = torch.empty(n, r, dtype=torch.float32, device=device)
+    score = torch.empty(n, dtype=torch.float32, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.Stream(device)
+    ms = []
+    with torch.cuda.stream(stream):
+        for it in range(3 + reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            _abi.pfd_chunk_loglik(logits, labels, n, r, v, row_ll, score, err)
+            e1.record(stream)
+            e1.synchronize()
+            if it >= 3:
+                ms.append(e0.elapsed_time(e1))
+    if int(err.item()) != 0:
+        raise RuntimeError(f"scoring head: device error word {int(err.item())}")
+    t = statistics.median(ms) * 1e-3
+    nbytes = n * r * v * 2 + r * 4 + n * r * 4 + n * 4
+    del logits
+    torch.cuda.empty_cache()
+    return {"workload": f"{n} chunks x {r} labelled rows x vocabulary {v}, bf16 logits",
+            "us": t * 1e6, "gbs": nbytes / t / 1e9, "bytes": nbytes, "bound": "hbm",
+            "timing": f"median of {reps} calls after 3 warm-ups (inputs larger than L2)"}
+
+
 def run_e2e(args, job, stream):
     """The same work through the C ABI from pinned host buffers.
 
@@ -712,10 +750,11 @@ def main():
     if world > 1:
         res["dec_ms"], res["pre_ms"], res["step_ms"] = max_over_ranks(
             [res["dec_ms"], res["pre_ms"], res["step_ms"]], device)
-    others = {}
+    others, next_rows = {}, {}
     if rank == 0:
         for name in [x for x in args.per_config.split(",") if x and x != args.config]:
             others[name] = time_workload(name, 0, device)
+        next_rows["scoring_head"] = time_scoring_head(device)
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -770,6 +809,15 @@ def main():
                 "prefill_tflops": f2["prefill_tflops"], "prefill_gbs": f2["prefill_gbs"],
                 "prefill_bound": f2["prefill_bound"], "prefill_frac": f2["prefill_frac"],
                 "timing": "median of 5 graph replays after 3 warm-ups, L2 flushed between"}
+    if next_rows:
+        line["next_rows"] = {}
+        for key, row in next_rows.items():
+            row = dict(row)
+            if row["bound"] == "hbm":
+                row["frac"] = row["gbs"] / hbm
+                row["peak"] = hbm
+                row["peak_kind"] = f"{peak_kind} HBM copy"
+            line["next_rows"][key] = row
     if "e2e" in res:
         e = res["e2e"]
         line["e2e"] = {"value": job_tflops(world, dflops, T, e["dec_ms"]), "unit": "TFLOP/s",

@@ -70,6 +70,7 @@ typedef enum {
 #define PFD_DEVERR_SLOT 4    /* slot_row[j] + B + 1 outside [0, pool_rows]    */
 #define PFD_DEVERR_TIMEOUT 8 /* an internal pipeline wait ran out of budget    */
 #define PFD_DEVERR_SHAPE 16  /* device cu_lq / cu_k disagree with host sizes   */
+#define PFD_DEVERR_LABEL 32  /* a label outside [0, vocab)                     */
 
 typedef uint16_t pfd_bf16; /* raw bfloat16 bits */
 
@@ -139,6 +140,27 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
                              int64_t pool_rows, const int32_t* slot_row, pfd_chunk_entry* table,
                              int32_t* dev_err, void* workspace, size_t workspace_bytes,
                              pfd_stream_t stream);
+
+/*
+ * Chunk scores from the model's logits (Methodology 1, predictive scoring:
+ * s_I is the negative log-likelihood of the query window given the chunk,
+ * s_P the likelihood of the pseudo-labels given the chunk and the query).
+ * For every chunk j and labelled row r:
+ *   row_ll[j][r] = logits[j][r][labels[r]] - log(sum_v exp(logits[j][r][v]))
+ *   score[j]     = sum_r row_ll[j][r]
+ * i.e. the summed log-likelihood of the labels.  With the query-window
+ * tokens as labels this is s_I negated (higher = more relevant, as
+ * pfd_select_chunks takes it); with the pseudo-labels it is s_P.
+ *   logits  [N, R, V] bf16 device (finite values)
+ *   labels  [R] int32 device, shared by every chunk; a label outside
+ *           [0, V) gives that row NaN and sets PFD_DEVERR_LABEL
+ *   row_ll  [N, R] fp32 device (written);  score [N] fp32 device (written)
+ * 1 <= N, 1 <= R, N * R < 2^31, 1 <= V < 2^31.  One pass over the logits:
+ * HBM-bound.  The result does not depend on scheduling (fixed-order sums).
+ */
+pfd_status pfd_chunk_loglik(const pfd_bf16* logits, const int32_t* labels, int N, int R,
+                            int64_t V, float* row_ll, float* score, int32_t* dev_err,
+                            pfd_stream_t stream);
 
 /*
  * Chunk selection (Methodology 1, "Selection"; Methodology 2 inter-chunk

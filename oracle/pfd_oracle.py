@@ -43,6 +43,11 @@ Readings where the pages leave a step open (each is stated where it is used):
   R4  The decode live block (query window + response, Lq rows) attends to
       itself and to the kept rows of the selected chunks, with no mask.
   R5  The softmax scale is 1/sqrt(D) unless given.
+  R6  The chunk scores come from the model's logits: s_I is the
+      log-likelihood of the query-window tokens and s_P that of the
+      pseudo-labels, each conditioned on the chunk -- the sum over the
+      labelled rows of log softmax(logits)[label].  s_I is the negated NLL
+      of the pages, so that both are "higher = more relevant" (R3).
 
 Inputs are float64 arrays (bf16 tensors widened exactly) and int arrays.
 All arithmetic is fp64 with numpy's matmul/exp/log; nothing is blocked,
@@ -281,6 +286,26 @@ def decode_attention_split(q, k_self, v_self, pool_k, pool_v, table, sel, sm_sca
         parts.append(split_partials(q, pool_k[lo:lo + n], pool_v[lo:lo + n], group, sm_scale))
     parts.append(split_partials(q, k_self, v_self, group, sm_scale))
     return lse_merge(parts)
+
+
+# ------------------------------------------------------- chunk scores --
+
+def chunk_loglik(logits, labels):
+    """[M1] + R6: summed label log-likelihood of every chunk.
+
+    logits: [N, R, V] (the model's outputs at R labelled positions when
+    conditioned on chunk j); labels: [R] ints in [0, V) (the query-window
+    tokens for s_I, the pseudo-labels for s_P).  Row r's log-probability of
+    its label is logits[j, r, y_r] - log(sum_v exp(logits[j, r, v])).
+    Returns (score [N], rows [N, R]) in fp64.
+    """
+    z = np.asarray(logits, dtype=np.float64)
+    y = np.asarray(labels, dtype=np.int64)
+    m = z.max(axis=-1, keepdims=True)
+    lse = m[..., 0] + np.log(np.exp(z - m).sum(axis=-1))
+    picked = np.take_along_axis(z, y[None, :, None].repeat(z.shape[0], axis=0), axis=-1)[..., 0]
+    rows = picked - lse
+    return rows.sum(axis=1), rows
 
 
 # ------------------------------------------------------ cost model [M3] --

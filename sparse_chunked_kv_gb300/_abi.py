@@ -17,7 +17,7 @@ STATUS_NAMES = {0: "PFD_OK", 1: "PFD_ERR_INVALID_ARG", 2: "PFD_ERR_UNSUPPORTED",
 # PFD_DECODE_STATIC_SCRATCH_BYTES of include/pfd.h
 DECODE_STATIC_SCRATCH_BYTES = 32 << 20
 
-DEVERR_TABLE, DEVERR_SEL, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_SHAPE = 1, 2, 4, 8, 16
+DEVERR_TABLE, DEVERR_SEL, DEVERR_SLOT, DEVERR_TIMEOUT, DEVERR_SHAPE, DEVERR_LABEL = 1, 2, 4, 8, 16, 32
 
 # (restype, argtypes) of every exported symbol, in the order of include/pfd.h.
 _P = ctypes.c_void_p
@@ -29,6 +29,7 @@ SIGNATURES = {
     "pfd_chunk_prefill_workspace": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "pfd_chunk_prefill": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P,
                                _I64, _P, _P, _P, _P, _SZ, _P]),
+    "pfd_chunk_loglik": (_I, [_P, _P, _I, _I, _I64, _P, _P, _P, _P]),
     "pfd_select_chunks": (_I, [_P, _P, _I, _I, _P, _P, _P]),
     "pfd_select_chunks_batched": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P]),
     "pfd_decode_plan_splits": (_I, [_I, _P, _P, _I, _I, _I, _I]),
@@ -197,3 +198,8 @@ def pfd_decode_partial(q, k_self, v_self, cu_lq, cu_lq_host, pool_k, pool_v, poo
 def pfd_lse_merge(part_o, part_lse, n_parts, rows, Hq, D, out, lse, stream=None):
     _check(load().pfd_lse_merge(_ptr(part_o), _ptr(part_lse), n_parts, rows, Hq, D, _ptr(out),
                                 _ptr(lse), _stream(stream)))
+
+
+def pfd_chunk_loglik(logits, labels, N, R, V, row_ll, score, dev_err, stream=None):
+    _check(load().pfd_chunk_loglik(_ptr(logits), _ptr(labels), N, R, int(V), _ptr(row_ll),
+                                   _ptr(score), _ptr(dev_err), _stream(stream)))

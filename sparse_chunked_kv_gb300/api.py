@@ -147,3 +147,20 @@ def lse_merge(part_o, part_lse, out=None, lse=None, stream=None):
         lse = torch.empty(rows, hq, dtype=torch.float32, device=part_o.device)
     _abi.pfd_lse_merge(part_o, part_lse, s, rows, hq, d, out, lse, stream)
     return out, lse
+
+
+def chunk_loglik(logits, labels, row_ll=None, score=None, dev_err=None, stream=None):
+    """Summed label log-likelihood per chunk (pfd_chunk_loglik): logits
+    [N, R, V] bf16, labels [R] int32.  Returns (score [N], row_ll [N, R],
+    dev_err)."""
+    _need_cuda(logits, labels)
+    n, r, v = logits.shape
+    dev = logits.device
+    if row_ll is None:
+        row_ll = torch.empty(n, r, dtype=torch.float32, device=dev)
+    if score is None:
+        score = torch.empty(n, dtype=torch.float32, device=dev)
+    if dev_err is None:
+        dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    _abi.pfd_chunk_loglik(logits, labels, n, r, v, row_ll, score, dev_err, stream)
+    return score, row_ll, dev_err

@@ -452,6 +452,17 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
   return from_cuda(launch_topb_compact(tp, st));   // sets the copy splits
 }
 
+pfd_status pfd_chunk_loglik(const pfd_bf16* logits, const int32_t* labels, int N, int R,
+                            int64_t V, float* row_ll, float* score, int32_t* dev_err,
+                            pfd_stream_t stream) {
+  if (!logits || !labels || !row_ll || !score || N < 1 || R < 1 || V < 1)
+    return PFD_ERR_INVALID_ARG;
+  if (static_cast<long long>(N) * R >= (1ll << 31) || V >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
+  return from_cuda(launch_chunk_loglik(reinterpret_cast<const bf16*>(logits), labels, N, R, V,
+                                       row_ll, score, dev_err,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
 pfd_status pfd_select_chunks(const float* s_I, const float* s_P, int N, int K, int32_t* sel,
                              float* s_out, pfd_stream_t stream) {
   if (!s_I || !s_P || !sel || N < 1 || K < 1 || K > N) return PFD_ERR_INVALID_ARG;

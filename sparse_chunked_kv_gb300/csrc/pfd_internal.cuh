@@ -146,6 +146,11 @@ struct MergeParams {
 // sm_count: SMs of the current device (the grid is one wave of resident CTAs).
 cudaError_t launch_lse_merge(const MergeParams& p, int sm_count, cudaStream_t stream);
 
+// -------------------------------------------------------- chunk scores --
+cudaError_t launch_chunk_loglik(const bf16* logits, const int32_t* labels, int n_chunks,
+                                int n_rows, long long vocab, float* row_ll, float* score,
+                                int32_t* dev_err, cudaStream_t stream);
+
 // ------------------------------------------------------------- helpers --
 // Raises a kernel's dynamic shared-memory limit once per (kernel, device), so
 // that later calls -- including calls made while a stream is being captured

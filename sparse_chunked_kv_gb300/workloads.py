@@ -184,6 +184,20 @@ def live_block(req: dict, step_inputs: dict) -> tuple:
     return q, k, v
 
 
+# Vocabulary of the scoring-head workload: a 7B-scale language model's
+# vocabulary size (152,064 entries).
+SCORING_VOCAB = 152064
+
+
+def make_logits(n_chunks: int, n_rows: int, vocab: int, seed: int, scale: float = 2.0) -> tuple:
+    """Synthetic logits [N, R, V] bf16 ~ N(0, scale^2) and labels [R] int32
+    uniform in [0, V), drawn in that order from a generator seeded `seed`."""
+    gen = torch.Generator().manual_seed(seed)
+    logits = (scale * torch.randn(n_chunks, n_rows, vocab, generator=gen)).to(torch.bfloat16)
+    labels = torch.randint(0, vocab, (n_rows,), generator=gen, dtype=torch.int64).to(torch.int32)
+    return logits, labels
+
+
 def to_f64(t: torch.Tensor):
     """Exact widening of a bf16/fp32 CPU tensor to a float64 numpy array."""
     return t.to(torch.float64).numpy()

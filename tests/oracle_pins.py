@@ -342,9 +342,43 @@ def check_cost_model(orc):
     assert macs[0] == macs[1], "decode cost must not depend on N"
 
 
+# ----------------------------------------------------------- chunk scores --
+
+def check_loglik_vs_cross_entropy(orc, seed=15):
+    """Summed label log-likelihood == -(torch cross-entropy, summed), the
+    library's own log-softmax + NLL, chunk by chunk, and the row values."""
+    gen = torch.Generator().manual_seed(seed)
+    n, r, v = 3, 5, 37
+    z = torch.randn(n, r, v, generator=gen, dtype=torch.float64) * 3.0
+    y = torch.randint(0, v, (r,), generator=gen)
+    score, rows = orc.chunk_loglik(z.numpy(), y.numpy())
+    for j in range(n):
+        ce = torch.nn.functional.cross_entropy(z[j], y, reduction="none").numpy()
+        assert np.max(np.abs(rows[j] + ce)) < 1e-12, "row log-likelihood != -cross-entropy"
+        assert abs(score[j] + ce.sum()) < 1e-11, "chunk score != -summed cross-entropy"
+
+
+def check_loglik_closed_forms(orc):
+    """Uniform logits give -R log V; one class gives 0; two classes give the
+    log-sigmoid of the logit margin; adding a constant to a row changes
+    nothing (log-softmax is shift invariant)."""
+    z = np.full((2, 4, 9), 0.7)
+    score, _ = orc.chunk_loglik(z, np.array([0, 3, 8, 5]))
+    assert np.allclose(score, -4 * math.log(9.0), rtol=0, atol=1e-12)
+    score, _ = orc.chunk_loglik(np.random.default_rng(0).standard_normal((3, 6, 1)), np.zeros(6, int))
+    assert np.all(score == 0.0)
+    a = np.array([[[1.5, -0.25], [0.0, 2.0], [-3.0, 1.0]]])
+    score, rows = orc.chunk_loglik(a, np.array([0, 1, 0]))
+    want = [-math.log1p(math.exp(-(1.5 + 0.25))), -math.log1p(math.exp(-2.0)),
+            -math.log1p(math.exp(4.0))]
+    assert np.max(np.abs(rows[0] - want)) < 1e-12
+    shifted = a + np.array([[[10.0], [-7.0], [3.5]]])
+    assert np.max(np.abs(orc.chunk_loglik(shifted, np.array([0, 1, 0]))[1] - rows)) < 1e-12
+
+
 ALL_CHECKS = [
     check_chunk_attention, check_scores_vs_sdpa, check_scores_brute_force, check_scores_invariants,
     check_scores_single_row, check_top_b, check_select, check_split_equals_concat,
-    check_split_at_arbitrary_points,
+    check_split_at_arbitrary_points, check_loglik_vs_cross_entropy, check_loglik_closed_forms,
     check_decode_vs_sdpa, check_dense_equivalence, check_compact, check_cost_model,
 ]

@@ -117,6 +117,23 @@ def _lse_merge_drops_max(parts):
     return acc / big_l[..., None], m_all + np.log(big_l)
 
 
+def _loglik_no_max_shift(logits, labels):
+    # mistake: picks the label logit but normalises with the max only
+    z = np.asarray(logits, dtype=np.float64)
+    y = np.asarray(labels)
+    rows = np.take_along_axis(z, y[None, :, None].repeat(z.shape[0], 0), -1)[..., 0] - z.max(-1)
+    return rows.sum(1), rows
+
+
+def _loglik_wrong_label_axis(logits, labels):
+    # mistake: gathers the label along the row axis instead of the vocabulary
+    z = np.asarray(logits, dtype=np.float64)
+    lse = np.log(np.exp(z).sum(-1))
+    idx = np.minimum(np.asarray(labels), z.shape[1] - 1)
+    rows = z[:, idx, 0] - lse
+    return rows.sum(1), rows
+
+
 MUTANTS = {
     "cross_chunk_attention": (Mutant(chunk_attention=_chunk_attention_global), pins.check_chunk_attention),
     "gqa_mapping": (Mutant(chunk_attention=_chunk_attention_bad_gqa), pins.check_chunk_attention),
@@ -131,6 +148,10 @@ MUTANTS = {
                               pins.check_split_equals_concat),
     "merge_drops_split_max": (Mutant(lse_merge=_lse_merge_drops_max),
                               pins.check_split_at_arbitrary_points),
+    "loglik_normaliser_dropped": (Mutant(chunk_loglik=_loglik_no_max_shift),
+                                  pins.check_loglik_vs_cross_entropy),
+    "loglik_label_axis": (Mutant(chunk_loglik=_loglik_wrong_label_axis),
+                          pins.check_loglik_closed_forms),
 }
 
 
