@@ -142,6 +142,37 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
                              pfd_stream_t stream);
 
 /*
+ * pfd_chunk_prefill under the two other readings of the intra-chunk ranking
+ * (Methodology 2, "Two-Level Sparsity": tokens are ranked by the cumulative
+ * attention weight they receive from the query tokens).  Arguments as in
+ * pfd_chunk_prefill, plus:
+ *   per_kv_head  0: one ranking per chunk (scores [N, C+1], kept_idx [N, B]),
+ *                   as pfd_chunk_prefill;
+ *                1: one ranking per chunk and KV head: scores[j][g][t] sums
+ *                   the window probabilities over the query heads of KV head
+ *                   g only (scores [N, Hkv, C+1]), kept_idx [N, Hkv, B], and
+ *                   KV head g's column of chunk j's pool slot holds head g's
+ *                   BOS row and head g's kept rows (the slot and the table
+ *                   entry are as before, so decode reads such a pool
+ *                   unchanged).
+ *   k_win        NULL: a window row's softmax runs over the chunk's C+1 keys
+ *                   (as pfd_chunk_prefill);
+ *                [W, Hkv, D] bf16 device: the window rows' own keys join
+ *                   that softmax's denominator (the scores stay the
+ *                   probabilities of the chunk's keys, so they sum to less
+ *                   than W * Hq).  Requires W >= 1.
+ * workspace >= pfd_chunk_prefill_workspace(...) bytes, as for
+ * pfd_chunk_prefill.
+ */
+pfd_status pfd_chunk_prefill_ex(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
+                                const pfd_bf16* q_win, const pfd_bf16* k_win, int N, int C, int W,
+                                int Hq, int Hkv, int D, int B, float sm_scale, int per_kv_head,
+                                pfd_bf16* out, float* scores, int32_t* kept_idx, pfd_bf16* pool_k,
+                                pfd_bf16* pool_v, int64_t pool_rows, const int32_t* slot_row,
+                                pfd_chunk_entry* table, int32_t* dev_err, void* workspace,
+                                size_t workspace_bytes, pfd_stream_t stream);
+
+/*
  * Chunk scores from the model's logits (Methodology 1, predictive scoring:
  * s_I is the negative log-likelihood of the query window given the chunk,
  * s_P the likelihood of the pseudo-labels given the chunk and the query).

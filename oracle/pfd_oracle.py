@@ -155,6 +155,36 @@ def window_scores(q_win, k, n_chunks, chunk_size, sm_scale, counter=None):
     return scores
 
 
+def window_scores_alt(q_win, k, n_chunks, chunk_size, sm_scale, per_kv_head=False, k_win=None):
+    """[M2] under the two other readings of the ranking.
+
+    per_kv_head: the column sums run over the query heads of each KV head
+      separately (one token ranking per KV head); returns [N, Hkv, C+1].
+    k_win ([W, Hkv, D] or None): when given, each window row's softmax runs
+      over the chunk's C+1 keys and the W window keys together; the scores
+      are still the probabilities of the chunk's keys.
+    Otherwise as window_scores (whose result is the sum over KV heads of the
+    per-KV-head scores).
+    """
+    rows = chunk_size + 1
+    n_win, n_q_heads, head_dim = q_win.shape
+    n_kv = k.shape[1]
+    group = n_q_heads // n_kv
+    scores = np.zeros((n_chunks, n_kv, rows), dtype=np.float64)
+    if n_win == 0:
+        return scores if per_kv_head else scores.sum(axis=1)
+    for j in range(n_chunks):
+        lo, hi = j * rows, (j + 1) * rows
+        for h in range(n_q_heads):
+            g = h // group
+            keys = k[lo:hi, g, :]
+            if k_win is not None:
+                keys = np.concatenate([keys, k_win[:, g, :]], axis=0)
+            p = softmax_rows(sm_scale * (q_win[:, h, :] @ keys.T))
+            scores[j, g] += p[:, :rows].sum(axis=0)
+    return scores if per_kv_head else scores.sum(axis=1)
+
+
 def _rank_key(value, index):
     """R3: descending value, NaN last, ties to the lower index, -0 == +0."""
     value = float(value)
@@ -196,6 +226,30 @@ def compact(k, v, kept, slot_row, chunk_size, pool_k, pool_v):
         base = int(slot_row[j])
         pool_k[base:base + n_keep + 1] = k[src]
         pool_v[base:base + n_keep + 1] = v[src]
+        table[j] = (base, n_keep + 1)
+    return table
+
+
+def top_b_per_head(scores, n_keep):
+    """[M2] per-KV-head reading: top_b applied to every (chunk, KV head)
+    score row of scores [N, Hkv, C+1]; returns kept [N, Hkv, n_keep]."""
+    n_chunks, n_kv, rows = scores.shape
+    return top_b(scores.reshape(n_chunks * n_kv, rows), n_keep).reshape(n_chunks, n_kv, n_keep)
+
+
+def compact_per_head(k, v, kept, slot_row, chunk_size, pool_k, pool_v):
+    """[M1]/[M2] per-KV-head reading: KV head g of chunk j's slot holds, in
+    order, head g of the BOS row and of head g's kept rows (ascending).
+    kept: [N, Hkv, B].  Returns the chunk table as compact does."""
+    rows = chunk_size + 1
+    n_chunks, n_kv, n_keep = kept.shape
+    table = np.empty((n_chunks, 2), dtype=np.int32)
+    for j in range(n_chunks):
+        base = int(slot_row[j])
+        for g in range(n_kv):
+            src = [j * rows] + [j * rows + 1 + int(t) for t in kept[j, g]]
+            pool_k[base:base + n_keep + 1, g] = k[src, g]
+            pool_v[base:base + n_keep + 1, g] = v[src, g]
         table[j] = (base, n_keep + 1)
     return table
 

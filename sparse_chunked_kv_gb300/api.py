@@ -43,6 +43,39 @@ def chunk_prefill(q, k, v, q_win, n_chunks, chunk_size, n_keep, slot_row, pool_r
                 table=table, dev_err=dev_err, workspace=ws)
 
 
+def chunk_prefill_ex(q, k, v, q_win, k_win, n_chunks, chunk_size, n_keep, slot_row, pool_rows,
+                     per_kv_head=False, sm_scale=0.0, pool_k=None, pool_v=None, stream=None):
+    """pfd_chunk_prefill_ex: the prefill under the other ranking readings
+    (per_kv_head; window keys k_win in the denominator).  Returns the dict of
+    chunk_prefill, with scores [N, Hkv, C+1] and kept_idx [N, Hkv, B] per
+    KV head."""
+    _need_cuda(q, k, v, q_win, k_win, slot_row)
+    rows, hq, d = q.shape
+    hkv = k.shape[1]
+    w = q_win.shape[0]
+    dev = q.device
+    out = torch.empty_like(q)
+    if pool_k is None:
+        pool_k = torch.zeros(pool_rows, hkv, d, dtype=torch.bfloat16, device=dev)
+    if pool_v is None:
+        pool_v = torch.zeros(pool_rows, hkv, d, dtype=torch.bfloat16, device=dev)
+    per = hkv if per_kv_head else 1
+    scores = torch.empty(n_chunks * per, chunk_size + 1, dtype=torch.float32, device=dev)
+    kept = torch.empty(n_chunks * per, max(n_keep, 1), dtype=torch.int32, device=dev)
+    table = torch.empty(n_chunks, 2, dtype=torch.int32, device=dev)
+    dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_bytes = _abi.pfd_chunk_prefill_workspace(n_chunks, chunk_size, w, hq, hkv, d, n_keep)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _abi.pfd_chunk_prefill_ex(q, k, v, q_win, k_win, n_chunks, chunk_size, w, hq, hkv, d, n_keep,
+                              sm_scale, int(per_kv_head), out, scores, kept, pool_k, pool_v,
+                              pool_rows, slot_row, table, dev_err, ws, ws_bytes, stream)
+    if per_kv_head:
+        scores = scores.view(n_chunks, hkv, chunk_size + 1)
+        kept = kept.view(n_chunks, hkv, -1)
+    return dict(out=out, scores=scores, kept_idx=kept[..., :n_keep], pool_k=pool_k,
+                pool_v=pool_v, table=table, dev_err=dev_err, workspace=ws)
+
+
 def select_chunks(s_i, s_p, n_select, stream=None):
     """Top-K chunk selection (pfd_select_chunks).  Returns (sel, s)."""
     _need_cuda(s_i, s_p)

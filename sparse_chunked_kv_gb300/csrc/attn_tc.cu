@@ -891,10 +891,19 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         const int head = it.g * G + jj;
         if (it.kind == kWindow) {
           // The window-score kernel's per-column constant b = m + log2(l)
-          // (+inf when the row saw no key, so its probabilities are 0).
-          if (row_ok)
+          // (+inf when the row saw no key, so its probabilities are 0).  With
+          // the window keys in the denominator, their log2-sum-exp is added:
+          // b = log2(2^b + 2^b_self).
+          if (row_ok) {
+            float b = l_sum > 0.0f ? m_used + log2f(l_sum) : -INFINITY;
+            if (p.win_self_b != nullptr) {
+              const float bw = p.win_self_b[static_cast<long long>(t) * p.Hq + head];
+              const float hi = fmaxf(b, bw), lo = fminf(b, bw);
+              b = hi + log2f(1.0f + ex2_approx(lo - hi));
+            }
             p.win_b[(static_cast<long long>(it.chunk) * p.Hkv + it.g) * p.win_stride + t * G + jj] =
-                l_sum > 0.0f ? m_used + log2f(l_sum) : INFINITY;
+                b == -INFINITY ? INFINITY : b;
+          }
         } else {
           const long long tok = it.q_row0 + t;
           const bool final_out = it.kind == kChunk || p.n_splits == 1;

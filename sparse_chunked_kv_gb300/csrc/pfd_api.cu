@@ -118,12 +118,13 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct PrefillWs {
-  size_t win_b, part_scores, total;
+  size_t win_b, part_scores, win_self, total;
   int win_stride;
 };
 
-// Window statistics [N, Hkv, W*G rounded up to 32] and per-KV-group partial
-// scores [N, Hkv, C+1].
+// Window statistics [N, Hkv, W*G rounded up to 32], per-KV-group partial
+// scores [N, Hkv, C+1] and the window rows' statistics over the window's own
+// keys [W, Hq] (used when those keys are in the denominator).
 PrefillWs prefill_ws_layout(int N, int C, int W, int Hq, int Hkv) {
   PrefillWs w;
   w.win_stride = (W * (Hq / Hkv) + 31) & ~31;
@@ -131,7 +132,8 @@ PrefillWs prefill_ws_layout(int N, int C, int W, int Hq, int Hkv) {
   w.win_b = 0;
   w.part_scores = align256(stats);
   const size_t ps = W > 0 ? static_cast<size_t>(N) * Hkv * (C + 1) * sizeof(float) : 0;
-  w.total = w.part_scores + align256(ps);
+  w.win_self = w.part_scores + align256(ps);
+  w.total = w.win_self + align256(static_cast<size_t>(W) * Hq * sizeof(float));
   return w;
 }
 
@@ -165,6 +167,144 @@ bool decode_host_ok(int batch, const int32_t* cu_lq_host, const int32_t* cu_k_ho
 }
 
 constexpr int kMaxSplits = 64;
+
+// Chunked prefill of one request (pfd_chunk_prefill, pfd_chunk_prefill_ex):
+// per_kv_head ranks per (chunk, KV head); k_win (may be null) puts the
+// window keys into the window rows' softmax denominator.
+pfd_status prefill_impl(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
+                        const pfd_bf16* q_win, int N, int C, int W, int Hq, int Hkv, int D, int B,
+                        float sm_scale, pfd_bf16* out, float* scores, int32_t* kept_idx,
+                        pfd_bf16* pool_k, pfd_bf16* pool_v, int64_t pool_rows,
+                        const int32_t* slot_row, pfd_chunk_entry* table, int32_t* dev_err,
+                        void* workspace, size_t workspace_bytes, bool per_kv_head,
+                        const pfd_bf16* k_win, pfd_stream_t stream) {
+  if (N < 1 || C < 1 || W < 0 || B < 0 || B > C) return PFD_ERR_INVALID_ARG;
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return PFD_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return PFD_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  if (C > 8192 || G > kBlockM || W > 256 || static_cast<long long>(W) * G > 512)
+    return PFD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(N) * (C + 1) * Hq * D >= (1ll << 40)) return PFD_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !out || !scores || !pool_k || !pool_v || !slot_row || !table)
+    return PFD_ERR_INVALID_ARG;
+  if (B > 0 && !kept_idx) return PFD_ERR_INVALID_ARG;
+  if (W > 0 && !q_win) return PFD_ERR_INVALID_ARG;
+  if (k_win != nullptr && (W == 0 || !aligned16(k_win))) return PFD_ERR_INVALID_ARG;
+  if (pool_rows < B + 1 || pool_rows >= (1ll << 31)) return PFD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(pool_k) ||
+      !aligned16(pool_v) || (W > 0 && !aligned16(q_win)))
+    return PFD_ERR_INVALID_ARG;
+  const PrefillWs ws = prefill_ws_layout(N, C, W, Hq, Hkv);
+  if (workspace_bytes < ws.total || (ws.total > 0 && workspace == nullptr) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return PFD_ERR_INVALID_ARG;
+  const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  const long long rows = static_cast<long long>(N) * (C + 1);
+
+  const int Tq = kBlockM / G;
+  AttnParams ap;
+  std::memset(&ap, 0, sizeof(ap));
+  if (!make_kv_maps(ap.tm_k, 0, k, rows, Hkv, D) || !make_kv_maps(ap.tm_v, 0, v, rows, Hkv, D) ||
+      !make_map(&ap.tm_q[0], q, rows, Hq, D, G, Tq))
+    return PFD_ERR_CUDA;
+  copy_kv_maps(ap.tm_k, 1, 0);
+  copy_kv_maps(ap.tm_v, 1, 0);
+  if (W > 0) {
+    if (!make_map(&ap.tm_q[1], q_win, W, Hq, D, G, Tq)) return PFD_ERR_CUDA;
+  } else {
+    ap.tm_q[1] = ap.tm_q[0];
+  }
+  ap.Tq = Tq;
+  ap.q = reinterpret_cast<const bf16*>(q);
+  ap.q_win = reinterpret_cast<const bf16*>(q_win);
+  ap.out = reinterpret_cast<bf16*>(out);
+  ap.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+  ap.win_b = reinterpret_cast<float*>(wsb + ws.win_b);
+  ap.win_stride = ws.win_stride;
+  ap.dev_err = dev_err;
+  ap.mode = kModePrefill;
+  ap.Hq = Hq;
+  ap.Hkv = Hkv;
+  ap.G = G;
+  ap.D = D;
+  ap.n_chunks = N;
+  ap.chunk_rows = C + 1;
+  ap.n_win = W;
+  ap.mt_chunk = ceil_div(C + 1, Tq);
+  ap.mt_win = W > 0 ? ceil_div(W, Tq) : 0;
+  ap.n_chunk_items = N * Hkv * ceil_div(ap.mt_chunk, 2);
+  ap.n_splits = 1;
+  ap.scale_log2 = scale * kLog2e;
+  const long long items =
+      static_cast<long long>(ap.n_chunk_items) + static_cast<long long>(N) * Hkv * ceil_div(ap.mt_win, 2);
+  if (items >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
+  ap.n_items = static_cast<int>(items);
+  // Every tensor map is encoded before the first launch, so that a failure
+  // to encode one launches nothing.
+  WinScoreParams wp;
+  std::memset(&wp, 0, sizeof(wp));
+  wp.k_tiles = ceil_div(C + 1, 128);
+  wp.concat = (C + 1 >= 128) ? 1 : 0;
+  const long long ws_items =
+      wp.concat ? (rows + 127) / 128 : static_cast<long long>(N) * wp.k_tiles;
+  if (ws_items >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
+  if (W > 0 && !make_map(&wp.tm_qwin, q_win, W, Hq, D, G, W)) return PFD_ERR_CUDA;
+  const int grid = static_cast<int>(std::min<long long>(items, device_sm_count()));
+  pfd_status s = PFD_OK;
+  if (k_win != nullptr) {
+    ap.win_self_b = reinterpret_cast<float*>(wsb + ws.win_self);
+    s = from_cuda(launch_window_self_stats(reinterpret_cast<const bf16*>(q_win),
+                                           reinterpret_cast<const bf16*>(k_win), W, Hq, Hkv, D,
+                                           ap.scale_log2, reinterpret_cast<float*>(wsb + ws.win_self),
+                                           st));
+    if (s != PFD_OK) return s;
+  }
+  s = from_cuda(launch_attention(ap, grid, st));
+  if (s != PFD_OK) return s;
+
+  if (W > 0) {
+    wp.tm_k = ap.tm_k[kBoxLevels - 1][0];
+    wp.q_win = ap.q_win;
+    wp.win_b = ap.win_b;
+    wp.win_stride = ap.win_stride;
+    wp.part_scores = reinterpret_cast<float*>(wsb + ws.part_scores);
+    wp.n_chunks = N;
+    wp.chunk_rows = C + 1;
+    wp.n_win = W;
+    wp.Hq = Hq;
+    wp.Hkv = Hkv;
+    wp.G = G;
+    wp.D = D;
+    wp.n_items = static_cast<int>(ws_items);
+    wp.scale_log2 = ap.scale_log2;
+    wp.dev_err = dev_err;
+    s = from_cuda(launch_window_scores(wp, st));
+    if (s != PFD_OK) return s;
+  }
+
+  TopBParams tp;
+  std::memset(&tp, 0, sizeof(tp));
+  tp.part_scores = W > 0 ? reinterpret_cast<const float*>(wsb + ws.part_scores) : nullptr;
+  tp.scores = scores;
+  tp.kept_idx = kept_idx;
+  tp.k = reinterpret_cast<const bf16*>(k);
+  tp.v = reinterpret_cast<const bf16*>(v);
+  tp.pool_k = reinterpret_cast<bf16*>(pool_k);
+  tp.pool_v = reinterpret_cast<bf16*>(pool_v);
+  tp.slot_row = slot_row;
+  tp.table = table;
+  tp.dev_err = dev_err;
+  tp.pool_rows = pool_rows;
+  tp.n_chunks = N;
+  tp.chunk_size = C;
+  tp.n_keep = B;
+  tp.Hkv = Hkv;
+  tp.D = D;
+  tp.per_head = per_kv_head ? 1 : 0;
+  return from_cuda(launch_topb_compact(tp, st));   // sets the copy splits
+}
 
 int plan_splits(int batch, const int32_t* cu_lq_host, const int32_t* cu_k_host, int Hq,
                 int Hkv, int D, int max_chunk_len, bool self_keys) {
@@ -335,121 +475,22 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
                              int64_t pool_rows, const int32_t* slot_row, pfd_chunk_entry* table,
                              int32_t* dev_err, void* workspace, size_t workspace_bytes,
                              pfd_stream_t stream) {
-  if (N < 1 || C < 1 || W < 0 || B < 0 || B > C) return PFD_ERR_INVALID_ARG;
-  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return PFD_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return PFD_ERR_UNSUPPORTED;
-  const int G = Hq / Hkv;
-  if (C > 8192 || G > kBlockM || W > 256 || static_cast<long long>(W) * G > 512)
-    return PFD_ERR_UNSUPPORTED;
-  if (static_cast<long long>(N) * (C + 1) * Hq * D >= (1ll << 40)) return PFD_ERR_UNSUPPORTED;
-  if (!q || !k || !v || !out || !scores || !pool_k || !pool_v || !slot_row || !table)
-    return PFD_ERR_INVALID_ARG;
-  if (B > 0 && !kept_idx) return PFD_ERR_INVALID_ARG;
-  if (W > 0 && !q_win) return PFD_ERR_INVALID_ARG;
-  if (pool_rows < B + 1 || pool_rows >= (1ll << 31)) return PFD_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(pool_k) ||
-      !aligned16(pool_v) || (W > 0 && !aligned16(q_win)))
-    return PFD_ERR_INVALID_ARG;
-  const PrefillWs ws = prefill_ws_layout(N, C, W, Hq, Hkv);
-  if (workspace_bytes < ws.total || (ws.total > 0 && workspace == nullptr) ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return PFD_ERR_INVALID_ARG;
-  const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* wsb = static_cast<uint8_t*>(workspace);
-  const long long rows = static_cast<long long>(N) * (C + 1);
+  return prefill_impl(q, k, v, q_win, N, C, W, Hq, Hkv, D, B, sm_scale, out, scores, kept_idx,
+                      pool_k, pool_v, pool_rows, slot_row, table, dev_err, workspace,
+                      workspace_bytes, false, nullptr, stream);
+}
 
-  const int Tq = kBlockM / G;
-  AttnParams ap;
-  std::memset(&ap, 0, sizeof(ap));
-  if (!make_kv_maps(ap.tm_k, 0, k, rows, Hkv, D) || !make_kv_maps(ap.tm_v, 0, v, rows, Hkv, D) ||
-      !make_map(&ap.tm_q[0], q, rows, Hq, D, G, Tq))
-    return PFD_ERR_CUDA;
-  copy_kv_maps(ap.tm_k, 1, 0);
-  copy_kv_maps(ap.tm_v, 1, 0);
-  if (W > 0) {
-    if (!make_map(&ap.tm_q[1], q_win, W, Hq, D, G, Tq)) return PFD_ERR_CUDA;
-  } else {
-    ap.tm_q[1] = ap.tm_q[0];
-  }
-  ap.Tq = Tq;
-  ap.q = reinterpret_cast<const bf16*>(q);
-  ap.q_win = reinterpret_cast<const bf16*>(q_win);
-  ap.out = reinterpret_cast<bf16*>(out);
-  ap.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
-  ap.win_b = reinterpret_cast<float*>(wsb + ws.win_b);
-  ap.win_stride = ws.win_stride;
-  ap.dev_err = dev_err;
-  ap.mode = kModePrefill;
-  ap.Hq = Hq;
-  ap.Hkv = Hkv;
-  ap.G = G;
-  ap.D = D;
-  ap.n_chunks = N;
-  ap.chunk_rows = C + 1;
-  ap.n_win = W;
-  ap.mt_chunk = ceil_div(C + 1, Tq);
-  ap.mt_win = W > 0 ? ceil_div(W, Tq) : 0;
-  ap.n_chunk_items = N * Hkv * ceil_div(ap.mt_chunk, 2);
-  ap.n_splits = 1;
-  ap.scale_log2 = scale * kLog2e;
-  const long long items =
-      static_cast<long long>(ap.n_chunk_items) + static_cast<long long>(N) * Hkv * ceil_div(ap.mt_win, 2);
-  if (items >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
-  ap.n_items = static_cast<int>(items);
-  // Every tensor map is encoded before the first launch, so that a failure
-  // to encode one launches nothing.
-  WinScoreParams wp;
-  std::memset(&wp, 0, sizeof(wp));
-  wp.k_tiles = ceil_div(C + 1, 128);
-  wp.concat = (C + 1 >= 128) ? 1 : 0;
-  const long long ws_items =
-      wp.concat ? (rows + 127) / 128 : static_cast<long long>(N) * wp.k_tiles;
-  if (ws_items >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
-  if (W > 0 && !make_map(&wp.tm_qwin, q_win, W, Hq, D, G, W)) return PFD_ERR_CUDA;
-  const int grid = static_cast<int>(std::min<long long>(items, device_sm_count()));
-  pfd_status s = from_cuda(launch_attention(ap, grid, st));
-  if (s != PFD_OK) return s;
-
-  if (W > 0) {
-    wp.tm_k = ap.tm_k[kBoxLevels - 1][0];
-    wp.q_win = ap.q_win;
-    wp.win_b = ap.win_b;
-    wp.win_stride = ap.win_stride;
-    wp.part_scores = reinterpret_cast<float*>(wsb + ws.part_scores);
-    wp.n_chunks = N;
-    wp.chunk_rows = C + 1;
-    wp.n_win = W;
-    wp.Hq = Hq;
-    wp.Hkv = Hkv;
-    wp.G = G;
-    wp.D = D;
-    wp.n_items = static_cast<int>(ws_items);
-    wp.scale_log2 = ap.scale_log2;
-    wp.dev_err = dev_err;
-    s = from_cuda(launch_window_scores(wp, st));
-    if (s != PFD_OK) return s;
-  }
-
-  TopBParams tp;
-  std::memset(&tp, 0, sizeof(tp));
-  tp.part_scores = W > 0 ? reinterpret_cast<const float*>(wsb + ws.part_scores) : nullptr;
-  tp.scores = scores;
-  tp.kept_idx = kept_idx;
-  tp.k = reinterpret_cast<const bf16*>(k);
-  tp.v = reinterpret_cast<const bf16*>(v);
-  tp.pool_k = reinterpret_cast<bf16*>(pool_k);
-  tp.pool_v = reinterpret_cast<bf16*>(pool_v);
-  tp.slot_row = slot_row;
-  tp.table = table;
-  tp.dev_err = dev_err;
-  tp.pool_rows = pool_rows;
-  tp.n_chunks = N;
-  tp.chunk_size = C;
-  tp.n_keep = B;
-  tp.Hkv = Hkv;
-  tp.D = D;
-  return from_cuda(launch_topb_compact(tp, st));   // sets the copy splits
+pfd_status pfd_chunk_prefill_ex(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
+                                const pfd_bf16* q_win, const pfd_bf16* k_win, int N, int C, int W,
+                                int Hq, int Hkv, int D, int B, float sm_scale, int per_kv_head,
+                                pfd_bf16* out, float* scores, int32_t* kept_idx, pfd_bf16* pool_k,
+                                pfd_bf16* pool_v, int64_t pool_rows, const int32_t* slot_row,
+                                pfd_chunk_entry* table, int32_t* dev_err, void* workspace,
+                                size_t workspace_bytes, pfd_stream_t stream) {
+  if (per_kv_head != 0 && per_kv_head != 1) return PFD_ERR_INVALID_ARG;
+  return prefill_impl(q, k, v, q_win, N, C, W, Hq, Hkv, D, B, sm_scale, out, scores, kept_idx,
+                      pool_k, pool_v, pool_rows, slot_row, table, dev_err, workspace,
+                      workspace_bytes, per_kv_head != 0, k_win, stream);
 }
 
 pfd_status pfd_chunk_loglik(const pfd_bf16* logits, const int32_t* labels, int N, int R,

@@ -56,6 +56,9 @@ struct AttnParams {
   float* win_b;         // prefill: [N, Hkv, win_stride] per window row n = w*G + j of
                         // each KV group: m + log2(l) of its softmax over the chunk
   int win_stride;       // (W*G rounded up to 32)
+  const float* win_self_b;  // prefill, window keys in the denominator: [W, Hq]
+                            // log2-sum-exp of each window row over the W window
+                            // keys, folded into win_b (null: chunk keys only)
 
   const pfd_chunk_entry* table;
   const int32_t* sel;
@@ -104,12 +107,14 @@ struct WinScoreParams {
 };
 
 cudaError_t launch_window_scores(const WinScoreParams& p, cudaStream_t stream);
+cudaError_t launch_window_self_stats(const bf16* q_win, const bf16* k_win, int W, int Hq, int Hkv,
+                                     int D, float scale_log2, float* b_self, cudaStream_t stream);
 
 // ------------------------------------------------- top-B + compaction --
 struct TopBParams {
   const float* part_scores;  // [N, Hkv, C+1] or null when W == 0
-  float* scores;             // [N, C+1]
-  int32_t* kept_idx;         // [N, B]
+  float* scores;             // [N, C+1] ([N, Hkv, C+1] per head)
+  int32_t* kept_idx;         // [N, B] ([N, Hkv, B] per head)
   const bf16* k;             // [N*(C+1), Hkv, D]
   const bf16* v;
   bf16* pool_k;              // [pool_rows, Hkv, D]
@@ -120,6 +125,8 @@ struct TopBParams {
   long long pool_rows;
   int n_chunks, chunk_size, n_keep, Hkv, D;
   int copy_splits;
+  int per_head;              // 1: one ranking per (chunk, KV head): scores [N, Hkv, C+1],
+                             // kept_idx [N, Hkv, B], head g's slot column from head g's set
 };
 
 cudaError_t launch_topb_compact(const TopBParams& p, cudaStream_t stream);

@@ -53,12 +53,13 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int& 
 
 // 4. Chunk table and the copy of BOS + kept rows (kept_src, slot order) into
 // chunk j's pool slot; CTA `part` of copy_splits copies its share of the rows.
-__device__ __forceinline__ void copy_kept_rows(const TopBParams& p, int j, int part, int rows,
-                                               const int* kept_src, int tid) {
+// Per-head ranking (head >= 0): only KV head `head`'s columns of the rows.
+__device__ __forceinline__ void copy_kept_rows(const TopBParams& p, int j, int head, int part,
+                                               int rows, const int* kept_src, int tid) {
   const int B = p.n_keep;
   const long long slot = p.slot_row[j];
   const bool slot_ok = slot >= 0 && slot + B + 1 <= p.pool_rows;
-  if (part == 0 && tid == 0) {
+  if (part == 0 && tid == 0 && head <= 0) {
     pfd_chunk_entry e;
     e.row = slot_ok ? static_cast<int32_t>(slot) : 0;
     e.len = slot_ok ? B + 1 : 0;
@@ -69,12 +70,14 @@ __device__ __forceinline__ void copy_kept_rows(const TopBParams& p, int j, int p
   const int n_rows_out = B + 1;
   const int r0 = static_cast<int>(static_cast<long long>(n_rows_out) * part / p.copy_splits);
   const int r1 = static_cast<int>(static_cast<long long>(n_rows_out) * (part + 1) / p.copy_splits);
-  const int units = p.Hkv * p.D / 8;  // 16-byte units per token row
+  const int row_units = p.Hkv * p.D / 8;              // 16-byte units per token row
+  const int units = head < 0 ? row_units : p.D / 8;   // units copied per row
+  const int u0 = head < 0 ? 0 : head * (p.D / 8);     // first unit copied
   const long long chunk_row0 = static_cast<long long>(j) * rows;
   for (int idx = tid; idx < (r1 - r0) * units; idx += kTopBThreads) {
-    const int r = r0 + idx / units, u = idx % units;
-    const long long src = (chunk_row0 + kept_src[r]) * units + u;
-    const long long dst = (slot + r) * units + u;
+    const int r = r0 + idx / units, u = u0 + idx % units;
+    const long long src = (chunk_row0 + kept_src[r]) * row_units + u;
+    const long long dst = (slot + r) * row_units + u;
     reinterpret_cast<uint4*>(p.pool_k)[dst] = __ldg(reinterpret_cast<const uint4*>(p.k) + src);
     reinterpret_cast<uint4*>(p.pool_v)[dst] = __ldg(reinterpret_cast<const uint4*>(p.v) + src);
   }
@@ -92,20 +95,29 @@ topb_compact_kernel(const TopBParams p) {
   grid_dependency_wait();
   grid_dependents_launch();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int j = blockIdx.x;
+  // Ranking unit: chunk j, or (chunk j, KV head g) with per-head ranking.
+  const int vj = blockIdx.x;
+  const int j = p.per_head ? vj / p.Hkv : vj;
+  const int head = p.per_head ? vj % p.Hkv : -1;
   const int part = blockIdx.y;
   const int C = p.chunk_size, rows = C + 1, B = p.n_keep;
   float* sc = reinterpret_cast<float*>(smem_raw);                   // [rows]
   int* kept_src = reinterpret_cast<int*>(smem_raw + ((rows * 4 + 15) & ~15));  // [B+1]
 
-  // 1. Scores: fixed-order sum of the Hkv partial column sums.
+  // 1. Scores: fixed-order sum of the Hkv partial column sums (per-head
+  // ranking: that head's partial alone).
   for (int t = tid; t < rows; t += kTopBThreads) {
     float s = 0.0f;
-    if (p.part_scores != nullptr)
-      for (int g = 0; g < p.Hkv; ++g)
-        s += p.part_scores[(static_cast<long long>(j) * p.Hkv + g) * rows + t];
+    if (p.part_scores != nullptr) {
+      if (head >= 0) {
+        s = p.part_scores[static_cast<long long>(vj) * rows + t];
+      } else {
+        for (int g = 0; g < p.Hkv; ++g)
+          s += p.part_scores[(static_cast<long long>(j) * p.Hkv + g) * rows + t];
+      }
+    }
     sc[t] = s;
-    if (part == 0) p.scores[static_cast<long long>(j) * rows + t] = s;
+    if (part == 0) p.scores[static_cast<long long>(vj) * rows + t] = s;
   }
   if (tid == 0) kept_src[0] = 0;  // BOS is slot row 0
   __syncthreads();
@@ -204,13 +216,13 @@ topb_compact_kernel(const TopBParams p) {
   for (int u = 0; u < kMaxPerThread; ++u) {
     if (kept_mask & (1u << u)) {
       kept_src[1 + pos] = 1 + i0 + u;
-      if (part == 0) p.kept_idx[static_cast<long long>(j) * B + pos] = i0 + u;
+      if (part == 0) p.kept_idx[static_cast<long long>(vj) * B + pos] = i0 + u;
       ++pos;
     }
   }
   __syncthreads();
 
-  copy_kept_rows(p, j, part, rows, kept_src, tid);
+  copy_kept_rows(p, j, head, part, rows, kept_src, tid);
 }
 
 constexpr int kSelectThreads = 1024;
@@ -273,8 +285,9 @@ cudaError_t launch_topb_compact(const TopBParams& params, cudaStream_t stream) {
                                                     smem) != cudaSuccess || per_sm < 1)
     per_sm = 1;
   const int wave = std::max(sm_count, 1) * per_sm;
-  p.copy_splits = std::max(1, std::min(wave / std::max(p.n_chunks, 1), std::max(1, (p.n_keep + 1) / 16)));
-  dim3 grid(p.n_chunks, p.copy_splits);
+  const int units = p.n_chunks * (p.per_head ? p.Hkv : 1);   // rankings
+  p.copy_splits = std::max(1, std::min(wave / std::max(units, 1), std::max(1, (p.n_keep + 1) / 16)));
+  dim3 grid(units, p.copy_splits);
   return launch_pdl(topb_compact_kernel, grid, dim3(kTopBThreads), smem, stream, p);
 }
 

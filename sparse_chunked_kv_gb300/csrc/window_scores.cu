@@ -290,4 +290,54 @@ cudaError_t launch_window_scores(const WinScoreParams& p, cudaStream_t stream) {
   return launch_pdl(window_score_kernel<128>, dim3(grid), dim3(kThreads), smem, stream, p);
 }
 
+// Each window row's log-sum-exp over the window's own W keys, for the reading
+// of "Two-Level Sparsity" in which a window row's softmax runs over the
+// chunk's keys and the window keys together:
+//   b_self[w][h] = log2 sum_{w'} 2^(x_{w'}),  x = sm_scale log2(e) q_{w,h} . k_win_{w',g}.
+// One warp per (w, h): lanes split D, the dot product is a warp sum, the
+// running (max, sum) is kept identically by every lane.  W <= 256 keys of
+// D <= 128: a few microseconds at most, once per prefill call.
+__global__ void __launch_bounds__(128)
+window_self_stats_kernel(const bf16* __restrict__ q_win, const bf16* __restrict__ k_win, int W,
+                         int Hq, int Hkv, int D, float scale_log2, float* __restrict__ b_self) {
+  grid_dependency_wait();
+  const int lane = threadIdx.x & 31;
+  const long long pair = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (pair >= static_cast<long long>(W) * Hq) return;
+  const int w = static_cast<int>(pair / Hq), h = static_cast<int>(pair % Hq);
+  const int g = h / (Hq / Hkv);
+  const uint16_t* q = reinterpret_cast<const uint16_t*>(q_win) + (static_cast<long long>(w) * Hq + h) * D;
+  float qv[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    qv[i] = lane + 32 * i < D ? __uint_as_float(static_cast<uint32_t>(q[lane + 32 * i]) << 16) : 0.0f;
+  float m = -INFINITY, l = 0.0f;
+  for (int k2 = 0; k2 < W; ++k2) {
+    const uint16_t* k = reinterpret_cast<const uint16_t*>(k_win) + (static_cast<long long>(k2) * Hkv + g) * D;
+    float dot = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (lane + 32 * i < D)
+        dot = fmaf(qv[i], __uint_as_float(static_cast<uint32_t>(k[lane + 32 * i]) << 16), dot);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
+    const float x = dot * scale_log2;
+    if (x > m) {
+      l = m == -INFINITY ? 0.0f : l * ex2_approx(m - x);
+      m = x;
+    }
+    l += ex2_approx(x - m);
+  }
+  if (lane == 0) b_self[pair] = m + log2f(l);
+  grid_dependents_launch();
+}
+
+cudaError_t launch_window_self_stats(const bf16* q_win, const bf16* k_win, int W, int Hq, int Hkv,
+                                     int D, float scale_log2, float* b_self, cudaStream_t stream) {
+  const long long pairs = static_cast<long long>(W) * Hq;
+  if (pairs <= 0) return cudaSuccess;
+  return launch_pdl(window_self_stats_kernel, dim3(static_cast<unsigned>((pairs + 3) / 4)),
+                    dim3(128), 0, stream, q_win, k_win, W, Hq, Hkv, D, scale_log2, b_self);
+}
+
 }  // namespace pfd

@@ -342,6 +342,68 @@ def check_cost_model(orc):
     assert macs[0] == macs[1], "decode cost must not depend on N"
 
 
+# ------------------------------------------------- alternative rankings --
+
+def check_scores_alt_readings(orc, seed=16):
+    """Per-KV-head scores: column sums of SDPA-with-identity probabilities
+    over each KV head's query heads; summed over KV heads they are the
+    shared scores.  Window keys in the denominator: the chunk columns of the
+    probability matrix over [chunk keys ; window keys] (SDPA with V =
+    identity over the concatenation); the scores then sum to less than
+    W * Hq by exactly the mass on the window keys."""
+    gen = torch.Generator().manual_seed(seed)
+    n, c, w, hq, hkv, d = 3, 5, 4, 6, 2, 8
+    rows = n * (c + 1)
+    k = rand(gen, rows, hkv, d)
+    q_win = rand(gen, w, hq, d)
+    k_win = rand(gen, w, hkv, d)
+    scale = 0.4
+    per = orc.window_scores_alt(q_win, k, n, c, scale, per_kv_head=True)
+    shared = orc.window_scores(q_win, k, n, c, scale)
+    assert np.max(np.abs(per.sum(axis=1) - shared)) < 1e-12
+    with_w = orc.window_scores_alt(q_win, k, n, c, scale, k_win=k_win)
+    with_w_per = orc.window_scores_alt(q_win, k, n, c, scale, per_kv_head=True, k_win=k_win)
+    assert np.max(np.abs(with_w_per.sum(axis=1) - with_w)) < 1e-12
+    for j in range(n):
+        lo = j * (c + 1)
+        window_mass = 0.0
+        for h in range(hq):
+            g = h // (hq // hkv)
+            keys = np.concatenate([k[lo:lo + c + 1, g], k_win[:, g]], axis=0)
+            eye = np.eye(keys.shape[0])
+            pm = sdpa(q_win[:, h], keys, eye, None, scale)       # [W, C+1+W] probabilities
+            window_mass += pm[:, c + 1:].sum()
+            want_g = np.zeros(c + 1)
+            for h2 in range(g * (hq // hkv), (g + 1) * (hq // hkv)):
+                want_g += sdpa(q_win[:, h2], keys, eye, None, scale)[:, :c + 1].sum(axis=0)
+            assert np.max(np.abs(with_w_per[j, g] - want_g)) < 1e-12
+        assert abs(with_w[j].sum() - (w * hq - window_mass)) < 1e-10
+
+
+def check_per_head_topb_and_compact(orc, seed=17):
+    """Per-KV-head top-B equals top_b on each head's row; each head's
+    column of a slot holds BOS and that head's kept rows only."""
+    gen = torch.Generator().manual_seed(seed)
+    n, c, hkv, d, b = 3, 9, 2, 4, 3
+    scores = rand(gen, n, hkv, c + 1)
+    kept = orc.top_b_per_head(scores, b)
+    for j in range(n):
+        for g in range(hkv):
+            assert kept[j, g].tolist() == sorted(ranked_by_counting(
+                [float(np.float32(x)) for x in scores[j, g, 1:]], b))
+    rows = n * (c + 1)
+    k, v = rand(gen, rows, hkv, d), rand(gen, rows, hkv, d)
+    slot = np.array([8, 0, 4], dtype=np.int32)
+    pk, pv = np.full((12, hkv, d), np.nan), np.full((12, hkv, d), np.nan)
+    table = orc.compact_per_head(k, v, kept, slot, c, pk, pv)
+    assert table.tolist() == [[8, 4], [0, 4], [4, 4]]
+    for j in range(n):
+        for g in range(hkv):
+            src = [j * (c + 1)] + [j * (c + 1) + 1 + int(t) for t in kept[j, g]]
+            assert np.array_equal(pk[slot[j]:slot[j] + b + 1, g], k[src, g])
+            assert np.array_equal(pv[slot[j]:slot[j] + b + 1, g], v[src, g])
+
+
 # ----------------------------------------------------------- chunk scores --
 
 def check_loglik_vs_cross_entropy(orc, seed=15):
@@ -380,5 +442,6 @@ ALL_CHECKS = [
     check_chunk_attention, check_scores_vs_sdpa, check_scores_brute_force, check_scores_invariants,
     check_scores_single_row, check_top_b, check_select, check_split_equals_concat,
     check_split_at_arbitrary_points, check_loglik_vs_cross_entropy, check_loglik_closed_forms,
+    check_scores_alt_readings, check_per_head_topb_and_compact,
     check_decode_vs_sdpa, check_dense_equivalence, check_compact, check_cost_model,
 ]

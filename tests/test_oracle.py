@@ -134,6 +134,17 @@ def _loglik_wrong_label_axis(logits, labels):
     return rows.sum(1), rows
 
 
+def _scores_alt_window_keys_ignored(q_win, k, n, c, scale, per_kv_head=False, k_win=None):
+    # mistake: drops the window keys from the denominator
+    return orc.window_scores_alt(q_win, k, n, c, scale, per_kv_head=per_kv_head, k_win=None)
+
+
+def _compact_per_head_shared_rows(k, v, kept, slot_row, c, pk, pv):
+    # mistake: copies every head's rows from KV head 0's kept set
+    return orc.compact_per_head(k, v, np.repeat(kept[:, :1], kept.shape[1], axis=1), slot_row, c,
+                                pk, pv)
+
+
 MUTANTS = {
     "cross_chunk_attention": (Mutant(chunk_attention=_chunk_attention_global), pins.check_chunk_attention),
     "gqa_mapping": (Mutant(chunk_attention=_chunk_attention_bad_gqa), pins.check_chunk_attention),
@@ -152,6 +163,10 @@ MUTANTS = {
                                   pins.check_loglik_vs_cross_entropy),
     "loglik_label_axis": (Mutant(chunk_loglik=_loglik_wrong_label_axis),
                           pins.check_loglik_closed_forms),
+    "scores_window_keys_dropped": (Mutant(window_scores_alt=_scores_alt_window_keys_ignored),
+                                   pins.check_scores_alt_readings),
+    "per_head_compact_shared_rows": (Mutant(compact_per_head=_compact_per_head_shared_rows),
+                                     pins.check_per_head_topb_and_compact),
 }
 
 
