@@ -142,6 +142,34 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
                              pfd_stream_t stream);
 
 /*
+ * The prefill of L layers of one request in one call (Methodology 1,
+ * "Chunked Prefill and KV Caching": every layer caches the KV of its chunks;
+ * one pool per layer).  Layer l is exactly pfd_chunk_prefill over layer l's
+ * tensors into layer l's pool; the layers run together, so each kernel
+ * (chunk attention with the window statistics, window scores, top-B with
+ * compaction) is launched once for all layers.
+ *   q [L, N*(C+1), Hq, D], k, v [L, N*(C+1), Hkv, D] bf16 (layers stacked)
+ *   q_win [L, W, Hq, D] bf16 (each layer's query-window rows)
+ *   out [L, N*(C+1), Hq, D]; scores [L, N, C+1]; kept_idx [L, N, B]
+ *   pool_k, pool_v [L, pool_rows, Hkv, D]: layer l's pool is rows
+ *       l*pool_rows .. of the stacked buffers
+ *   slot_row [N]: the slot of chunk j in every layer's pool
+ *   table [L, N]: layer l's table (rows relative to layer l's pool)
+ *   workspace >= pfd_chunk_prefill_layers_workspace(...) bytes
+ * Limits as for pfd_chunk_prefill, with L * N * (C+1) < 2^31 rows.
+ */
+size_t pfd_chunk_prefill_layers_workspace(int L, int N, int C, int W, int Hq, int Hkv, int D,
+                                          int B);
+
+pfd_status pfd_chunk_prefill_layers(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
+                                    const pfd_bf16* q_win, int L, int N, int C, int W, int Hq,
+                                    int Hkv, int D, int B, float sm_scale, pfd_bf16* out,
+                                    float* scores, int32_t* kept_idx, pfd_bf16* pool_k,
+                                    pfd_bf16* pool_v, int64_t pool_rows, const int32_t* slot_row,
+                                    pfd_chunk_entry* table, int32_t* dev_err, void* workspace,
+                                    size_t workspace_bytes, pfd_stream_t stream);
+
+/*
  * pfd_chunk_prefill under the two other readings of the intra-chunk ranking
  * (Methodology 2, "Two-Level Sparsity": tokens are ranked by the cumulative
  * attention weight they receive from the query tokens).  Arguments as in

@@ -254,6 +254,29 @@ def compact_per_head(k, v, kept, slot_row, chunk_size, pool_k, pool_v):
     return table
 
 
+def chunk_prefill_layers(q, k, v, q_win, n_chunks, chunk_size, n_keep, slot_row, pool_rows,
+                         sm_scale):
+    """[M1] over L layers: every layer caches the KV of its own chunks, so
+    layer l is the single-layer prefill (chunk_attention, window_scores,
+    top_b, compact) of its own tensors into its own pool.
+
+    q, k, v: [L, N*(C+1), H, D]; q_win [L, W, Hq, D]; slot_row [N] (the same
+    slots in every layer's pool of pool_rows rows).  Returns a list, one dict
+    per layer, with out, scores, kept, pool_k, pool_v and table.
+    """
+    layers = []
+    for l in range(q.shape[0]):
+        out = chunk_attention(q[l], k[l], v[l], n_chunks, chunk_size, sm_scale)
+        scores = window_scores(q_win[l], k[l], n_chunks, chunk_size, sm_scale)
+        kept = top_b(scores, n_keep)
+        pool_k = np.zeros((pool_rows,) + k.shape[2:])
+        pool_v = np.zeros((pool_rows,) + v.shape[2:])
+        table = compact(k[l], v[l], kept, slot_row, chunk_size, pool_k, pool_v)
+        layers.append(dict(out=out, scores=scores, kept=kept, pool_k=pool_k, pool_v=pool_v,
+                           table=table))
+    return layers
+
+
 def select_chunks(s_i, s_p, n_select):
     """[M1] + R3: the n_select chunks with the largest s = fl32(s_I + s_P).
 

@@ -76,6 +76,35 @@ def chunk_prefill_ex(q, k, v, q_win, k_win, n_chunks, chunk_size, n_keep, slot_r
                 pool_v=pool_v, table=table, dev_err=dev_err, workspace=ws)
 
 
+def chunk_prefill_layers(q, k, v, q_win, n_chunks, chunk_size, n_keep, slot_row, pool_rows,
+                         sm_scale=0.0, stream=None):
+    """pfd_chunk_prefill_layers: L layers' prefill in one call.  q, k, v:
+    [L, N*(C+1), H, D]; q_win [L, W, Hq, D].  Returns a dict with out,
+    scores [L, N, C+1], kept_idx [L, N, B], pool_k / pool_v
+    [L, pool_rows, Hkv, D], table [L, N, 2] and dev_err."""
+    _need_cuda(q, k, v, q_win, slot_row)
+    n_layers, rows, hq, d = q.shape
+    hkv = k.shape[2]
+    w = q_win.shape[1]
+    dev = q.device
+    out = torch.empty_like(q)
+    pool_k = torch.zeros(n_layers, pool_rows, hkv, d, dtype=torch.bfloat16, device=dev)
+    pool_v = torch.zeros_like(pool_k)
+    scores = torch.empty(n_layers, n_chunks, chunk_size + 1, dtype=torch.float32, device=dev)
+    kept = torch.empty(n_layers, n_chunks, max(n_keep, 1), dtype=torch.int32, device=dev)
+    table = torch.empty(n_layers, n_chunks, 2, dtype=torch.int32, device=dev)
+    dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_bytes = _abi.pfd_chunk_prefill_layers_workspace(n_layers, n_chunks, chunk_size, w, hq, hkv,
+                                                       d, n_keep)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _abi.pfd_chunk_prefill_layers(q, k, v, q_win if w > 0 else None, n_layers, n_chunks,
+                                  chunk_size, w, hq, hkv, d, n_keep, sm_scale, out, scores, kept,
+                                  pool_k, pool_v, pool_rows, slot_row, table, dev_err, ws,
+                                  ws_bytes, stream)
+    return dict(out=out, scores=scores, kept_idx=kept[..., :n_keep], pool_k=pool_k,
+                pool_v=pool_v, table=table, dev_err=dev_err, workspace=ws)
+
+
 def select_chunks(s_i, s_p, n_select, stream=None):
     """Top-K chunk selection (pfd_select_chunks).  Returns (sel, s)."""
     _need_cuda(s_i, s_p)

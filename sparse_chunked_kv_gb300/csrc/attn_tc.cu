@@ -134,7 +134,8 @@ __device__ __forceinline__ bool resolve_item(const AttnParams& p, int idx, Item&
     idx /= pairs;
     it.g = idx % p.Hkv;
     it.chunk = idx / p.Hkv;
-    it.q_row0 = it.kind == kChunk ? static_cast<long long>(it.chunk) * p.chunk_rows : 0;
+    it.q_row0 = it.kind == kChunk ? static_cast<long long>(it.chunk) * p.chunk_rows
+                                  : static_cast<long long>(it.chunk / p.layer_chunks) * p.n_win;
     it.split = 0;
     it.k0 = it.k1 = 0;
   } else {

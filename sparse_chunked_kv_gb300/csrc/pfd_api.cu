@@ -168,23 +168,31 @@ bool decode_host_ok(int batch, const int32_t* cu_lq_host, const int32_t* cu_k_ho
 
 constexpr int kMaxSplits = 64;
 
-// Chunked prefill of one request (pfd_chunk_prefill, pfd_chunk_prefill_ex):
-// per_kv_head ranks per (chunk, KV head); k_win (may be null) puts the
-// window keys into the window rows' softmax denominator.
+// Chunked prefill of one request (pfd_chunk_prefill, pfd_chunk_prefill_ex,
+// pfd_chunk_prefill_layers): L stacked layers of N chunks (layer l's chunk j
+// is chunk l*N + j of the stacked tensors, its window rows l*W.., its pool
+// l*pool_rows rows further, its slot slot_row[j]); per_kv_head ranks per
+// (chunk, KV head); k_win (may be null; L == 1) puts the window keys into the
+// window rows' softmax denominator.
 pfd_status prefill_impl(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
-                        const pfd_bf16* q_win, int N, int C, int W, int Hq, int Hkv, int D, int B,
+                        const pfd_bf16* q_win, int L, int N, int C, int W, int Hq, int Hkv, int D,
+                        int B,
                         float sm_scale, pfd_bf16* out, float* scores, int32_t* kept_idx,
                         pfd_bf16* pool_k, pfd_bf16* pool_v, int64_t pool_rows,
                         const int32_t* slot_row, pfd_chunk_entry* table, int32_t* dev_err,
                         void* workspace, size_t workspace_bytes, bool per_kv_head,
                         const pfd_bf16* k_win, pfd_stream_t stream) {
-  if (N < 1 || C < 1 || W < 0 || B < 0 || B > C) return PFD_ERR_INVALID_ARG;
+  if (L < 1 || N < 1 || C < 1 || W < 0 || B < 0 || B > C) return PFD_ERR_INVALID_ARG;
+  if (k_win != nullptr && L != 1) return PFD_ERR_INVALID_ARG;
   if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return PFD_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return PFD_ERR_UNSUPPORTED;
   const int G = Hq / Hkv;
   if (C > 8192 || G > kBlockM || W > 256 || static_cast<long long>(W) * G > 512)
     return PFD_ERR_UNSUPPORTED;
-  if (static_cast<long long>(N) * (C + 1) * Hq * D >= (1ll << 40)) return PFD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(L) * N * (C + 1) * Hq * D >= (1ll << 40) ||
+      static_cast<long long>(L) * N * (C + 1) >= (1ll << 31) ||
+      static_cast<long long>(L) * N >= (1ll << 24))
+    return PFD_ERR_UNSUPPORTED;
   if (!q || !k || !v || !out || !scores || !pool_k || !pool_v || !slot_row || !table)
     return PFD_ERR_INVALID_ARG;
   if (B > 0 && !kept_idx) return PFD_ERR_INVALID_ARG;
@@ -194,14 +202,15 @@ pfd_status prefill_impl(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(pool_k) ||
       !aligned16(pool_v) || (W > 0 && !aligned16(q_win)))
     return PFD_ERR_INVALID_ARG;
-  const PrefillWs ws = prefill_ws_layout(N, C, W, Hq, Hkv);
+  const int NL = L * N;   // chunks of all layers
+  const PrefillWs ws = prefill_ws_layout(NL, C, W, Hq, Hkv);
   if (workspace_bytes < ws.total || (ws.total > 0 && workspace == nullptr) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return PFD_ERR_INVALID_ARG;
   const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
-  const long long rows = static_cast<long long>(N) * (C + 1);
+  const long long rows = static_cast<long long>(NL) * (C + 1);
 
   const int Tq = kBlockM / G;
   AttnParams ap;
@@ -212,7 +221,8 @@ pfd_status prefill_impl(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
   copy_kv_maps(ap.tm_k, 1, 0);
   copy_kv_maps(ap.tm_v, 1, 0);
   if (W > 0) {
-    if (!make_map(&ap.tm_q[1], q_win, W, Hq, D, G, Tq)) return PFD_ERR_CUDA;
+    if (!make_map(&ap.tm_q[1], q_win, static_cast<long long>(L) * W, Hq, D, G, Tq))
+      return PFD_ERR_CUDA;
   } else {
     ap.tm_q[1] = ap.tm_q[0];
   }
@@ -229,16 +239,17 @@ pfd_status prefill_impl(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
   ap.Hkv = Hkv;
   ap.G = G;
   ap.D = D;
-  ap.n_chunks = N;
+  ap.n_chunks = NL;
+  ap.layer_chunks = N;
   ap.chunk_rows = C + 1;
   ap.n_win = W;
   ap.mt_chunk = ceil_div(C + 1, Tq);
   ap.mt_win = W > 0 ? ceil_div(W, Tq) : 0;
-  ap.n_chunk_items = N * Hkv * ceil_div(ap.mt_chunk, 2);
+  ap.n_chunk_items = NL * Hkv * ceil_div(ap.mt_chunk, 2);
   ap.n_splits = 1;
   ap.scale_log2 = scale * kLog2e;
   const long long items =
-      static_cast<long long>(ap.n_chunk_items) + static_cast<long long>(N) * Hkv * ceil_div(ap.mt_win, 2);
+      static_cast<long long>(ap.n_chunk_items) + static_cast<long long>(NL) * Hkv * ceil_div(ap.mt_win, 2);
   if (items >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
   ap.n_items = static_cast<int>(items);
   // Every tensor map is encoded before the first launch, so that a failure
@@ -247,10 +258,12 @@ pfd_status prefill_impl(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
   std::memset(&wp, 0, sizeof(wp));
   wp.k_tiles = ceil_div(C + 1, 128);
   wp.concat = (C + 1 >= 128) ? 1 : 0;
+  const long long layer_rows = static_cast<long long>(N) * (C + 1);   // tiles per layer
   const long long ws_items =
-      wp.concat ? (rows + 127) / 128 : static_cast<long long>(N) * wp.k_tiles;
+      wp.concat ? (layer_rows + 127) / 128 : static_cast<long long>(N) * wp.k_tiles;
   if (ws_items >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
-  if (W > 0 && !make_map(&wp.tm_qwin, q_win, W, Hq, D, G, W)) return PFD_ERR_CUDA;
+  if (W > 0 && !make_map(&wp.tm_qwin, q_win, static_cast<long long>(L) * W, Hq, D, G, W))
+    return PFD_ERR_CUDA;
   const int grid = static_cast<int>(std::min<long long>(items, device_sm_count()));
   pfd_status s = PFD_OK;
   if (k_win != nullptr) {
@@ -271,6 +284,7 @@ pfd_status prefill_impl(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
     wp.win_stride = ap.win_stride;
     wp.part_scores = reinterpret_cast<float*>(wsb + ws.part_scores);
     wp.n_chunks = N;
+    wp.n_layers = L;
     wp.chunk_rows = C + 1;
     wp.n_win = W;
     wp.Hq = Hq;
@@ -297,7 +311,9 @@ pfd_status prefill_impl(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
   tp.table = table;
   tp.dev_err = dev_err;
   tp.pool_rows = pool_rows;
-  tp.n_chunks = N;
+  tp.layer_pool_rows = pool_rows;
+  tp.layer_chunks = N;
+  tp.n_chunks = NL;
   tp.chunk_size = C;
   tp.n_keep = B;
   tp.Hkv = Hkv;
@@ -475,7 +491,7 @@ pfd_status pfd_chunk_prefill(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf1
                              int64_t pool_rows, const int32_t* slot_row, pfd_chunk_entry* table,
                              int32_t* dev_err, void* workspace, size_t workspace_bytes,
                              pfd_stream_t stream) {
-  return prefill_impl(q, k, v, q_win, N, C, W, Hq, Hkv, D, B, sm_scale, out, scores, kept_idx,
+  return prefill_impl(q, k, v, q_win, 1, N, C, W, Hq, Hkv, D, B, sm_scale, out, scores, kept_idx,
                       pool_k, pool_v, pool_rows, slot_row, table, dev_err, workspace,
                       workspace_bytes, false, nullptr, stream);
 }
@@ -488,9 +504,29 @@ pfd_status pfd_chunk_prefill_ex(const pfd_bf16* q, const pfd_bf16* k, const pfd_
                                 pfd_chunk_entry* table, int32_t* dev_err, void* workspace,
                                 size_t workspace_bytes, pfd_stream_t stream) {
   if (per_kv_head != 0 && per_kv_head != 1) return PFD_ERR_INVALID_ARG;
-  return prefill_impl(q, k, v, q_win, N, C, W, Hq, Hkv, D, B, sm_scale, out, scores, kept_idx,
+  return prefill_impl(q, k, v, q_win, 1, N, C, W, Hq, Hkv, D, B, sm_scale, out, scores, kept_idx,
                       pool_k, pool_v, pool_rows, slot_row, table, dev_err, workspace,
                       workspace_bytes, per_kv_head != 0, k_win, stream);
+}
+
+size_t pfd_chunk_prefill_layers_workspace(int L, int N, int C, int W, int Hq, int Hkv, int D,
+                                          int B) {
+  (void)D;
+  (void)B;
+  if (L < 1 || N < 1 || C < 1 || W < 0 || Hq < 1 || Hkv < 1) return 0;
+  return prefill_ws_layout(L * N, C, W, Hq, Hkv).total;
+}
+
+pfd_status pfd_chunk_prefill_layers(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
+                                    const pfd_bf16* q_win, int L, int N, int C, int W, int Hq,
+                                    int Hkv, int D, int B, float sm_scale, pfd_bf16* out,
+                                    float* scores, int32_t* kept_idx, pfd_bf16* pool_k,
+                                    pfd_bf16* pool_v, int64_t pool_rows, const int32_t* slot_row,
+                                    pfd_chunk_entry* table, int32_t* dev_err, void* workspace,
+                                    size_t workspace_bytes, pfd_stream_t stream) {
+  return prefill_impl(q, k, v, q_win, L, N, C, W, Hq, Hkv, D, B, sm_scale, out, scores, kept_idx,
+                      pool_k, pool_v, pool_rows, slot_row, table, dev_err, workspace,
+                      workspace_bytes, false, nullptr, stream);
 }
 
 pfd_status pfd_chunk_loglik(const pfd_bf16* logits, const int32_t* labels, int N, int R,

@@ -75,6 +75,7 @@ struct AttnParams {
 
   // prefill
   int n_chunks, chunk_rows, n_win;
+  int layer_chunks;     // chunks per layer (window rows of chunk c: layer c / layer_chunks)
   int mt_chunk;         // query tiles per (chunk, KV head) of chunk rows
   int mt_win;           // query tiles per (chunk, KV head) of window rows
   int n_chunk_items;    // n_chunks * Hkv * mt_chunk
@@ -101,7 +102,9 @@ struct WinScoreParams {
   int n_chunks, chunk_rows, n_win, Hq, Hkv, G, D;
   int k_tiles;              // ceil((C+1) / 128)
   int concat;               // 1: 128-row tiles over the chunks laid end to end (C+1 >= 128)
-  int n_items;              // tiles per KV group
+  int n_items;              // tiles per KV group and layer
+  int n_layers;             // stacked layers: layer l's chunks are l*N .. l*N+N-1, its
+                            // window rows l*W .. l*W+W-1 of the q_win map
   float scale_log2;
   int32_t* dev_err;
 };
@@ -125,6 +128,10 @@ struct TopBParams {
   long long pool_rows;
   int n_chunks, chunk_size, n_keep, Hkv, D;
   int copy_splits;
+  int layer_chunks;          // chunks per layer: chunk c writes layer c / layer_chunks's
+                             // pool (layer_pool_rows rows further per layer) at slot
+                             // slot_row[c % layer_chunks], table entries relative to it
+  long long layer_pool_rows;
   int per_head;              // 1: one ranking per (chunk, KV head): scores [N, Hkv, C+1],
                              // kept_idx [N, Hkv, B], head g's slot column from head g's set
 };

@@ -57,8 +57,11 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int& 
 __device__ __forceinline__ void copy_kept_rows(const TopBParams& p, int j, int head, int part,
                                                int rows, const int* kept_src, int tid) {
   const int B = p.n_keep;
-  const long long slot = p.slot_row[j];
-  const bool slot_ok = slot >= 0 && slot + B + 1 <= p.pool_rows;
+  // Layer of chunk j: its pool starts layer_pool_rows rows further per layer.
+  const int layer = j / p.layer_chunks;
+  const long long slot = p.slot_row[j % p.layer_chunks];
+  const bool slot_ok = slot >= 0 && slot + B + 1 <= p.layer_pool_rows;
+  const long long pool0 = static_cast<long long>(layer) * p.layer_pool_rows;
   if (part == 0 && tid == 0 && head <= 0) {
     pfd_chunk_entry e;
     e.row = slot_ok ? static_cast<int32_t>(slot) : 0;
@@ -77,7 +80,7 @@ __device__ __forceinline__ void copy_kept_rows(const TopBParams& p, int j, int h
   for (int idx = tid; idx < (r1 - r0) * units; idx += kTopBThreads) {
     const int r = r0 + idx / units, u = u0 + idx % units;
     const long long src = (chunk_row0 + kept_src[r]) * row_units + u;
-    const long long dst = (slot + r) * row_units + u;
+    const long long dst = (pool0 + slot + r) * row_units + u;
     reinterpret_cast<uint4*>(p.pool_k)[dst] = __ldg(reinterpret_cast<const uint4*>(p.k) + src);
     reinterpret_cast<uint4*>(p.pool_v)[dst] = __ldg(reinterpret_cast<const uint4*>(p.v) + src);
   }

@@ -14,8 +14,10 @@
 // partial score per KV group; the top-B kernel adds the Hkv partials in a
 // fixed order.
 //
-// The kernel is persistent: CTA c serves KV group c % Hkv, loads that group's
-// window rows once and streams 128-row K tiles through a two-slot ring.  When
+// The kernel is persistent: CTA c serves KV group c % Hkv of one layer (of
+// several stacked layers, each with its own window rows), loads that group's
+// window rows once and streams that layer's 128-row K tiles through a
+// two-slot ring.  When
 // a chunk has at least 128 rows the tiles run over the chunks' rows laid end to
 // end (a tile then spans at most two chunks, so no tile is mostly padding);
 // otherwise each tile is a piece of one chunk.  S^T is split into two column
@@ -72,8 +74,13 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
 
   grid_dependency_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // CTA -> (KV group g, layer, index among the CTAs of that pair).
   const int g = blockIdx.x % p.Hkv;
-  const int cta_g = blockIdx.x / p.Hkv, n_cta_g = gridDim.x / p.Hkv;
+  const int layer = (blockIdx.x / p.Hkv) % p.n_layers;
+  const int cta_g = blockIdx.x / (p.Hkv * p.n_layers);
+  const int n_cta_g = gridDim.x / (p.Hkv * p.n_layers);
+  const long long layer_row0 = static_cast<long long>(layer) * p.n_chunks * p.chunk_rows;
+  const long long layer_chunk0 = static_cast<long long>(layer) * p.n_chunks;
   const int nw = p.n_win * p.G;          // window rows of this group (TMEM columns)
   const int nwp = (nw + 31) & ~31;       // padded: two halves of a multiple of 16
   const int half = nwp / 2;
@@ -91,7 +98,7 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
   // (2^(s - inf) = 0).
   auto b_src = [&](int c, int n) -> const float* {
     if (c >= p.n_chunks || n >= nw) return nullptr;
-    return p.win_b + (static_cast<long long>(c) * p.Hkv + g) * p.win_stride + n;
+    return p.win_b + ((layer_chunk0 + c) * p.Hkv + g) * p.win_stride + n;
   };
   const int n_items = p.n_items;
 
@@ -136,14 +143,15 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
       bool ok = true;
       mbar_arrive_expect_tx(&q_full, static_cast<uint32_t>(nw) * D * 2u);
       for (int pn = 0; pn < D / 64; ++pn)
-        tma_load_3d(q_tile + pn * q_panel, &p.tm_qwin, &q_full, pn * 64, g * p.G, 0);
+        tma_load_3d(q_tile + pn * q_panel, &p.tm_qwin, &q_full, pn * 64, g * p.G,
+                    layer * p.n_win);
       auto load_k = [&](int k, int i) {
         const int slot = k & 1;
         mbar_arrive_expect_tx(&k_full[slot], kKBytes);
         const Tile t = tile_of(p, i);
         for (int pn = 0; pn < D / 64; ++pn)
           tma_load_3d(k_ring + slot * kKBytes + pn * kPanelBytes, &p.tm_k, &k_full[slot], pn * 64, g,
-                      static_cast<int>(t.row0));
+                      static_cast<int>(layer_row0 + t.row0));
       };
       int k = 0;
       if (cta_g < n_items) load_k(0, cta_g);
@@ -248,7 +256,7 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
       named_barrier_sync(kConsumerBarrier, kConsumers);
       if (sub == 0 && row < t.nrows && c_row < p.n_chunks) {
         const int tt = static_cast<int>(r - static_cast<long long>(c_row) * p.chunk_rows);
-        p.part_scores[(static_cast<long long>(c_row) * p.Hkv + g) * p.chunk_rows + tt] =
+        p.part_scores[((layer_chunk0 + c_row) * p.Hkv + g) * p.chunk_rows + tt] =
             acc + red[k & 1][row];
       }
     }
@@ -275,8 +283,9 @@ cudaError_t launch_window_scores(const WinScoreParams& p, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return err;
-  const int per_g = std::max(1, std::min(sms / p.Hkv, p.n_items));
-  const int grid = per_g * p.Hkv;
+  const int pairs = p.Hkv * std::max(1, p.n_layers);   // (KV group, layer) pairs
+  const int per_g = std::max(1, std::min(sms / pairs, p.n_items));
+  const int grid = per_g * pairs;
   const size_t smem =
       1024 + ((static_cast<size_t>(nwp) * p.D * 2 + 1023) & ~static_cast<size_t>(1023)) +
       2 * 128 * static_cast<size_t>(p.D) * 2;

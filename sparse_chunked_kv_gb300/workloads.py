@@ -167,6 +167,17 @@ def make_request(cfg: Config, seq: int = 0) -> dict:
                 slot_row=slot_row, needle_chunks=needle_chunks, needle_rows=needle_rows)
 
 
+def make_layers(cfg: Config, n_layers: int, seq: int = 0) -> dict:
+    """L layers of one request: layer l is make_request(cfg, seq + 101 * l);
+    q, k, v [L, N*(C+1), H, D] and q_win [L, W, Hq, D] stacked; the slots
+    (slot_row) are layer 0's, shared by every layer's pool."""
+    reqs = [make_request(cfg, seq + 101 * l) for l in range(n_layers)]
+    out = {key: torch.stack([r[key] for r in reqs]) for key in ("q", "k", "v", "q_win")}
+    out["slot_row"] = reqs[0]["slot_row"]
+    out["layers"] = reqs
+    return out
+
+
 def make_step(cfg: Config, seq: int, step: int) -> dict:
     """Draws the response rows of denoising step `step`."""
     gen = torch.Generator().manual_seed(1000 * cfg.config_id + seq + 7919 * (step + 1))

@@ -404,6 +404,32 @@ def check_per_head_topb_and_compact(orc, seed=17):
             assert np.array_equal(pv[slot[j]:slot[j] + b + 1, g], v[src, g])
 
 
+def check_layers_are_independent(orc, seed=18):
+    """Multi-layer prefill: each layer equals the single-layer prefill of its
+    own tensors (chunk attention against SDPA with a block mask), and
+    reversing the layer order reverses the results."""
+    gen = torch.Generator().manual_seed(seed)
+    n_layers, n, c, w, hq, hkv, d, b = 3, 2, 5, 3, 4, 2, 8, 2
+    rows = n * (c + 1)
+    q, k, v = rand(gen, n_layers, rows, hq, d), rand(gen, n_layers, rows, hkv, d), \
+        rand(gen, n_layers, rows, hkv, d)
+    q_win = rand(gen, n_layers, w, hq, d)
+    slot = np.array([3, 0], dtype=np.int32)
+    res = orc.chunk_prefill_layers(q, k, v, q_win, n, c, b, slot, 6, 0.3)
+    rev = orc.chunk_prefill_layers(q[::-1], k[::-1], v[::-1], q_win[::-1], n, c, b, slot, 6, 0.3)
+    blk = np.arange(rows) // (c + 1)
+    mask = blk[:, None] == blk[None, :]
+    for l in range(n_layers):
+        for h in range(hq):
+            want = sdpa(q[l, :, h], k[l, :, h // 2], v[l, :, h // 2], mask, 0.3)
+            assert np.max(np.abs(res[l]["out"][:, h] - want)) < 1e-12
+        s1 = orc.window_scores(q_win[l], k[l], n, c, 0.3)
+        assert np.max(np.abs(res[l]["scores"] - s1)) < 1e-12
+        assert np.array_equal(res[l]["kept"], orc.top_b(s1, b))
+        for key in ("out", "scores", "kept", "pool_k", "pool_v", "table"):
+            assert np.array_equal(res[l][key], rev[n_layers - 1 - l][key])
+
+
 # ----------------------------------------------------------- chunk scores --
 
 def check_loglik_vs_cross_entropy(orc, seed=15):
@@ -442,6 +468,6 @@ ALL_CHECKS = [
     check_chunk_attention, check_scores_vs_sdpa, check_scores_brute_force, check_scores_invariants,
     check_scores_single_row, check_top_b, check_select, check_split_equals_concat,
     check_split_at_arbitrary_points, check_loglik_vs_cross_entropy, check_loglik_closed_forms,
-    check_scores_alt_readings, check_per_head_topb_and_compact,
+    check_scores_alt_readings, check_per_head_topb_and_compact, check_layers_are_independent,
     check_decode_vs_sdpa, check_dense_equivalence, check_compact, check_cost_model,
 ]
