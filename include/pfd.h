@@ -350,6 +350,50 @@ pfd_status pfd_decode_partial(const pfd_bf16* q, const pfd_bf16* k_self, const p
 pfd_status pfd_lse_merge(const pfd_bf16* part_o, const float* part_lse, int n_parts, int rows,
                          int Hq, int D, pfd_bf16* out, float* lse, pfd_stream_t stream);
 
+/*
+ * Dynamic chunk reselection.  The pages list static selection (no
+ * reselection during decoding) as a limitation of the method; this is the
+ * reading taken here.  At a reselection step the live rows score every chunk
+ * of their sequence by the attention mass its cached rows receive at that
+ * step's normaliser:
+ *   mass[c] = (1 / (Lq_b * Hq)) * sum over the sequence's live rows r, query
+ *             heads h and the rows t of chunk c's slot of
+ *             exp(sm_scale * q[r][h] . k_pool[t][h / (Hq/Hkv)] - lse[r][h])
+ * with lse the step's decode log-sum-exp (pfd_decode_attention's lse
+ * output).  For a selected chunk this is its share of the step's attention;
+ * for the others, the share they would take at the same normaliser.
+ * Sequence b's chunks are table entries cu_n_host[b] .. cu_n_host[b+1]-1;
+ * mass is written at the same indices.
+ *   q            [total_lq, Hq, D] bf16 live rows (the step's queries)
+ *   cu_lq        [batch+1] int32 device; cu_lq_host, cu_n_host [batch+1] host
+ *   pool_k       [pool_rows, Hkv, D] bf16; table [table_len]
+ *   lse          [total_lq, Hq] fp32 device
+ *   mass         [table_len] fp32 device (written for the listed chunks)
+ *   workspace    >= pfd_chunk_mass_workspace(...) bytes
+ * batch <= 64.  QK on the tensor cores over every chunk's slot (no PV);
+ * fixed-order sums, so repeated calls give the same bits.
+ */
+size_t pfd_chunk_mass_workspace(int batch, const int32_t* cu_lq_host, const int32_t* cu_n_host,
+                                int Hq, int Hkv);
+
+pfd_status pfd_chunk_mass(const pfd_bf16* q, const int32_t* cu_lq, const int32_t* cu_lq_host,
+                          const pfd_bf16* pool_k, int64_t pool_rows, const pfd_chunk_entry* table,
+                          int32_t table_len, const int32_t* cu_n_host, const float* lse, int batch,
+                          int Hq, int Hkv, int D, float sm_scale, float* mass, int32_t* dev_err,
+                          void* workspace, size_t workspace_bytes, pfd_stream_t stream);
+
+/*
+ * The new selection: for every chunk s'[c] = fl32(s[c] + fl32(lambda *
+ * mass[c])) (two fp32 roundings, nearest even), then the top-K of s' per
+ * sequence with pfd_select_chunks_batched's rules and layout (sel holds
+ * table indices in rank order; s_out [..] receives s', or NULL).  s is the
+ * static score fl32(s_I + s_P) (pfd_select_chunks's s_out).  lambda >= 0;
+ * lambda = 0 gives the static selection.
+ */
+pfd_status pfd_reselect_chunks(const float* s, const float* mass, float lambda,
+                               const int32_t* cu_n, const int32_t* cu_k, int batch, int max_n,
+                               int32_t* sel, float* s_out, pfd_stream_t stream);
+
 /* Bytes of the static device scratch used by
  * pfd_decode_attention_static_scratch (per device). */
 #define PFD_DECODE_STATIC_SCRATCH_BYTES ((size_t)32 << 20)

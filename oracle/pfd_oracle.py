@@ -43,6 +43,15 @@ Readings where the pages leave a step open (each is stated where it is used):
   R4  The decode live block (query window + response, Lq rows) attends to
       itself and to the kept rows of the selected chunks, with no mask.
   R5  The softmax scale is 1/sqrt(D) unless given.
+  R7  Dynamic reselection (the pages list static selection as a limitation):
+      at a reselection step the live rows score every chunk j of the
+      sequence by the attention mass its cached rows would receive at that
+      step's normaliser, mass_j = mean over (row, head) of
+      sum over the slot's rows t of exp(sm_scale q . k_t - lse), lse the
+      step's decode log-sum-exp; for a selected chunk this is its share of
+      the step's attention.  The new selection is the top-K of
+      s'_j = fl32(s_j + fl32(lambda * mass_j)), s_j = fl32(s_I + s_P), with
+      the ranking rules of R3; lambda = 0 keeps the static selection.
   R6  The chunk scores come from the model's logits: s_I is the
       log-likelihood of the query-window tokens and s_P that of the
       pseudo-labels, each conditioned on the chunk -- the sum over the
@@ -363,6 +372,40 @@ def decode_attention_split(q, k_self, v_self, pool_k, pool_v, table, sel, sm_sca
         parts.append(split_partials(q, pool_k[lo:lo + n], pool_v[lo:lo + n], group, sm_scale))
     parts.append(split_partials(q, k_self, v_self, group, sm_scale))
     return lse_merge(parts)
+
+
+# ---------------------------------------------------- reselection (R7) --
+
+def chunk_mass(q, pool_k, table, chunks, lse, sm_scale):
+    """R7: mean attention mass of each listed chunk at the normaliser lse.
+
+    q: [Lq, Hq, D] live rows; pool_k [pool_rows, Hkv, D]; table [.., 2];
+    chunks: table indices; lse [Lq, Hq] (natural log).  Returns [len(chunks)]
+    fp64: sum over rows, heads and the chunk's slot rows of
+    exp(sm_scale q . k - lse), divided by Lq * Hq.
+    """
+    n_live, n_q_heads, _ = q.shape
+    group = n_q_heads // pool_k.shape[1]
+    out = np.zeros(len(chunks))
+    for i, c in enumerate(chunks):
+        lo, n = int(table[c, 0]), int(table[c, 1])
+        total = 0.0
+        for h in range(n_q_heads):
+            logits = sm_scale * (q[:, h, :] @ pool_k[lo:lo + n, h // group, :].T)   # [Lq, n]
+            total += np.exp(logits - lse[:, h:h + 1]).sum()
+        out[i] = total / (n_live * n_q_heads)
+    return out
+
+
+def reselect_chunks(s, mass, lam, n_select):
+    """R7 + R3: the n_select chunks with the largest
+    s' = fl32(fl32(s) + fl32(fl32(lam) * fl32(mass))) (two fp32 roundings,
+    round to nearest even); returns (sel [n_select] in rank order, s' [N])."""
+    s32 = np.asarray(s, dtype=np.float32)
+    bonus = np.float32(lam) * np.asarray(mass, dtype=np.float32)
+    s2 = (s32 + bonus.astype(np.float32)).astype(np.float32)
+    order = sorted(range(s2.shape[0]), key=lambda j: _rank_key(s2[j], j))
+    return np.array(order[:n_select], dtype=np.int32), s2
 
 
 # ------------------------------------------------------- chunk scores --

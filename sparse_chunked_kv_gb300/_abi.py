@@ -48,6 +48,10 @@ SIGNATURES = {
     "pfd_decode_partial": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _P, ctypes.c_int32, _P, _P, _P,
                                 _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "pfd_lse_merge": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P]),
+    "pfd_chunk_mass_workspace": (_SZ, [_I, _P, _P, _I, _I]),
+    "pfd_chunk_mass": (_I, [_P, _P, _P, _P, _I64, _P, ctypes.c_int32, _P, _P, _I, _I, _I, _I, _F,
+                            _P, _P, _P, _SZ, _P]),
+    "pfd_reselect_chunks": (_I, [_P, _P, _F, _P, _P, _I, _I, _P, _P, _P]),
     "pfd_status_string": (ctypes.c_char_p, [_I]),
     "pfd_abi_version": (_I, []),
 }
@@ -232,3 +236,23 @@ def pfd_chunk_prefill_layers(q, k, v, q_win, L, N, C, W, Hq, Hkv, D, B, sm_scale
         _ptr(out), _ptr(scores), _ptr(kept_idx), _ptr(pool_k), _ptr(pool_v), int(pool_rows),
         _ptr(slot_row), _ptr(table), _ptr(dev_err), _ptr(workspace), int(workspace_bytes),
         _stream(stream)))
+
+
+def pfd_chunk_mass_workspace(batch, cu_lq_host, cu_n_host, Hq, Hkv):
+    a, b = _host_i32(cu_lq_host), _host_i32(cu_n_host)
+    return load().pfd_chunk_mass_workspace(batch, ctypes.cast(a, _P), ctypes.cast(b, _P), Hq, Hkv)
+
+
+def pfd_chunk_mass(q, cu_lq, cu_lq_host, pool_k, pool_rows, table, table_len, cu_n_host, lse,
+                   batch, Hq, Hkv, D, sm_scale, mass, dev_err, workspace, workspace_bytes,
+                   stream=None):
+    a, b = _host_i32(cu_lq_host), _host_i32(cu_n_host)
+    _check(load().pfd_chunk_mass(
+        _ptr(q), _ptr(cu_lq), ctypes.cast(a, _P), _ptr(pool_k), int(pool_rows), _ptr(table),
+        int(table_len), ctypes.cast(b, _P), _ptr(lse), batch, Hq, Hkv, D, float(sm_scale),
+        _ptr(mass), _ptr(dev_err), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def pfd_reselect_chunks(s, mass, lam, cu_n, cu_k, batch, max_n, sel, s_out, stream=None):
+    _check(load().pfd_reselect_chunks(_ptr(s), _ptr(mass), float(lam), _ptr(cu_n), _ptr(cu_k),
+                                      batch, max_n, _ptr(sel), _ptr(s_out), _stream(stream)))

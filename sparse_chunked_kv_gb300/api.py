@@ -226,3 +226,38 @@ def chunk_loglik(logits, labels, row_ll=None, score=None, dev_err=None, stream=N
         dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
     _abi.pfd_chunk_loglik(logits, labels, n, r, v, row_ll, score, dev_err, stream)
     return score, row_ll, dev_err
+
+
+def chunk_mass(q, pool_k, table, lse, cu_lq, cu_n, sm_scale=0.0, mass=None, dev_err=None,
+               stream=None):
+    """Attention mass of every chunk at the step's normaliser (pfd_chunk_mass).
+    cu_lq, cu_n: host lists.  Returns (mass [table_len], dev_err)."""
+    _need_cuda(q, pool_k, table, lse)
+    dev = q.device
+    total_lq, hq, d = q.shape
+    hkv = pool_k.shape[1]
+    cu_lq_host, cu_n_host = [int(x) for x in cu_lq], [int(x) for x in cu_n]
+    batch = len(cu_lq_host) - 1
+    cu_lq_dev = torch.tensor(cu_lq_host, dtype=torch.int32).to(dev)
+    if mass is None:
+        mass = torch.zeros(table.shape[0], dtype=torch.float32, device=dev)
+    if dev_err is None:
+        dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_bytes = _abi.pfd_chunk_mass_workspace(batch, cu_lq_host, cu_n_host, hq, hkv)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    _abi.pfd_chunk_mass(q, cu_lq_dev, cu_lq_host, pool_k, pool_k.shape[0], table, table.shape[0],
+                        cu_n_host, lse, batch, hq, hkv, d, sm_scale, mass, dev_err, ws, ws_bytes,
+                        stream)
+    return mass, dev_err
+
+
+def reselect_chunks(s, mass, lam, cu_n, cu_k, max_n, stream=None):
+    """New selection from s + lambda * mass (pfd_reselect_chunks).  cu_n, cu_k:
+    device int32.  Returns (sel, s')."""
+    _need_cuda(s, mass, cu_n, cu_k)
+    batch = cu_n.shape[0] - 1
+    total_k = int(cu_k[-1].item())
+    sel = torch.empty(max(total_k, 1), dtype=torch.int32, device=s.device)
+    s2 = torch.empty_like(s)
+    _abi.pfd_reselect_chunks(s, mass, lam, cu_n, cu_k, batch, max_n, sel, s2, stream)
+    return sel[:total_k], s2

@@ -66,11 +66,12 @@ constexpr float kRescaleThreshold = 8.0f;        // log2 units
 constexpr uint32_t kPanelBytes = 128u * 128u;    // 128 rows x 128 B
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
 
 __device__ __forceinline__ uint32_t tmem_s_col(int x) { return x ? 128u : 0u; }
 __device__ __forceinline__ uint32_t tmem_o_col(int x) { return x ? 384u : 256u; }
 
-enum ItemKind : int { kChunk = 0, kWindow = 1, kDecode = 2 };
+enum ItemKind : int { kChunk = 0, kWindow = 1, kDecode = 2, kMass = 3 };
 
 // Valid rows of a 16-row key group, one byte per group: 16 for a full
 // group, 0 for a group past the tile's end, n (1..15) for the last group of a
@@ -138,6 +139,24 @@ __device__ __forceinline__ bool resolve_item(const AttnParams& p, int idx, Item&
                                   : static_cast<long long>(it.chunk / p.layer_chunks) * p.n_win;
     it.split = 0;
     it.k0 = it.k1 = 0;
+  } else if (p.mode == kModeMass) {
+    // sequence b of the item (mass_item0 is non-decreasing, b < 64)
+    int b = 0;
+    while (b + 1 < p.mass_batch && p.mass_item0[b + 1] <= idx) ++b;
+    const int local = idx - p.mass_item0[b];
+    const int pairs = p.mass_pairs[b];
+    it.kind = kMass;
+    it.ta = 2 * (local % pairs);
+    const int rest = local / pairs;
+    it.g = rest % p.Hkv;
+    it.chunk = p.mass_n0[b] + rest / p.Hkv;   // table index
+    it.q_map = 0;
+    it.split = 0;
+    it.k0 = it.k1 = 0;
+    const int lq0 = p.cu_lq[b], lq1 = p.cu_lq[b + 1];
+    if (lq0 < 0 || lq1 < lq0 || lq1 > p.total_lq) return false;   // reported by the producer
+    it.q_row0 = lq0;
+    it.n_t = lq1 - lq0;
   } else {
     const int pairs = (p.mt_max + 1) / 2;
     it.kind = kDecode;
@@ -165,6 +184,12 @@ __device__ __forceinline__ bool resolve_item(const AttnParams& p, int idx, Item&
 
 __device__ __forceinline__ bool item_shape_error(const AttnParams& p, int idx) {
   if (p.mode == kModePrefill) return false;
+  if (p.mode == kModeMass) {
+    int b = 0;
+    while (b + 1 < p.mass_batch && p.mass_item0[b + 1] <= idx) ++b;
+    const int lq0 = p.cu_lq[b], lq1 = p.cu_lq[b + 1];
+    return lq0 < 0 || lq1 < lq0 || lq1 > p.total_lq;
+  }
   const int pairs = (p.mt_max + 1) / 2;
   const int seq = idx / pairs / p.n_splits / p.Hkv;
   const int lq0 = p.cu_lq[seq], lq1 = p.cu_lq[seq + 1];
@@ -238,7 +263,16 @@ __device__ __forceinline__ int load_segments(const AttnParams& p, const Item& it
                                              int32_t* seg_len, int32_t* seg_g0, int lane) {
   int nseg;
   __syncwarp();
-  if (it.kind != kDecode) {
+  if (it.kind == kMass) {
+    nseg = 1;
+    if (lane == 0) {
+      const pfd_chunk_entry e = p.table[it.chunk];
+      const bool bad = e.row < 0 || e.len < 0 || static_cast<long long>(e.row) + e.len > p.pool_rows;
+      if (bad) raise_dev_err(p.dev_err, PFD_DEVERR_TABLE);
+      seg_row[0] = bad ? 0 : e.row;
+      seg_len[0] = bad ? 0 : e.len;
+    }
+  } else if (it.kind != kDecode) {
     nseg = 1;
     if (lane == 0) {
       seg_row[0] = it.chunk * p.chunk_rows + 1;   // the content rows; BOS enters analytically
@@ -295,8 +329,9 @@ struct RowState {
 };
 
 // kPrefill: a prefill launch (chunk and window items, with the analytic BOS
-// key); else a decode launch, compiled without that code.
-template <int D, bool kPrefill>
+// key); else a decode launch, compiled without that code.  kMassMode: a
+// chunk-mass launch (decode-shaped, mass items only).
+template <int D, bool kPrefill, bool kMassMode>
 __global__ void __launch_bounds__(kThreads, 1)
 attention_kernel(const __grid_constant__ AttnParams p) {
   using L = Layout<D>;
@@ -372,7 +407,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         if (lane == 0 && item_shape_error(p, idx)) raise_dev_err(p.dev_err, PFD_DEVERR_SHAPE);
         continue;
       }
-      const bool with_pv = it.kind != kWindow;
+      const bool with_pv = it.kind != kWindow && it.kind != kMass;
       const int nseg = load_segments(p, it, seg_row, seg_len, seg_g0, lane);
       const long long total = seg_g0[nseg];
       const int n_splits = it.kind == kDecode ? p.n_splits : 1;
@@ -521,7 +556,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
       for (int kk = 0, idx; ok && (idx = nth_item<kPrefill>(p, kk)) >= 0; ++kk) {
         Item it;
         if (!resolve_item(p, idx, it)) continue;
-        const bool with_pv = it.kind != kWindow;
+        const bool with_pv = it.kind != kWindow && it.kind != kMass;
         const int nx = it.has_b ? 2 : 1;
         bool ofree_done[2] = {items_done == 0, items_done == 0};
         auto wait_ofree = [&](int x) -> bool {
@@ -675,9 +710,24 @@ attention_kernel(const __grid_constant__ AttnParams p) {
     for (int kk = 0, idx; ok && (idx = nth_item<kPrefill>(p, kk)) >= 0; ++kk) {
       Item it;
       if (!resolve_item(p, idx, it)) continue;
-      const bool with_pv = it.kind != kWindow;
+      const bool with_pv = it.kind != kWindow && it.kind != kMass;
       const bool active = x == 0 || it.has_b;
       float m_used = -INFINITY, l_sum = 0.0f;
+      if constexpr (kMassMode) {
+        // Mass items: every probability is taken at the step's normaliser,
+        // p = 2^(s * scale - lse * log2(e)), so the row's reference is its
+        // lse and never moves (rows past the block, or with no finite lse,
+        // get +inf: their probabilities are 0).
+        const int t_local = row / G;
+        const int t = (it.ta + x) * p.Tq + t_local;
+        float b = INFINITY;
+        if (active && row < q_rows && t < it.n_t) {
+          const float lse_row =
+              p.mass_lse[(it.q_row0 + t) * p.Hq + it.g * G + (row - t_local * G)];
+          if (isfinite(lse_row)) b = lse_row * kLog2e;
+        }
+        m_used = b;
+      }
       float s_bos = 0.0f;   // prefill: this row's BOS logit q . k0 (unscaled)
       int n_seen = 0;
       const uint8_t* bos = smem + L::kBos0 + (items_done & 1) * 2 * L::kBosBox;
@@ -766,6 +816,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
           }
         }
 
+        if constexpr (!kMassMode) {
         // Pass 1: row max over the tile, 64 columns (two TMEM loads) at a time.
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
@@ -814,6 +865,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
           }
           l_sum *= alpha;
           m_used = m_new;
+        }
         }
 
         // Pass 2: probabilities relative to m_used -> bf16 pairs in TMEM
@@ -884,7 +936,18 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         l_sum = l_sum * o_alpha + o_bos;
         m_used = m_new;
       }
-      if (active) {
+      if constexpr (kMassMode) {
+        // This warp's rows' mass over the chunk: one partial per (item, query
+        // tile, warp), summed per chunk in a fixed order by the mass-sum
+        // kernel.
+        const int t_local = row / G;
+        const int t = (it.ta + x) * p.Tq + t_local;
+        float v = (active && row < q_rows && t < it.n_t) ? l_sum : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        if (lane == 0) p.mass_part[static_cast<long long>(idx) * 8 + x * 4 + quarter] = v;
+      }
+      if (!kMassMode && active) {
         const int t_local = row / G;
         const int jj = row - t_local * G;
         const int t = (it.ta + x) * p.Tq + t_local;
@@ -1013,23 +1076,28 @@ size_t attention_smem_bytes(int D, bool prefill) {
   return 1024 + (prefill ? Layout<128>::kTotalPrefill : Layout<128>::kTotalDecode);
 }
 
-template <int D, bool kPrefill>
+template <int D, bool kPrefill, bool kMassMode>
 cudaError_t launch_attention_t(const AttnParams& p, int grid, size_t smem, cudaStream_t stream) {
   const cudaError_t err = ensure_smem_limit(
-      reinterpret_cast<const void*>(attention_kernel<D, kPrefill>), static_cast<int>(smem));
+      reinterpret_cast<const void*>(attention_kernel<D, kPrefill, kMassMode>),
+      static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  return launch_pdl(attention_kernel<D, kPrefill>, dim3(grid), dim3(kThreads), smem, stream, p);
+  return launch_pdl(attention_kernel<D, kPrefill, kMassMode>, dim3(grid), dim3(kThreads), smem,
+                    stream, p);
 }
 
 cudaError_t launch_attention(const AttnParams& p, int grid, cudaStream_t stream) {
   if (grid <= 0 || p.n_items <= 0) return cudaSuccess;
   const bool prefill = p.mode == kModePrefill;
   const size_t smem = attention_smem_bytes(p.D, prefill);
+  if (p.mode == kModeMass)
+    return p.D == 64 ? launch_attention_t<64, false, true>(p, grid, smem, stream)
+                     : launch_attention_t<128, false, true>(p, grid, smem, stream);
   if (p.D == 64)
-    return prefill ? launch_attention_t<64, true>(p, grid, smem, stream)
-                   : launch_attention_t<64, false>(p, grid, smem, stream);
-  return prefill ? launch_attention_t<128, true>(p, grid, smem, stream)
-                 : launch_attention_t<128, false>(p, grid, smem, stream);
+    return prefill ? launch_attention_t<64, true, false>(p, grid, smem, stream)
+                   : launch_attention_t<64, false, false>(p, grid, smem, stream);
+  return prefill ? launch_attention_t<128, true, false>(p, grid, smem, stream)
+                 : launch_attention_t<128, false, false>(p, grid, smem, stream);
 }
 
 }  // namespace pfd

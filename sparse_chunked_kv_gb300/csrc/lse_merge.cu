@@ -242,4 +242,65 @@ cudaError_t launch_lse_merge(const MergeParams& params, int sm_count, cudaStream
   return launch_merge_with(lse_merge_kernel_one, 1, 1, params, sm_count, stream);
 }
 
+namespace {
+
+// Per-chunk sums of the chunk-mass partials (see AttnParams::mass_*): one
+// warp per chunk of every sequence; lane l adds values l, l + 32, ... of
+// the chunk's contiguous partials in order, then a fixed shuffle tree.
+struct MassSumParams {
+  const float* part;
+  float* mass;
+  int batch, Hkv;
+  int chunk_base[kMaxMassBatch + 1];   // prefix of the sequences' chunk counts
+  int n0[kMaxMassBatch];
+  int item0[kMaxMassBatch];
+  int pairs[kMaxMassBatch];
+  float inv_rows[kMaxMassBatch];       // 1 / (Lq_b * Hq), 0 when Lq_b = 0
+};
+
+__global__ void __launch_bounds__(128) mass_sum_kernel(const __grid_constant__ MassSumParams p) {
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (i >= p.chunk_base[p.batch]) return;
+  int b = 0;
+  while (b + 1 < p.batch && p.chunk_base[b + 1] <= i) ++b;
+  const int c = i - p.chunk_base[b];
+  const int n_vals = p.Hkv * p.pairs[b] * 8;
+  const float* src = p.part + (static_cast<long long>(p.item0[b]) + static_cast<long long>(c) * p.Hkv * p.pairs[b]) * 8;
+  float acc = 0.0f;
+  for (int k = lane; k < n_vals; k += 32) acc += src[k];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  if (lane == 0) p.mass[p.n0[b] + c] = acc * p.inv_rows[b];
+}
+
+}  // namespace
+
+cudaError_t launch_mass_sum(const AttnParams& ap, const int32_t* cu_lq_host, int n_chunks_total,
+                            float* mass, cudaStream_t stream) {
+  if (n_chunks_total <= 0) return cudaSuccess;
+  MassSumParams p;
+  p.part = ap.mass_part;
+  p.mass = mass;
+  p.batch = ap.mass_batch;
+  p.Hkv = ap.Hkv;
+  p.chunk_base[0] = 0;
+  for (int b = 0; b < ap.mass_batch; ++b) {
+    const int n_b = (ap.mass_pairs[b] > 0 && ap.Hkv > 0)
+                        ? (ap.mass_item0[b + 1] - ap.mass_item0[b]) / (ap.Hkv * ap.mass_pairs[b])
+                        : 0;
+    p.chunk_base[b + 1] = p.chunk_base[b] + n_b;
+    p.n0[b] = ap.mass_n0[b];
+    p.item0[b] = ap.mass_item0[b];
+    p.pairs[b] = ap.mass_pairs[b];
+    const long long rows = static_cast<long long>(cu_lq_host[b + 1] - cu_lq_host[b]) * ap.Hq;
+    p.inv_rows[b] = rows > 0 ? static_cast<float>(1.0 / static_cast<double>(rows)) : 0.0f;
+  }
+  const int n = p.chunk_base[ap.mass_batch];
+  if (n <= 0) return cudaSuccess;
+  return launch_pdl(mass_sum_kernel, dim3((n + 3) / 4), dim3(128), 0, stream, p);
+}
+
 }  // namespace pfd

@@ -544,7 +544,7 @@ pfd_status pfd_select_chunks(const float* s_I, const float* s_P, int N, int K, i
                              float* s_out, pfd_stream_t stream) {
   if (!s_I || !s_P || !sel || N < 1 || K < 1 || K > N) return PFD_ERR_INVALID_ARG;
   if (N > 16384) return PFD_ERR_UNSUPPORTED;
-  return from_cuda(launch_select(s_I, s_P, nullptr, nullptr, N, K, 1, N, sel, s_out,
+  return from_cuda(launch_select(s_I, s_P, nullptr, nullptr, N, K, 1, N, 1.0f, sel, s_out,
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -554,7 +554,7 @@ pfd_status pfd_select_chunks_batched(const float* s_I, const float* s_P, const i
   if (!s_I || !s_P || !sel || !cu_n || !cu_k || batch < 1 || max_n < 1)
     return PFD_ERR_INVALID_ARG;
   if (max_n > 16384) return PFD_ERR_UNSUPPORTED;
-  return from_cuda(launch_select(s_I, s_P, cu_n, cu_k, 0, 0, batch, max_n, sel, s_out,
+  return from_cuda(launch_select(s_I, s_P, cu_n, cu_k, 0, 0, batch, max_n, 1.0f, sel, s_out,
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -633,6 +633,129 @@ pfd_status pfd_lse_merge(const pfd_bf16* part_o, const float* part_lse, int n_pa
   mp.Hq = Hq;
   mp.D = D;
   return from_cuda(launch_lse_merge(mp, device_sm_count(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------- reselection --
+
+namespace {
+
+struct MassPlan {
+  int batch = 0;
+  int item0[kMaxMassBatch + 1];
+  int n0[kMaxMassBatch];
+  int pairs[kMaxMassBatch];
+  long long items = 0;
+  int chunks = 0;
+};
+
+bool mass_plan(int batch, const int32_t* cu_lq_host, const int32_t* cu_n_host, int Hq, int Hkv,
+               MassPlan* mp) {
+  if (batch < 1 || batch > kMaxMassBatch || !cu_lq_host || !cu_n_host) return false;
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Hq / Hkv > kBlockM) return false;
+  if (cu_lq_host[0] != 0 || cu_n_host[0] != 0) return false;
+  const int Tq = kBlockM / (Hq / Hkv);
+  mp->batch = batch;
+  long long items = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int lq = cu_lq_host[b + 1] - cu_lq_host[b], n = cu_n_host[b + 1] - cu_n_host[b];
+    if (lq < 0 || n < 0) return false;
+    mp->item0[b] = static_cast<int>(items);
+    mp->n0[b] = cu_n_host[b];
+    mp->pairs[b] = (ceil_div(lq, Tq) + 1) / 2;
+    items += static_cast<long long>(n) * Hkv * mp->pairs[b];
+    if (items >= (1ll << 31)) return false;
+  }
+  mp->item0[batch] = static_cast<int>(items);
+  mp->items = items;
+  mp->chunks = cu_n_host[batch];
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pfd_chunk_mass_workspace(int batch, const int32_t* cu_lq_host, const int32_t* cu_n_host,
+                                int Hq, int Hkv) {
+  MassPlan mp;
+  if (!mass_plan(batch, cu_lq_host, cu_n_host, Hq, Hkv, &mp)) return 0;
+  return align256(static_cast<size_t>(mp.items) * 8 * sizeof(float));
+}
+
+pfd_status pfd_chunk_mass(const pfd_bf16* q, const int32_t* cu_lq, const int32_t* cu_lq_host,
+                          const pfd_bf16* pool_k, int64_t pool_rows, const pfd_chunk_entry* table,
+                          int32_t table_len, const int32_t* cu_n_host, const float* lse, int batch,
+                          int Hq, int Hkv, int D, float sm_scale, float* mass, int32_t* dev_err,
+                          void* workspace, size_t workspace_bytes, pfd_stream_t stream) {
+  if (!q || !cu_lq || !pool_k || !table || !lse || !mass) return PFD_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return PFD_ERR_UNSUPPORTED;
+  if (batch > kMaxMassBatch) return PFD_ERR_UNSUPPORTED;
+  MassPlan mp;
+  if (!mass_plan(batch, cu_lq_host, cu_n_host, Hq, Hkv, &mp)) return PFD_ERR_INVALID_ARG;
+  const int total_lq = cu_lq_host[batch];
+  if (total_lq < 1 || cu_n_host[batch] > table_len || table_len < 1 || pool_rows < 1)
+    return PFD_ERR_INVALID_ARG;
+  if (pool_rows >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(pool_k)) return PFD_ERR_INVALID_ARG;
+  const size_t need = align256(static_cast<size_t>(mp.items) * 8 * sizeof(float));
+  if (workspace_bytes < need || (need > 0 && workspace == nullptr) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return PFD_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (mp.items == 0) return PFD_OK;
+  const int G = Hq / Hkv;
+  const int Tq = kBlockM / G;
+  AttnParams ap;
+  std::memset(&ap, 0, sizeof(ap));
+  if (!make_map(&ap.tm_q[0], q, total_lq, Hq, D, G, Tq) ||
+      !make_kv_maps(ap.tm_k, 0, pool_k, pool_rows, Hkv, D))
+    return PFD_ERR_CUDA;
+  ap.tm_q[1] = ap.tm_q[0];
+  copy_kv_maps(ap.tm_k, 1, 0);
+  for (int lv = 0; lv < kBoxLevels; ++lv)
+    for (int t = 0; t < 2; ++t) ap.tm_v[lv][t] = ap.tm_k[lv][t];   // no PV in mass items
+  const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  ap.Tq = Tq;
+  ap.q = reinterpret_cast<const bf16*>(q);
+  ap.table = table;
+  ap.table_len = table_len;
+  ap.pool_rows = pool_rows;
+  ap.cu_lq = cu_lq;
+  ap.total_lq = total_lq;
+  ap.dev_err = dev_err;
+  ap.mode = kModeMass;
+  ap.Hq = Hq;
+  ap.Hkv = Hkv;
+  ap.G = G;
+  ap.D = D;
+  ap.batch = batch;
+  ap.n_splits = 1;
+  ap.scale_log2 = scale * kLog2e;
+  ap.mass_lse = lse;
+  ap.mass_part = static_cast<float*>(workspace);
+  ap.mass_batch = batch;
+  for (int b = 0; b <= batch; ++b) ap.mass_item0[b] = mp.item0[b];
+  for (int b = 0; b < batch; ++b) {
+    ap.mass_n0[b] = mp.n0[b];
+    ap.mass_pairs[b] = mp.pairs[b];
+  }
+  ap.n_items = static_cast<int>(mp.items);
+  const int grid = static_cast<int>(std::min<long long>(mp.items, device_sm_count()));
+  pfd_status s = from_cuda(launch_attention(ap, grid, st));
+  if (s != PFD_OK) return s;
+  return from_cuda(launch_mass_sum(ap, cu_lq_host, mp.chunks, mass, st));
+}
+
+pfd_status pfd_reselect_chunks(const float* s, const float* mass, float lambda,
+                               const int32_t* cu_n, const int32_t* cu_k, int batch, int max_n,
+                               int32_t* sel, float* s_out, pfd_stream_t stream) {
+  if (!s || !mass || !sel || !cu_n || !cu_k || batch < 1 || max_n < 1 || !(lambda >= 0.0f))
+    return PFD_ERR_INVALID_ARG;
+  if (max_n > 16384) return PFD_ERR_UNSUPPORTED;
+  return from_cuda(launch_select(s, mass, cu_n, cu_k, 0, 0, batch, max_n, lambda, sel, s_out,
+                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -31,7 +31,8 @@ constexpr int kBlockN = kGroupRows * kGroupsPerTile;
 constexpr int kBoxLevels = 4;      // K/V box heights 16, 32, 64, 128 rows
 constexpr int kMaxSegments = 512;   // selected chunks per sequence + the live block
 
-enum AttnMode : int { kModePrefill = 0, kModeDecode = 1 };
+enum AttnMode : int { kModePrefill = 0, kModeDecode = 1, kModeMass = 2 };
+constexpr int kMaxMassBatch = 64;   // sequences of one chunk-mass call
 
 struct AttnParams {
   // Query tensors addressed by TMA: index 0 = prefill chunk rows or decode
@@ -86,6 +87,16 @@ struct AttnParams {
 
   float scale_log2;     // sm_scale * log2(e)
   int out_v8;           // out is 32-byte aligned: whole-sector (32-byte) stores
+
+  // chunk mass (kModeMass): items of sequence b are mass_item0[b] ..
+  // mass_item0[b+1]-1, item = (chunk c * Hkv + g) * mass_pairs[b] + pair, the
+  // chunk being table entry mass_n0[b] + c
+  const float* mass_lse;   // [total_lq, Hq] the step's decode log-sum-exp (natural log)
+  float* mass_part;        // [n_items, 8] partial sums (two query tiles x four warps)
+  int mass_batch;
+  int mass_item0[kMaxMassBatch + 1];
+  int mass_n0[kMaxMassBatch];
+  int mass_pairs[kMaxMassBatch];
 };
 
 cudaError_t launch_attention(const AttnParams& p, int grid, cudaStream_t stream);
@@ -139,9 +150,10 @@ struct TopBParams {
 cudaError_t launch_topb_compact(const TopBParams& p, cudaStream_t stream);
 
 // ----------------------------------------------------------- selection --
+// s = fl32(s_i + fl32(lambda * s_p)) per chunk (lambda = 1: fl32(s_i + s_p)).
 cudaError_t launch_select(const float* s_i, const float* s_p, const int32_t* cu_n,
                           const int32_t* cu_k, int n_scalar, int k_scalar, int batch, int max_n,
-                          int32_t* sel, float* s_out, cudaStream_t stream);
+                          float lambda, int32_t* sel, float* s_out, cudaStream_t stream);
 
 // ------------------------------------------------------------ LSE merge --
 struct MergeParams {
@@ -159,6 +171,11 @@ struct MergeParams {
 
 // sm_count: SMs of the current device (the grid is one wave of resident CTAs).
 cudaError_t launch_lse_merge(const MergeParams& p, int sm_count, cudaStream_t stream);
+
+// Per-chunk sums of the chunk-mass partials: mass[n0[b] + c] = (sum of the
+// partials of chunk c of sequence b) / (Lq_b * Hq).
+cudaError_t launch_mass_sum(const AttnParams& p, const int32_t* cu_lq_host, int n_chunks_total,
+                            float* mass, cudaStream_t stream);
 
 // -------------------------------------------------------- chunk scores --
 cudaError_t launch_chunk_loglik(const bf16* logits, const int32_t* labels, int n_chunks,

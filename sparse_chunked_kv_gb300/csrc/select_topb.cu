@@ -233,7 +233,8 @@ constexpr int kSelectThreads = 1024;
 __global__ void __launch_bounds__(kSelectThreads)
 select_kernel(const float* __restrict__ s_i, const float* __restrict__ s_p,
               const int32_t* __restrict__ cu_n, const int32_t* __restrict__ cu_k, int n_scalar,
-              int k_scalar, int max_n, int32_t* __restrict__ sel, float* __restrict__ s_out) {
+              int k_scalar, int max_n, float lambda, int32_t* __restrict__ sel,
+              float* __restrict__ s_out) {
   extern __shared__ uint32_t keys[];
   grid_dependency_wait();
   grid_dependents_launch();
@@ -251,7 +252,9 @@ select_kernel(const float* __restrict__ s_i, const float* __restrict__ s_p,
     return;
   }
   for (int t = threadIdx.x; t < n; t += kSelectThreads) {
-    const float s = s_i[off + t] + s_p[off + t];
+    // fl32(s_i + fl32(lambda * s_p)), each step rounded to nearest even (no
+    // contraction); lambda = 1 gives fl32(s_i + s_p) exactly.
+    const float s = __fadd_rn(s_i[off + t], __fmul_rn(lambda, s_p[off + t]));
     if (s_out) s_out[off + t] = s;
     keys[t] = rank_key(s);
   }
@@ -296,12 +299,12 @@ cudaError_t launch_topb_compact(const TopBParams& params, cudaStream_t stream) {
 
 cudaError_t launch_select(const float* s_i, const float* s_p, const int32_t* cu_n,
                           const int32_t* cu_k, int n_scalar, int k_scalar, int batch, int max_n,
-                          int32_t* sel, float* s_out, cudaStream_t stream) {
+                          float lambda, int32_t* sel, float* s_out, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(max_n) * 4;
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel), static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   return launch_pdl(select_kernel, dim3(batch), dim3(kSelectThreads), smem, stream, s_i, s_p, cu_n,
-                    cu_k, n_scalar, k_scalar, max_n, sel, s_out);
+                    cu_k, n_scalar, k_scalar, max_n, lambda, sel, s_out);
 }
 
 }  // namespace pfd

@@ -430,6 +430,65 @@ def check_layers_are_independent(orc, seed=18):
             assert np.array_equal(res[l][key], rev[n_layers - 1 - l][key])
 
 
+# ------------------------------------------------------------ reselection --
+
+def check_chunk_mass(orc, seed=19):
+    """The masses of the selected chunks plus the live block's mass sum to
+    one at the step's own lse (the decode softmax, pinned to SDPA, sums to
+    one); a selected chunk's mass is e^(m - lse) l of its split partial
+    (the "free" decode mass); an unselected chunk's mass equals a brute-force
+    scalar loop."""
+    gen = torch.Generator().manual_seed(seed)
+    hq, hkv, d, lq = 4, 2, 8, 5
+    pool_k, pool_v = rand(gen, 40, hkv, d), rand(gen, 40, hkv, d)
+    table = np.array([[0, 7], [9, 5], [20, 11], [33, 4]], dtype=np.int32)
+    sel = np.array([2, 0], dtype=np.int32)
+    q, ks, vs = rand(gen, lq, hq, d), rand(gen, lq, hkv, d), rand(gen, lq, hkv, d)
+    scale = 0.45
+    _, lse = orc.decode_attention(q, ks, vs, pool_k, pool_v, table, sel, scale)
+    m_sel = orc.chunk_mass(q, pool_k, table, sel, lse, scale)
+    self_mass = 0.0
+    for h in range(hq):
+        logits = scale * (q[:, h] @ ks[:, h // 2].T)
+        self_mass += np.exp(logits - lse[:, h:h + 1]).sum()
+    assert abs(m_sel.sum() + self_mass / (lq * hq) - 1.0) < 1e-12
+    for i, c in enumerate(sel):
+        lo, n = table[c]
+        m, l, _ = orc.split_partials(q, pool_k[lo:lo + n], pool_v[lo:lo + n], 2, scale)
+        assert abs((np.exp(m - lse) * l).sum() / (lq * hq) - m_sel[i]) < 1e-12
+    got = orc.chunk_mass(q, pool_k, table, [3], lse, scale)[0]
+    want = 0.0
+    for r in range(lq):
+        for h in range(hq):
+            for t in range(33, 37):
+                x = scale * sum(q[r, h, e] * pool_k[t, h // 2, e] for e in range(d))
+                want += math.exp(x - lse[r, h])
+    assert abs(got - want / (lq * hq)) < 1e-12
+
+
+def check_reselect(orc):
+    """lambda = 0 gives the static selection; the ranking follows the
+    counting rule on fl32(s + fl32(lambda * mass)); a large enough mass lifts
+    an unselected chunk into the selection."""
+    rng = np.random.default_rng(3)
+    s = rng.standard_normal(12).astype(np.float32)
+    mass = rng.random(12).astype(np.float32)
+    sel0, _ = orc.reselect_chunks(s, mass, 0.0, 4)
+    static, _ = orc.select_chunks(s, np.zeros(12, np.float32), 4)
+    assert list(sel0) == list(static)
+    for lam in (0.5, 3.0, 100.0):
+        sel, s2 = orc.reselect_chunks(s, mass, lam, 5)
+        want = [float(np.float32(np.float32(x) + np.float32(np.float32(lam) * np.float32(m))))
+                for x, m in zip(s, mass)]
+        assert [float(x) for x in s2] == want
+        assert list(sel) == ranked_by_counting(want, 5)
+    low = int(np.argmin(s))
+    boost = np.zeros(12, np.float32)
+    boost[low] = 1.0
+    sel, _ = orc.reselect_chunks(s, boost, float(s.max() - s.min()) + 1.0, 1)
+    assert list(sel) == [low]
+
+
 # ----------------------------------------------------------- chunk scores --
 
 def check_loglik_vs_cross_entropy(orc, seed=15):
@@ -469,5 +528,6 @@ ALL_CHECKS = [
     check_scores_single_row, check_top_b, check_select, check_split_equals_concat,
     check_split_at_arbitrary_points, check_loglik_vs_cross_entropy, check_loglik_closed_forms,
     check_scores_alt_readings, check_per_head_topb_and_compact, check_layers_are_independent,
+    check_chunk_mass, check_reselect,
     check_decode_vs_sdpa, check_dense_equivalence, check_compact, check_cost_model,
 ]

@@ -145,6 +145,18 @@ def _compact_per_head_shared_rows(k, v, kept, slot_row, c, pk, pv):
                                 pk, pv)
 
 
+def _mass_without_normaliser(q, pool_k, table, chunks, lse, scale):
+    # mistake: forgets to subtract the step's log-sum-exp
+    return orc.chunk_mass(q, pool_k, table, chunks, np.zeros_like(lse), scale)
+
+
+def _reselect_single_rounding(s, mass, lam, n_select):
+    # mistake: s + lambda * mass in fp64 (one rounding at the end)
+    s2 = (np.asarray(s, np.float64) + lam * np.asarray(mass, np.float64)).astype(np.float32)
+    order = sorted(range(len(s2)), key=lambda j: orc._rank_key(s2[j], j))
+    return np.array(order[:n_select], np.int32), s2
+
+
 MUTANTS = {
     "cross_chunk_attention": (Mutant(chunk_attention=_chunk_attention_global), pins.check_chunk_attention),
     "gqa_mapping": (Mutant(chunk_attention=_chunk_attention_bad_gqa), pins.check_chunk_attention),
@@ -167,6 +179,9 @@ MUTANTS = {
                                    pins.check_scores_alt_readings),
     "per_head_compact_shared_rows": (Mutant(compact_per_head=_compact_per_head_shared_rows),
                                      pins.check_per_head_topb_and_compact),
+    "mass_without_normaliser": (Mutant(chunk_mass=_mass_without_normaliser), pins.check_chunk_mass),
+    "reselect_single_rounding": (Mutant(reselect_chunks=_reselect_single_rounding),
+                                 pins.check_reselect),
 }
 
 
