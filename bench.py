@@ -468,6 +468,121 @@ def time_scoring_head(device, reps=10):
             "timing": f"median of {reps} calls after 3 warm-ups (inputs larger than L2)"}
 
 
+def _time_calls(fn, stream, reps, flush=None):
+    """Median ms of fn() over reps calls after 3 warm-ups, CUDA events on
+    `stream`, L2 flushed before each call when a flush buffer is given."""
+    import torch
+    ms = []
+    with torch.cuda.stream(stream):
+        for it in range(3 + reps):
+            if flush is not None:
+                flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            if it >= 3:
+                ms.append(e0.elapsed_time(e1))
+    return statistics.median(ms)
+
+
+def time_next_rows(device, reps=5):
+    """The other rows of the path on the 8K-prefix workload (one request):
+    the prefill under the other ranking readings, four layers' prefill in
+    one call, and one reselection (chunk masses of all 16 chunks at decode
+    step 0's normaliser, then the new top-K); the reselection also on the
+    128K workload (all 512 chunks).  L2 flushed before every call."""
+    import torch
+
+    from sparse_chunked_kv_gb300 import _abi
+    from sparse_chunked_kv_gb300 import workloads as wl
+    out = {}
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    cfg = wl.CTX_8K
+    hq, hkv, d = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    req = wl.make_request(cfg, 0)
+    cu = lambda t: t.to(device).contiguous()  # noqa: E731
+    q, k, v, q_win, k_win = (cu(req[x]) for x in ("q", "k", "v", "q_win", "k_win"))
+    slot = cu(req["slot_row"])
+    n, c, b, w = cfg.n_chunks, cfg.chunk_size, cfg.n_keep, cfg.n_win
+    pool_k = torch.zeros(cfg.pool_rows, hkv, d, dtype=torch.bfloat16, device=device)
+    pool_v = torch.zeros_like(pool_k)
+    o = torch.empty_like(q)
+    scores = torch.empty(n * hkv, c + 1, dtype=torch.float32, device=device)
+    kept = torch.empty(n * hkv, b, dtype=torch.int32, device=device)
+    table = torch.empty(n, 2, dtype=torch.int32, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    ws_b = _abi.pfd_chunk_prefill_workspace(n, c, w, hq, hkv, d, b)
+    ws = torch.empty(ws_b, dtype=torch.uint8, device=device)
+    pflops, pbytes = prefill_flops(cfg), prefill_bytes(cfg)
+    for key, per_head, kw in (("rank_per_kv_head", 1, None), ("rank_window_keys", 0, k_win),
+                              ("rank_per_kv_head_window_keys", 1, k_win)):
+        ms = _time_calls(lambda: _abi.pfd_chunk_prefill_ex(
+            q, k, v, q_win, kw, n, c, w, hq, hkv, d, b, 0.0, per_head, o, scores, kept, pool_k,
+            pool_v, cfg.pool_rows, slot, table, err, ws, ws_b), stream, reps, flush)
+        out[key] = {"workload": "8k prefill (pfd_chunk_prefill_ex)", "us": ms * 1e3,
+                    "tflops": pflops / (ms * 1e-3) / 1e12, "gbs": pbytes / (ms * 1e-3) / 1e9,
+                    "bound": "tensor", "flops": pflops}
+    # four layers in one call
+    n_layers = 4
+    lay = wl.make_layers(cfg, n_layers)
+    lq, lk, lv, lqw = (cu(lay[x]) for x in ("q", "k", "v", "q_win"))
+    lo = torch.empty_like(lq)
+    lscores = torch.empty(n_layers, n, c + 1, dtype=torch.float32, device=device)
+    lkept = torch.empty(n_layers, n, b, dtype=torch.int32, device=device)
+    lpk = torch.zeros(n_layers, cfg.pool_rows, hkv, d, dtype=torch.bfloat16, device=device)
+    lpv = torch.zeros_like(lpk)
+    ltab = torch.empty(n_layers, n, 2, dtype=torch.int32, device=device)
+    lws_b = _abi.pfd_chunk_prefill_layers_workspace(n_layers, n, c, w, hq, hkv, d, b)
+    lws = torch.empty(lws_b, dtype=torch.uint8, device=device)
+    ms = _time_calls(lambda: _abi.pfd_chunk_prefill_layers(
+        lq, lk, lv, lqw, n_layers, n, c, w, hq, hkv, d, b, 0.0, lo, lscores, lkept, lpk, lpv,
+        cfg.pool_rows, slot, ltab, err, lws, lws_b), stream, reps, flush)
+    ms_single = _time_calls(lambda: [_abi.pfd_chunk_prefill(
+        lq[l], lk[l], lv[l], lqw[l], n, c, w, hq, hkv, d, b, 0.0, lo[l], lscores[l], lkept[l],
+        lpk[l], lpv[l], cfg.pool_rows, slot, ltab[l], err, lws, lws_b) for l in range(n_layers)],
+        stream, reps, flush)
+    out["multi_layer_prefill"] = {
+        "workload": f"8k prefill x {n_layers} layers in one call (pfd_chunk_prefill_layers)",
+        "us": ms * 1e3, "tflops": n_layers * pflops / (ms * 1e-3) / 1e12,
+        "us_as_separate_calls": ms_single * 1e3, "bound": "tensor", "flops": n_layers * pflops}
+    del lq, lk, lv, lo, lpk, lpv
+    # reselection: masses of every chunk at step 0's normaliser + new top-K
+    for name in ("8k", "128k"):
+        cfg = wl.CONFIGS[name]
+        job = Job([cfg], 0, device)
+        job.prefill_select()
+        job.decode(0)
+        torch.cuda.synchronize()
+        cu_n = [0, cfg.n_chunks]
+        mws_b = _abi.pfd_chunk_mass_workspace(1, job.cu_lq_host, cu_n, job.hq, job.hkv)
+        mws = torch.empty(max(mws_b, 256), dtype=torch.uint8, device=device)
+        mass = torch.empty(cfg.n_chunks, dtype=torch.float32, device=device)
+        cu_n_d = torch.tensor(cu_n, dtype=torch.int32, device=device)
+        sel2 = torch.empty_like(job.sel)
+        s2 = torch.empty_like(job.s_out)
+
+        def resel():
+            _abi.pfd_chunk_mass(job.live[0][0], job.cu_lq, job.cu_lq_host, job.pool_k,
+                                job.pool_rows, job.table, job.table_len, cu_n, job.dec_lse[0], 1,
+                                job.hq, job.hkv, job.d, 0.0, mass, job.dev_err, mws, mws_b)
+            _abi.pfd_reselect_chunks(job.s_out, mass, 1.0, cu_n_d, job.cu_k, 1, cfg.n_chunks,
+                                     sel2, s2)
+        ms = _time_calls(resel, stream, reps, flush)
+        if int(job.dev_err.item()) != 0:
+            raise RuntimeError(f"reselection {name}: device error {int(job.dev_err.item())}")
+        fl = 2.0 * job.hq * cfg.n_live * cfg.n_chunks * (cfg.n_keep + 1) * job.d
+        out[f"reselection_{name}"] = {
+            "workload": f"{name}: masses of all {cfg.n_chunks} chunks at decode step 0 + top-"
+                        f"{cfg.n_select} (pfd_chunk_mass + pfd_reselect_chunks)",
+            "us": ms * 1e3, "tflops": fl / (ms * 1e-3) / 1e12, "bound": "tensor", "flops": fl}
+        del job
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_e2e(args, job, stream):
     """The same work through the C ABI from pinned host buffers.
 
@@ -755,6 +870,7 @@ def main():
         for name in [x for x in args.per_config.split(",") if x and x != args.config]:
             others[name] = time_workload(name, 0, device)
         next_rows["scoring_head"] = time_scoring_head(device)
+        next_rows.update(time_next_rows(device))
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -817,6 +933,10 @@ def main():
                 row["frac"] = row["gbs"] / hbm
                 row["peak"] = hbm
                 row["peak_kind"] = f"{peak_kind} HBM copy"
+            else:
+                row["frac"] = row["tflops"] / burst
+                row["peak"] = burst
+                row["peak_kind"] = f"{peak_kind} bf16 burst"
             line["next_rows"][key] = row
     if "e2e" in res:
         e = res["e2e"]

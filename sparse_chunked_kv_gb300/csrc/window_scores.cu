@@ -303,41 +303,57 @@ cudaError_t launch_window_scores(const WinScoreParams& p, cudaStream_t stream) {
 // of "Two-Level Sparsity" in which a window row's softmax runs over the
 // chunk's keys and the window keys together:
 //   b_self[w][h] = log2 sum_{w'} 2^(x_{w'}),  x = sm_scale log2(e) q_{w,h} . k_win_{w',g}.
-// One warp per (w, h): lanes split D, the dot product is a warp sum, the
-// running (max, sum) is kept identically by every lane.  W <= 256 keys of
-// D <= 128: a few microseconds at most, once per prefill call.
+// One warp per (w, h): the query row is staged in shared memory, lane l
+// takes keys l, l + 32, ... (W <= 256: at most 8) and computes their whole
+// dot products with 16-byte loads, all in flight together; then one
+// (max, sum) reduction over the warp.  Once per prefill call.
 __global__ void __launch_bounds__(128)
 window_self_stats_kernel(const bf16* __restrict__ q_win, const bf16* __restrict__ k_win, int W,
                          int Hq, int Hkv, int D, float scale_log2, float* __restrict__ b_self) {
+  __shared__ float q_sh[4][128];
   grid_dependency_wait();
-  const int lane = threadIdx.x & 31;
-  const long long pair = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
-  if (pair >= static_cast<long long>(W) * Hq) return;
-  const int w = static_cast<int>(pair / Hq), h = static_cast<int>(pair % Hq);
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const long long pair = static_cast<long long>(blockIdx.x) * 4 + wib;
+  const bool live = pair < static_cast<long long>(W) * Hq;
+  const int w = live ? static_cast<int>(pair / Hq) : 0, h = live ? static_cast<int>(pair % Hq) : 0;
   const int g = h / (Hq / Hkv);
   const uint16_t* q = reinterpret_cast<const uint16_t*>(q_win) + (static_cast<long long>(w) * Hq + h) * D;
-  float qv[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    qv[i] = lane + 32 * i < D ? __uint_as_float(static_cast<uint32_t>(q[lane + 32 * i]) << 16) : 0.0f;
+  for (int e = lane; e < D; e += 32)
+    q_sh[wib][e] = live ? __uint_as_float(static_cast<uint32_t>(q[e]) << 16) : 0.0f;
+  __syncwarp();
   float m = -INFINITY, l = 0.0f;
-  for (int k2 = 0; k2 < W; ++k2) {
-    const uint16_t* k = reinterpret_cast<const uint16_t*>(k_win) + (static_cast<long long>(k2) * Hkv + g) * D;
-    float dot = 0.0f;
+  if (live) {
+    float x[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (lane + 32 * i < D)
-        dot = fmaf(qv[i], __uint_as_float(static_cast<uint32_t>(k[lane + 32 * i]) << 16), dot);
+    for (int i = 0; i < 8; ++i) {
+      const int k2 = lane + 32 * i;
+      x[i] = -INFINITY;
+      if (k2 < W) {
+        const uint4* k = reinterpret_cast<const uint4*>(k_win) +
+                         ((static_cast<long long>(k2) * Hkv + g) * D) / 8;
+        float dot = 0.0f;
+        for (int c8 = 0; c8 < D / 8; ++c8) {
+          const uint4 kv = __ldg(k + c8);
+          const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-    const float x = dot * scale_log2;
-    if (x > m) {
-      l = m == -INFINITY ? 0.0f : l * ex2_approx(m - x);
-      m = x;
+          for (int j = 0; j < 4; ++j) {
+            dot = fmaf(q_sh[wib][c8 * 8 + 2 * j], __uint_as_float(kw[j] << 16), dot);
+            dot = fmaf(q_sh[wib][c8 * 8 + 2 * j + 1], __uint_as_float(kw[j] & 0xFFFF0000u), dot);
+          }
+        }
+        x[i] = dot * scale_log2;
+      }
+      m = fmaxf(m, x[i]);
     }
-    l += ex2_approx(x - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (x[i] != -INFINITY) l += ex2_approx(x[i] - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
+    if (lane == 0) b_self[pair] = m + log2f(l);
   }
-  if (lane == 0) b_self[pair] = m + log2f(l);
   grid_dependents_launch();
 }
 
