@@ -415,22 +415,32 @@ attention_kernel(const __grid_constant__ AttnParams p) {
       const int g_hi = static_cast<int>(total * (it.split + 1) / n_splits);
       const int n_tiles = (g_hi - g_lo + kGroupsPerTile - 1) / kGroupsPerTile;
       const int tiles_to_publish = n_tiles > 0 ? n_tiles : 1;
+      // Segment of each lane's group: found by binary search for the item's
+      // first tile, then carried from tile to tile (a lane's group moves 8
+      // groups on per tile, so its segment can only move forward).
+      int lseg = 0;
       for (int j = 0; ok && j < tiles_to_publish; ++j) {
         // Lanes 0..ng-1 each place one 16-row key group of the tile: its
-        // segment (binary search in the group prefix sums), source row,
-        // tensor and valid-row code.
+        // segment (seg_g0[s] <= g < seg_g0[s + 1]), source row, tensor and
+        // valid-row code.
         const int g0 = g_lo + j * kGroupsPerTile;
         const int ng = n_tiles > 0 ? min(kGroupsPerTile, g_hi - g0) : 0;
         int row = 0, t = 0;
         uint32_t code = 0;
         if (lane < ng) {
           const int g = g0 + lane;
-          int lo = 0, hi = nseg;   // seg_g0[lo] <= g < seg_g0[hi]
-          while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (seg_g0[mid] <= g) lo = mid;
-            else hi = mid;
+          int lo = lseg;
+          if (j == 0) {
+            int hi = nseg;
+            while (hi - lo > 1) {
+              const int mid = (lo + hi) >> 1;
+              if (seg_g0[mid] <= g) lo = mid;
+              else hi = mid;
+            }
+          } else {
+            while (lo + 1 < nseg && seg_g0[lo + 1] <= g) ++lo;
           }
+          lseg = lo;
           const int len = seg_len[lo];
           const int gofs = g - seg_g0[lo];
           const int nv = min(kGroupRows, len - gofs * kGroupRows);
