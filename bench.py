@@ -53,6 +53,15 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip the timings of the scoring head, ranking readings, layers and "
+                         "reselection")
+    ap.add_argument("--seqs", default="",
+                    help="comma list: run only these sequences of the workload (profiling)")
+    ap.add_argument("--profile", default="", choices=["", "decode", "prefill"],
+                    help="one small eager pass for a profiler, then exit: 'prefill' runs the "
+                         "prefill twice; 'decode' runs the prefill, frees its tensors and runs "
+                         "two decode calls")
     return ap.parse_args(argv)
 
 
@@ -231,7 +240,7 @@ class Job:
     """Device-resident buffers of one job (one or more sequences sharing one
     chunk pool and chunk table) and the library calls of one step."""
 
-    def __init__(self, cfgs, seq0, device):
+    def __init__(self, cfgs, seq0, device, max_steps=None):
         import torch
 
         from sparse_chunked_kv_gb300 import _abi
@@ -242,6 +251,8 @@ class Job:
         assert all((c.n_q_heads, c.n_kv_heads, c.head_dim, c.n_steps) == (hq, hkv, d, c0.n_steps)
                    for c in self.cfgs)
         self.hq, self.hkv, self.d, self.T = hq, hkv, d, c0.n_steps
+        if max_steps is not None:
+            self.T = min(self.T, max_steps)
         self.batch = len(self.cfgs)
         dev = device
         cu = lambda t: t.to(dev).contiguous()  # noqa: E731
@@ -299,6 +310,14 @@ class Job:
         self.dec_out = [torch.empty_like(ql) for ql, _, _ in self.live]
         self.dec_lse = [torch.empty(cu_lq[-1], hq, dtype=torch.float32, device=dev)
                         for _ in self.live]
+
+    def release_prefill(self):
+        """Drops the prefill's own inputs and outputs (the pool, table and
+        selection stay), so that a decode profile holds little memory."""
+        for sq in self.seqs:
+            for key in ("q", "k", "v", "out", "scores", "kept"):
+                sq[key] = None
+        self.ws = None
 
     def launches_per_step(self):
         prefill = sum(2 + (1 if c.n_win > 0 else 0) for c in self.cfgs)
@@ -847,12 +866,38 @@ def roofline_fracs(cfgs, dec_ms_per_call, pre_ms, peaks):
                 prefill_frac=max(t_hbm, t_tc) / pre_s)
 
 
+def run_profile(args, cfgs, device):
+    """One small eager pass for a profiler (see --profile)."""
+    import torch
+    job = Job(cfgs, 0, device, max_steps=2 if args.profile == "decode" else 1)
+    job.prefill_select()
+    if args.profile == "prefill":
+        job.prefill_select()
+    else:
+        torch.cuda.synchronize()
+        job.release_prefill()
+        torch.cuda.empty_cache()
+        job.decode(0)
+        job.decode(1)
+    torch.cuda.synchronize()
+    if int(job.dev_err.item()) != 0:
+        raise RuntimeError(f"device error word {int(job.dev_err.item())}")
+    print(json.dumps({"profile": args.profile, "workload": workload_name(args.config, cfgs),
+                      "decode_splits": job.n_splits}))
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     cfgs = job_configs(args.config)
+    if args.seqs:
+        cfgs = [cfgs[int(i)] for i in args.seqs.split(",")]
+    if args.profile:
+        import torch
+        run_profile(args, cfgs, torch.device("cuda", 0))
+        return
     if args.impl == "reference":
         run_reference(args, cfgs, rank, args.config)
         return
@@ -869,8 +914,9 @@ def main():
     if rank == 0:
         for name in [x for x in args.per_config.split(",") if x and x != args.config]:
             others[name] = time_workload(name, 0, device)
-        next_rows["scoring_head"] = time_scoring_head(device)
-        next_rows.update(time_next_rows(device))
+        if not args.no_next_rows:
+            next_rows["scoring_head"] = time_scoring_head(device)
+            next_rows.update(time_next_rows(device))
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
