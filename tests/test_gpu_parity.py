@@ -450,3 +450,39 @@ def test_outputs_aligned_to_16_but_not_32_bytes():
                              P.cuda(torch.from_numpy(sel)), n_splits=n_splits, out=dout)
         torch.cuda.synchronize()
         P.assert_close_out(dout.cpu().double().numpy(), o_ref, "decode out (16-byte aligned)")
+
+
+def test_decode_bf16_partials_error_margin(capsys):
+    """The split partials are stored as bf16 O / l with fp32 (m, l): the
+    extra rounding against one split, measured on the 8K workload's step 0
+    (every live row and head), for S = 1, 4 and 7.  Prints the figures and
+    checks each against the oracle at the parity tolerance."""
+    cfg = wl.CTX_8K
+    req = wl.make_request(cfg, 0)
+    scores = orc.window_scores(f64(req["q_win"]), f64(req["k"]), cfg.n_chunks, cfg.chunk_size,
+                               cfg.sm_scale)
+    kept = orc.top_b(scores, cfg.n_keep)
+    pk, pv, table = P.oracle_pool(cfg, req, kept, req["slot_row"], cfg.pool_rows)
+    sel, _ = orc.select_chunks(req["s_i"].numpy(), req["s_p"].numpy(), cfg.n_select)
+    ql, kl, vl = wl.live_block(req, wl.make_step(cfg, 0, 0))
+    o_ref, lse_ref = orc.decode_attention(f64(ql), f64(kl), f64(vl), pk, pv, table, sel,
+                                          cfg.sm_scale)
+    dpk, dpv = P.cuda(P.bf16_of(pk)), P.cuda(P.bf16_of(pv))
+    dtab, dsel = P.cuda(torch.from_numpy(table)), P.cuda(torch.from_numpy(sel))
+    outs = {}
+    for s in (1, 4, 7):
+        out, lse = api.decode_attention(P.cuda(ql), P.cuda(kl), P.cuda(vl), dpk, dpv, dtab, dsel,
+                                        n_splits=s)
+        torch.cuda.synchronize()
+        outs[s] = (out.cpu().double().numpy(), lse.cpu().double().numpy())
+    lines = []
+    for s, (o, l) in outs.items():
+        mx, mean = P.assert_close_out(o, o_ref, f"S={s} vs oracle")
+        lerr = np.abs(l - lse_ref).max()
+        assert lerr <= P.LSE_MAX_ABS
+        lines.append(f"S={s} vs oracle: out max {mx:.3e} mean {mean:.3e}; lse max {lerr:.3e}")
+    for s in (4, 7):
+        d = np.abs(outs[s][0] - outs[1][0])
+        lines.append(f"S={s} vs S=1: out max {d.max():.3e} mean {d.mean():.3e}")
+    with capsys.disabled():
+        print("\n" + "\n".join(lines))
