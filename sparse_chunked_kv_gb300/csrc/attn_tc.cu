@@ -808,81 +808,24 @@ attention_kernel(const __grid_constant__ AttnParams p) {
             }
           }
         };
-        // Groups that need masking, per half: for the row sum and P every
-        // group that is not 16 keys (rag2); for the row max only those whose
-        // extra rows are not keys of this row at all (rag1: groups past the
-        // tile's end, and an unshifted ragged group, whose rows past its
-        // segment may hold another slot or padding).  A shifted group's
-        // repeated rows are keys of the same segment, harmless to the max.
-        uint32_t rag1 = 0, rag2 = 0;
+        // Groups that need masking (not 16 keys), per half.
+        uint32_t rag2 = 0;
         if (!full) {
 #pragma unroll
-          for (int g = 0; g < kGroupsPerTile; ++g) {
-            const int code = nv_of(g);
-            if (code != kGroupRows) {
-              rag2 |= 1u << g;
-              if (!(code & kShifted)) rag1 |= 1u << g;
-            }
-          }
+          for (int g = 0; g < kGroupsPerTile; ++g)
+            if (nv_of(g) != kGroupRows) rag2 |= 1u << g;
         }
 
-        if constexpr (!kMassMode) {
-        // Pass 1: row max over the tile, 64 columns (two TMEM loads) at a time.
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          if (half * 64 < ncol) {
-            uint32_t sr[2][32];
-            tmem_ld32(lane_base + s_col + half * 64, sr[0]);
-            tmem_ld32(lane_base + s_col + half * 64 + 32, sr[1]);
-            tmem_ld_wait(sr[0]);
-            reg_fence(sr[1]);
-            const uint32_t m1 = (rag1 >> (4 * half)) & 0xFu;
-            if (m1) mask_half(sr, half, m1);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const int a = (i >> 1) & 1;
-              mx[a] = max3(mx[a], __uint_as_float(sr[0][i]), __uint_as_float(sr[0][i + 1]));
-              mx[2 + a] = max3(mx[2 + a], __uint_as_float(sr[1][i]), __uint_as_float(sr[1][i + 1]));
-            }
-          }
-        }
-        const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale;
-
-        // Rescale decision per row; the TMEM rescale of O is warp-collective,
-        // so a warp rescales when any of its rows needs it (alpha = 1 for the
-        // others).  s_full covers PV(j-1): O_x is complete here.
-        const bool mine = m_tile > m_used + kRescaleThreshold;
-        if (__any_sync(0xFFFFFFFFu, mine)) {
-          const float m_new = mine ? m_tile : m_used;
-          const float alpha = mine ? ex2_approx(m_used - m_new) : 1.0f;
-          if (n_seen > 1 && with_pv) {
-            uint32_t o0[32], o1[32];
-#pragma unroll 1
-            for (int ch = 0; ch < D / 32; ch += 2) {
-              tmem_ld32(lane_base + o_col + ch * 32, o0);
-              tmem_ld32(lane_base + o_col + ch * 32 + 32, o1);
-              tmem_ld_wait(o0);
-              reg_fence(o1);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                o0[i] = __float_as_uint(__uint_as_float(o0[i]) * alpha);
-                o1[i] = __float_as_uint(__uint_as_float(o1[i]) * alpha);
-              }
-              tmem_st32(lane_base + o_col + ch * 32, o0);
-              tmem_st32(lane_base + o_col + ch * 32 + 32, o1);
-            }
-          }
-          l_sum *= alpha;
-          m_used = m_new;
-        }
-        }
-
-        // Pass 2: probabilities relative to m_used -> bf16 pairs in TMEM
-        // columns [0, 64) of S_x (over logits already read), fp32 row sum.
-        const float neg_m = -m_used;
-        const uint64_t scale2 = f2_pack(scale, scale), neg_m2 = f2_pack(neg_m, neg_m);
-        uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+        // One pass over the tile, 64 columns (two TMEM loads) at a time: the
+        // masked logits, their max, the rescale decision, then probabilities
+        // relative to m_used -> bf16 pairs in TMEM columns [32 half, 32 half
+        // + 32) of S_x (over logits already read) and the fp32 row sum.
+        // A half whose max exceeds m_used by more than the threshold moves
+        // m_used (per row; alpha = 1 for the warp's other rows, as the TMEM
+        // accesses are warp-collective) and rescales what was summed against
+        // the old reference: l, O (complete here: s_full covers PV(j-1)) and,
+        // in the second half, the first half's P.  Masked logits are -inf:
+        // they add nothing to the max or the sum.
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           if (half * 64 < ncol) {
@@ -893,6 +836,48 @@ attention_kernel(const __grid_constant__ AttnParams p) {
             reg_fence(sr[1]);
             const uint32_t m2 = (rag2 >> (4 * half)) & 0xFu;
             if (m2) mask_half(sr, half, m2);
+            if constexpr (!kMassMode) {
+              float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const int a = (i >> 1) & 1;
+                mx[a] = max3(mx[a], __uint_as_float(sr[0][i]), __uint_as_float(sr[0][i + 1]));
+                mx[2 + a] = max3(mx[2 + a], __uint_as_float(sr[1][i]), __uint_as_float(sr[1][i + 1]));
+              }
+              const float m_half = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale;
+              const bool mine = m_half > m_used + kRescaleThreshold;
+              if (__any_sync(0xFFFFFFFFu, mine)) {
+                const float m_new = mine ? m_half : m_used;
+                const float alpha = mine ? ex2_approx(m_used - m_new) : 1.0f;
+                if (n_seen > 1 && with_pv) {
+#pragma unroll 1
+                  for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t o0[32];
+                    tmem_ld32(lane_base + o_col + ch * 32, o0);
+                    tmem_ld_wait(o0);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o0[i] = __float_as_uint(__uint_as_float(o0[i]) * alpha);
+                    tmem_st32(lane_base + o_col + ch * 32, o0);
+                  }
+                }
+                if (half == 1 && with_pv) {
+                  uint32_t p0[32];
+                  tmem_st_wait();   // the first half's P is in TMEM
+                  tmem_ld32(lane_base + s_col, p0);
+                  tmem_ld_wait(p0);
+#pragma unroll
+                  for (int i = 0; i < 32; ++i)
+                    p0[i] = pack_bf16x2(__uint_as_float(p0[i] << 16) * alpha,
+                                        __uint_as_float(p0[i] & 0xFFFF0000u) * alpha);
+                  tmem_st32(lane_base + s_col, p0);
+                }
+                l_sum *= alpha;
+                m_used = m_new;
+              }
+            }
+            const float neg_m = -m_used;
+            const uint64_t scale2 = f2_pack(scale, scale), neg_m2 = f2_pack(neg_m, neg_m);
+            uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
             uint32_t packed[32];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
@@ -909,12 +894,12 @@ attention_kernel(const __grid_constant__ AttnParams p) {
               packed[16 + (i >> 1)] = pack_bf16x2(b0, b1);
             }
             if (with_pv) tmem_st32(lane_base + s_col + half * 32, packed);
+            float sum[4];
+            f2_unpack(sum2[0], sum[0], sum[1]);
+            f2_unpack(sum2[1], sum[2], sum[3]);
+            l_sum += (sum[0] + sum[1]) + (sum[2] + sum[3]);
           }
         }
-        float sum[4];
-        f2_unpack(sum2[0], sum[0], sum[1]);
-        f2_unpack(sum2[1], sum[2], sum[3]);
-        l_sum += (sum[0] + sum[1]) + (sum[2] + sum[3]);
         if (with_pv) tmem_st_wait();
         // The BOS logit, while the Q tile is certainly resident: before the
         // item's last P is handed over (after it the last PV may complete and
