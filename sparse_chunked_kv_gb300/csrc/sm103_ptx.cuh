@@ -224,18 +224,6 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Warpgroup-wide register reallocation (all 128 threads of the warpgroup
-// execute it).  An increase draws on registers released by decreases of the
-// same CTA, so the shares must add up to at most the launch allocation.
-template <uint32_t kRegs>
-__device__ __forceinline__ void regs_decrease() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-template <uint32_t kRegs>
-__device__ __forceinline__ void regs_increase() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-
 // ------------------------------------------------------------- math ops --
 // Hardware base-2 exponential (MUFU), flushes denormals; exp2(-inf) = 0.
 __device__ __forceinline__ float ex2_approx(float x) {
