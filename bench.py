@@ -236,16 +236,29 @@ def recorded_traffic(profile_name, key="traffic_bytes_per_launch"):
 
 # ------------------------------------------------------------ GPU path --
 
+def prefill_shape(cfg):
+    """Sequences of one prefill shape are prefilled in one call."""
+    return (cfg.chunk_size, cfg.n_chunks, cfg.n_win, cfg.n_keep)
+
+
 class Job:
     """Device-resident buffers of one job (one or more sequences sharing one
-    chunk pool and chunk table) and the library calls of one step."""
+    chunk pool and chunk table) and the library calls of one step.
+
+    The job orders its sequences by prefill shape (stably), so that the
+    sequences of one shape are contiguous in the chunk table and are
+    prefilled by one pfd_chunk_prefill_batch call; seq_ids[i] is sequence
+    i's data seed (its index in the workload, plus seq0)."""
 
     def __init__(self, cfgs, seq0, device, max_steps=None):
         import torch
 
         from sparse_chunked_kv_gb300 import _abi
         from sparse_chunked_kv_gb300 import workloads as wl
-        self.cfgs, self.abi, self.torch = list(cfgs), _abi, torch
+        cfgs = list(cfgs)
+        order = sorted(range(len(cfgs)), key=lambda i: prefill_shape(cfgs[i]))
+        self.seq_ids = [seq0 + i for i in order]
+        self.cfgs, self.abi, self.torch = [cfgs[i] for i in order], _abi, torch
         c0 = self.cfgs[0]
         hq, hkv, d = c0.n_q_heads, c0.n_kv_heads, c0.head_dim
         assert all((c.n_q_heads, c.n_kv_heads, c.head_dim, c.n_steps) == (hq, hkv, d, c0.n_steps)
@@ -269,26 +282,51 @@ class Job:
         self.pool_v = torch.zeros_like(self.pool_k)
         self.table = torch.zeros(self.table_len, 2, dtype=torch.int32, device=dev)
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+        # Runs of sequences of one prefill shape: (first sequence, count).
+        self.groups = []
+        for i, c in enumerate(self.cfgs):
+            if self.groups and prefill_shape(self.cfgs[self.groups[-1]["i0"]]) == prefill_shape(c):
+                self.groups[-1]["L"] += 1
+            else:
+                self.groups.append(dict(i0=i, L=1))
         ws = 0
         live = [[] for _ in range(self.T)]
+        for grp in self.groups:
+            # Each group's prefill inputs and outputs are stacked [L, ...];
+            # every sequence's tensors are views of them.
+            c, L = self.cfgs[grp["i0"]], grp["L"]
+            rows = c.n_chunks * (c.chunk_size + 1)
+            grp["q"] = torch.empty(L, rows, hq, d, dtype=torch.bfloat16, device=dev)
+            grp["k"] = torch.empty(L, rows, hkv, d, dtype=torch.bfloat16, device=dev)
+            grp["v"] = torch.empty_like(grp["k"])
+            grp["q_win"] = torch.empty(L, c.n_win, hq, d, dtype=torch.bfloat16, device=dev)
+            grp["slot_row"] = torch.empty(L, c.n_chunks, dtype=torch.int32, device=dev)
+            grp["out"] = torch.empty_like(grp["q"])
+            grp["scores"] = torch.empty(L, c.n_chunks, c.chunk_size + 1, dtype=torch.float32,
+                                        device=dev)
+            grp["kept"] = torch.empty(L, c.n_chunks, max(c.n_keep, 1), dtype=torch.int32,
+                                      device=dev)
+            grp["ws_bytes"] = (
+                _abi.pfd_chunk_prefill_workspace(c.n_chunks, c.chunk_size, c.n_win, hq, hkv, d,
+                                                 c.n_keep) if L == 1 else
+                _abi.pfd_chunk_prefill_layers_workspace(L, c.n_chunks, c.chunk_size, c.n_win, hq,
+                                                        hkv, d, c.n_keep))
+            ws = max(ws, grp["ws_bytes"])
         for i, c in enumerate(self.cfgs):
-            req = wl.make_request(c, seq0 + i)
+            grp = next(g for g in self.groups if g["i0"] <= i < g["i0"] + g["L"])
+            l = i - grp["i0"]
+            req = wl.make_request(c, self.seq_ids[i])
             req["slot_row"] = (req["slot_row"] + pool_base[i]).to(torch.int32)
             self.host.append(req)
             sq = dict(cfg=c, n0=cu_n[i])
-            sq["q"], sq["k"], sq["v"] = cu(req["q"]), cu(req["k"]), cu(req["v"])
-            sq["q_win"] = cu(req["q_win"])
-            sq["slot_row"] = cu(req["slot_row"])
-            sq["out"] = torch.empty_like(sq["q"])
-            sq["scores"] = torch.empty(c.n_chunks, c.chunk_size + 1, dtype=torch.float32,
-                                       device=dev)
-            sq["kept"] = torch.empty(c.n_chunks, max(c.n_keep, 1), dtype=torch.int32, device=dev)
-            sq["ws_bytes"] = _abi.pfd_chunk_prefill_workspace(c.n_chunks, c.chunk_size, c.n_win,
-                                                              hq, hkv, d, c.n_keep)
-            ws = max(ws, sq["ws_bytes"])
+            for key in ("q", "k", "v", "q_win", "slot_row"):
+                sq[key] = grp[key][l]
+                sq[key].copy_(req[key])
+            for key in ("out", "scores", "kept"):
+                sq[key] = grp[key][l]
             self.seqs.append(sq)
             for t in range(self.T):
-                live[t].append(wl.live_block(req, wl.make_step(c, seq0 + i, t)))
+                live[t].append(wl.live_block(req, wl.make_step(c, self.seq_ids[i], t)))
         self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
         self.s_i = cu(torch.cat([h["s_i"] for h in self.host]))
         self.s_p = cu(torch.cat([h["s_p"] for h in self.host]))
@@ -314,24 +352,35 @@ class Job:
     def release_prefill(self):
         """Drops the prefill's own inputs and outputs (the pool, table and
         selection stay), so that a decode profile holds little memory."""
-        for sq in self.seqs:
+        for sq in self.seqs + self.groups:
             for key in ("q", "k", "v", "out", "scores", "kept"):
                 sq[key] = None
         self.ws = None
 
     def launches_per_step(self):
-        prefill = sum(2 + (1 if c.n_win > 0 else 0) for c in self.cfgs)
+        prefill = sum(2 + (1 if self.cfgs[g["i0"]].n_win > 0 else 0) for g in self.groups)
         return prefill + 1 + self.T * (1 + (1 if self.n_splits > 1 else 0))
 
     def prefill_select(self):
         a, hq, hkv, d = self.abi, self.hq, self.hkv, self.d
-        for sq in self.seqs:
-            c = sq["cfg"]
-            a.pfd_chunk_prefill(sq["q"], sq["k"], sq["v"], sq["q_win"] if c.n_win else None,
-                                c.n_chunks, c.chunk_size, c.n_win, hq, hkv, d, c.n_keep, 0.0,
-                                sq["out"], sq["scores"], sq["kept"], self.pool_k, self.pool_v,
-                                self.pool_rows, sq["slot_row"], self.table[sq["n0"]:],
-                                self.dev_err, self.ws, sq["ws_bytes"])
+        for grp in self.groups:
+            sq = self.seqs[grp["i0"]]
+            c, L = sq["cfg"], grp["L"]
+            if L == 1:
+                a.pfd_chunk_prefill(sq["q"], sq["k"], sq["v"], sq["q_win"] if c.n_win else None,
+                                    c.n_chunks, c.chunk_size, c.n_win, hq, hkv, d, c.n_keep, 0.0,
+                                    sq["out"], sq["scores"], sq["kept"], self.pool_k,
+                                    self.pool_v, self.pool_rows, sq["slot_row"],
+                                    self.table[sq["n0"]:], self.dev_err, self.ws,
+                                    grp["ws_bytes"])
+            else:
+                a.pfd_chunk_prefill_batch(grp["q"], grp["k"], grp["v"],
+                                          grp["q_win"] if c.n_win else None, L, c.n_chunks,
+                                          c.chunk_size, c.n_win, hq, hkv, d, c.n_keep, 0.0,
+                                          grp["out"], grp["scores"], grp["kept"], self.pool_k,
+                                          self.pool_v, self.pool_rows, grp["slot_row"],
+                                          self.table[sq["n0"]:], self.dev_err, self.ws,
+                                          grp["ws_bytes"])
         if self.batch == 1:
             c = self.cfgs[0]
             a.pfd_select_chunks(self.s_i, self.s_p, c.n_chunks, c.n_select, self.sel, self.s_out)

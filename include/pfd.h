@@ -170,6 +170,36 @@ pfd_status pfd_chunk_prefill_layers(const pfd_bf16* q, const pfd_bf16* k, const 
                                     size_t workspace_bytes, pfd_stream_t stream);
 
 /*
+ * The prefill of L requests of one shape (N, C, W, B, heads) in one call,
+ * their slots in one shared pool (Methodology 1, "Chunked Prefill and KV
+ * Caching": each request's chunks are processed on their own and cached;
+ * Methodology 3, "Decoding with Static KV Reuse": a batch of requests decodes
+ * from one pool through one chunk table).  Request l is exactly
+ * pfd_chunk_prefill over request l's tensors with slot_row[l] and table[l]
+ * into the shared pool; the requests run together, so each kernel is
+ * launched once for the batch.
+ *   q [L, N*(C+1), Hq, D], k, v [L, N*(C+1), Hkv, D] bf16 (requests stacked)
+ *   q_win [L, W, Hq, D] bf16 (each request's query-window rows)
+ *   out [L, N*(C+1), Hq, D]; scores [L, N, C+1]; kept_idx [L, N, B]
+ *   pool_k, pool_v [pool_rows, Hkv, D]: the one pool
+ *   slot_row [L, N]: first pool row of request l's chunk j; the L*N slots of
+ *       B+1 rows must not overlap (not checked); a slot outside the pool
+ *       raises PFD_DEVERR_SLOT and gets an empty table entry
+ *   table [L, N]: rows absolute in the pool (so a batched decode reads it
+ *       directly when the requests' table ranges are laid out in this order)
+ *   workspace >= pfd_chunk_prefill_layers_workspace(L, N, C, W, Hq, Hkv, D,
+ *       B) bytes
+ * Limits as for pfd_chunk_prefill, with L * N * (C+1) < 2^31 rows.
+ */
+pfd_status pfd_chunk_prefill_batch(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
+                                   const pfd_bf16* q_win, int L, int N, int C, int W, int Hq,
+                                   int Hkv, int D, int B, float sm_scale, pfd_bf16* out,
+                                   float* scores, int32_t* kept_idx, pfd_bf16* pool_k,
+                                   pfd_bf16* pool_v, int64_t pool_rows, const int32_t* slot_row,
+                                   pfd_chunk_entry* table, int32_t* dev_err, void* workspace,
+                                   size_t workspace_bytes, pfd_stream_t stream);
+
+/*
  * pfd_chunk_prefill under the two other readings of the intra-chunk ranking
  * (Methodology 2, "Two-Level Sparsity": tokens are ranked by the cumulative
  * attention weight they receive from the query tokens).  Arguments as in

@@ -34,6 +34,8 @@ SIGNATURES = {
     "pfd_chunk_prefill_layers_workspace": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "pfd_chunk_prefill_layers": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                                       _P, _P, _P, _I64, _P, _P, _P, _P, _SZ, _P]),
+    "pfd_chunk_prefill_batch": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P,
+                                     _P, _P, _P, _I64, _P, _P, _P, _P, _SZ, _P]),
     "pfd_chunk_loglik": (_I, [_P, _P, _I, _I, _I64, _P, _P, _P, _P]),
     "pfd_select_chunks": (_I, [_P, _P, _I, _I, _P, _P, _P]),
     "pfd_select_chunks_batched": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P]),
@@ -232,6 +234,16 @@ def pfd_chunk_prefill_layers(q, k, v, q_win, L, N, C, W, Hq, Hkv, D, B, sm_scale
                              kept_idx, pool_k, pool_v, pool_rows, slot_row, table, dev_err,
                              workspace, workspace_bytes, stream=None):
     _check(load().pfd_chunk_prefill_layers(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(q_win), L, N, C, W, Hq, Hkv, D, B, float(sm_scale),
+        _ptr(out), _ptr(scores), _ptr(kept_idx), _ptr(pool_k), _ptr(pool_v), int(pool_rows),
+        _ptr(slot_row), _ptr(table), _ptr(dev_err), _ptr(workspace), int(workspace_bytes),
+        _stream(stream)))
+
+
+def pfd_chunk_prefill_batch(q, k, v, q_win, L, N, C, W, Hq, Hkv, D, B, sm_scale, out, scores,
+                            kept_idx, pool_k, pool_v, pool_rows, slot_row, table, dev_err,
+                            workspace, workspace_bytes, stream=None):
+    _check(load().pfd_chunk_prefill_batch(
         _ptr(q), _ptr(k), _ptr(v), _ptr(q_win), L, N, C, W, Hq, Hkv, D, B, float(sm_scale),
         _ptr(out), _ptr(scores), _ptr(kept_idx), _ptr(pool_k), _ptr(pool_v), int(pool_rows),
         _ptr(slot_row), _ptr(table), _ptr(dev_err), _ptr(workspace), int(workspace_bytes),

@@ -105,6 +105,32 @@ def chunk_prefill_layers(q, k, v, q_win, n_chunks, chunk_size, n_keep, slot_row,
                 pool_v=pool_v, table=table, dev_err=dev_err, workspace=ws)
 
 
+def chunk_prefill_batch(q, k, v, q_win, n_chunks, chunk_size, n_keep, slot_row, pool_k, pool_v,
+                        table, sm_scale=0.0, stream=None):
+    """pfd_chunk_prefill_batch: L same-shaped requests' prefill in one call,
+    their slots in one shared pool.  q, k, v: [L, N*(C+1), H, D]; q_win
+    [L, W, Hq, D]; slot_row [L, N] absolute pool rows; pool_k / pool_v
+    [pool_rows, Hkv, D] and table [L, N, 2] are written in place.  Returns a
+    dict with out, scores [L, N, C+1], kept_idx [L, N, B] and dev_err."""
+    _need_cuda(q, k, v, q_win, slot_row, pool_k, pool_v, table)
+    n_req, rows, hq, d = q.shape
+    hkv = k.shape[2]
+    w = q_win.shape[1]
+    dev = q.device
+    out = torch.empty_like(q)
+    scores = torch.empty(n_req, n_chunks, chunk_size + 1, dtype=torch.float32, device=dev)
+    kept = torch.empty(n_req, n_chunks, max(n_keep, 1), dtype=torch.int32, device=dev)
+    dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_bytes = _abi.pfd_chunk_prefill_layers_workspace(n_req, n_chunks, chunk_size, w, hq, hkv, d,
+                                                       n_keep)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _abi.pfd_chunk_prefill_batch(q, k, v, q_win if w > 0 else None, n_req, n_chunks, chunk_size,
+                                 w, hq, hkv, d, n_keep, sm_scale, out, scores, kept, pool_k,
+                                 pool_v, pool_k.shape[0], slot_row, table, dev_err, ws, ws_bytes,
+                                 stream)
+    return dict(out=out, scores=scores, kept_idx=kept[..., :n_keep], dev_err=dev_err, workspace=ws)
+
+
 def select_chunks(s_i, s_p, n_select, stream=None):
     """Top-K chunk selection (pfd_select_chunks).  Returns (sel, s)."""
     _need_cuda(s_i, s_p)

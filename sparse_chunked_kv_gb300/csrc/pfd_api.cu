@@ -168,12 +168,13 @@ bool decode_host_ok(int batch, const int32_t* cu_lq_host, const int32_t* cu_k_ho
 
 constexpr int kMaxSplits = 64;
 
-// Chunked prefill of one request (pfd_chunk_prefill, pfd_chunk_prefill_ex,
-// pfd_chunk_prefill_layers): L stacked layers of N chunks (layer l's chunk j
-// is chunk l*N + j of the stacked tensors, its window rows l*W.., its pool
-// l*pool_rows rows further, its slot slot_row[j]); per_kv_head ranks per
-// (chunk, KV head); k_win (may be null; L == 1) puts the window keys into the
-// window rows' softmax denominator.
+// Chunked prefill (pfd_chunk_prefill, pfd_chunk_prefill_ex,
+// pfd_chunk_prefill_layers, pfd_chunk_prefill_batch): L stacked layers (or
+// requests) of N chunks (layer l's chunk j is chunk l*N + j of the stacked
+// tensors, its window rows l*W..; its slot slot_row[j] in its own pool
+// l*pool_rows rows further, or with shared_pool slot_row[l*N + j] in the
+// one pool); per_kv_head ranks per (chunk, KV head); k_win (may be null;
+// L == 1) puts the window keys into the window rows' softmax denominator.
 pfd_status prefill_impl(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
                         const pfd_bf16* q_win, int L, int N, int C, int W, int Hq, int Hkv, int D,
                         int B,
@@ -181,7 +182,7 @@ pfd_status prefill_impl(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
                         pfd_bf16* pool_k, pfd_bf16* pool_v, int64_t pool_rows,
                         const int32_t* slot_row, pfd_chunk_entry* table, int32_t* dev_err,
                         void* workspace, size_t workspace_bytes, bool per_kv_head,
-                        const pfd_bf16* k_win, pfd_stream_t stream) {
+                        const pfd_bf16* k_win, pfd_stream_t stream, bool shared_pool = false) {
   if (L < 1 || N < 1 || C < 1 || W < 0 || B < 0 || B > C) return PFD_ERR_INVALID_ARG;
   if (k_win != nullptr && L != 1) return PFD_ERR_INVALID_ARG;
   if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return PFD_ERR_INVALID_ARG;
@@ -312,6 +313,7 @@ pfd_status prefill_impl(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
   tp.dev_err = dev_err;
   tp.pool_rows = pool_rows;
   tp.layer_pool_rows = pool_rows;
+  tp.slot_per_chunk = shared_pool ? 1 : 0;
   tp.layer_chunks = N;
   tp.n_chunks = NL;
   tp.chunk_size = C;
@@ -527,6 +529,18 @@ pfd_status pfd_chunk_prefill_layers(const pfd_bf16* q, const pfd_bf16* k, const 
   return prefill_impl(q, k, v, q_win, L, N, C, W, Hq, Hkv, D, B, sm_scale, out, scores, kept_idx,
                       pool_k, pool_v, pool_rows, slot_row, table, dev_err, workspace,
                       workspace_bytes, false, nullptr, stream);
+}
+
+pfd_status pfd_chunk_prefill_batch(const pfd_bf16* q, const pfd_bf16* k, const pfd_bf16* v,
+                                   const pfd_bf16* q_win, int L, int N, int C, int W, int Hq,
+                                   int Hkv, int D, int B, float sm_scale, pfd_bf16* out,
+                                   float* scores, int32_t* kept_idx, pfd_bf16* pool_k,
+                                   pfd_bf16* pool_v, int64_t pool_rows, const int32_t* slot_row,
+                                   pfd_chunk_entry* table, int32_t* dev_err, void* workspace,
+                                   size_t workspace_bytes, pfd_stream_t stream) {
+  return prefill_impl(q, k, v, q_win, L, N, C, W, Hq, Hkv, D, B, sm_scale, out, scores, kept_idx,
+                      pool_k, pool_v, pool_rows, slot_row, table, dev_err, workspace,
+                      workspace_bytes, false, nullptr, stream, true);
 }
 
 pfd_status pfd_chunk_loglik(const pfd_bf16* logits, const int32_t* labels, int N, int R,

@@ -143,6 +143,8 @@ struct TopBParams {
                              // pool (layer_pool_rows rows further per layer) at slot
                              // slot_row[c % layer_chunks], table entries relative to it
   long long layer_pool_rows;
+  int slot_per_chunk;        // 1: chunk c's slot is slot_row[c], a row of the one pool of
+                             // pool_rows rows (a batch of requests), table rows absolute
   int per_head;              // 1: one ranking per (chunk, KV head): scores [N, Hkv, C+1],
                              // kept_idx [N, Hkv, B], head g's slot column from head g's set
 };

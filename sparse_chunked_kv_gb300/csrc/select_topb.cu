@@ -58,10 +58,12 @@ __device__ __forceinline__ void copy_kept_rows(const TopBParams& p, int j, int h
                                                int rows, const int* kept_src, int tid) {
   const int B = p.n_keep;
   // Layer of chunk j: its pool starts layer_pool_rows rows further per layer.
+  // A batch of requests shares one pool: every chunk has its own slot there.
   const int layer = j / p.layer_chunks;
-  const long long slot = p.slot_row[j % p.layer_chunks];
-  const bool slot_ok = slot >= 0 && slot + B + 1 <= p.layer_pool_rows;
-  const long long pool0 = static_cast<long long>(layer) * p.layer_pool_rows;
+  const long long slot = p.slot_row[p.slot_per_chunk ? j : j % p.layer_chunks];
+  const long long slot_limit = p.slot_per_chunk ? p.pool_rows : p.layer_pool_rows;
+  const bool slot_ok = slot >= 0 && slot + B + 1 <= slot_limit;
+  const long long pool0 = p.slot_per_chunk ? 0 : static_cast<long long>(layer) * p.layer_pool_rows;
   if (part == 0 && tid == 0 && head <= 0) {
     pfd_chunk_entry e;
     e.row = slot_ok ? static_cast<int32_t>(slot) : 0;

@@ -88,9 +88,9 @@ def _check_pool(cfg, req, kept, table, pool_k, pool_v, label, table_base):
 
 @pytest.mark.parametrize("name", ["8k", "32k", "128k", "mix"])
 def test_full_size_job(name):
-    cfgs = bench.job_configs(name)
     dev = torch.device("cuda", 0)
-    job = bench.Job(cfgs, 0, dev)
+    job = bench.Job(bench.job_configs(name), 0, dev)
+    cfgs = job.cfgs   # the job's order: sequences of one prefill shape together
     job.prefill_select()
     last = job.T - 1
     for t in (0, last):
@@ -118,7 +118,7 @@ def test_full_size_job(name):
     for t in (0, last):
         out, lse = job.dec_out[t].cpu(), job.dec_lse[t].cpu()
         for i, (c, req) in enumerate(zip(cfgs, job.host)):
-            ql, kl, vl = wl.live_block(req, wl.make_step(c, i, t))
+            ql, kl, vl = wl.live_block(req, wl.make_step(c, job.seq_ids[i], t))
             o_ref, lse_ref = orc.decode_attention(
                 f64(ql), f64(kl), f64(vl), pk, pv, tab,
                 sel_arr[job.cu_k_host[i]:job.cu_k_host[i + 1]], c.sm_scale)

@@ -75,3 +75,59 @@ def test_layers_match_single_calls_and_oracle(name):
         o_ref = orc.chunk_attention_rows(f64(req["q"]), k, v, cfg.chunk_size, pick, cfg.sm_scale)
         P.assert_close_out(res["out"][l].cpu()[pick].double().numpy(), o_ref,
                            f"{name} layer {l}: prefill rows")
+
+
+BATCH_SHAPES = {
+    "small_x3": (wl.scaled(wl.CTX_8K, n_chunks=3, chunk_size=200, n_keep=50, n_win=16), 3),
+    "d64_x2": (wl.scaled(wl.TINY, n_chunks=5, chunk_size=70, n_keep=20, n_win=12), 2),
+    "mix_c256_x3": (wl.scaled(wl.mix_configs()[0], n_chunks=16), 3),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BATCH_SHAPES))
+def test_batch_matches_single_calls_into_one_pool(name):
+    """pfd_chunk_prefill_batch: L same-shaped requests, each with its own
+    permuted slots in one shared pool (request l's slots offset by l pools
+    and reversed for odd l), against L pfd_chunk_prefill calls into the same
+    pool: every output, the whole pool and the table, bit for bit, and the
+    scores and kept sets against the oracle."""
+    cfg, n_req = BATCH_SHAPES[name]
+    reqs = [wl.make_request(cfg, seq) for seq in range(n_req)]
+    slots = []
+    for l, r in enumerate(reqs):
+        s = r["slot_row"].clone() if l % 2 == 0 else r["slot_row"].flip(0).clone()
+        slots.append(s + l * cfg.pool_rows)
+    pool_rows = n_req * cfg.pool_rows
+    stack = lambda key: P.cuda(torch.stack([r[key] for r in reqs]))  # noqa: E731
+    slot_b = P.cuda(torch.stack(slots).to(torch.int32))
+    hkv, d = cfg.n_kv_heads, cfg.head_dim
+    pk_b = torch.zeros(pool_rows, hkv, d, dtype=torch.bfloat16, device="cuda")
+    pv_b = torch.zeros_like(pk_b)
+    tab_b = torch.zeros(n_req, cfg.n_chunks, 2, dtype=torch.int32, device="cuda")
+    res = api.chunk_prefill_batch(stack("q"), stack("k"), stack("v"), stack("q_win"),
+                                  cfg.n_chunks, cfg.chunk_size, cfg.n_keep, slot_b, pk_b, pv_b,
+                                  tab_b)
+    torch.cuda.synchronize()
+    assert int(res["dev_err"].item()) == 0
+    pk_s, pv_s = torch.zeros_like(pk_b), torch.zeros_like(pv_b)
+    for l, r in enumerate(reqs):
+        single = api.chunk_prefill(P.cuda(r["q"]), P.cuda(r["k"]), P.cuda(r["v"]),
+                                   P.cuda(r["q_win"]), cfg.n_chunks, cfg.chunk_size, cfg.n_keep,
+                                   P.cuda(slots[l].to(torch.int32)), pool_rows)
+        torch.cuda.synchronize()
+        assert int(single["dev_err"].item()) == 0
+        for key in ("out", "scores", "kept_idx"):
+            assert torch.equal(res[key][l], single[key]), f"{name} request {l}: {key} differs"
+        assert torch.equal(tab_b[l], single["table"]), f"{name} request {l}: table differs"
+        for j in range(cfg.n_chunks):
+            base = int(slots[l][j])
+            n = cfg.n_keep + 1
+            pk_s[base:base + n] = single["pool_k"][base:base + n]
+            pv_s[base:base + n] = single["pool_v"][base:base + n]
+        s_ref = orc.window_scores(f64(r["q_win"]), f64(r["k"]), cfg.n_chunks, cfg.chunk_size,
+                                  cfg.sm_scale)
+        s_gpu = res["scores"][l].cpu().double().numpy()
+        assert (np.abs(s_gpu - s_ref) <= P.score_tol(s_ref, cfg.n_win, cfg.n_q_heads)).all()
+        P.check_kept(res["kept_idx"][l].cpu().numpy(), s_ref, cfg.n_keep)
+    assert torch.equal(pk_b.view(torch.int16), pk_s.view(torch.int16)), f"{name}: pool_k"
+    assert torch.equal(pv_b.view(torch.int16), pv_s.view(torch.int16)), f"{name}: pool_v"
