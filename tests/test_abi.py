@@ -72,6 +72,28 @@ def test_prefill_host_checks(lib, over, status):
     assert _prefill_status(lib, **over) == status
 
 
+def _prefill_batch_status(lib, L=2, **over):
+    a = dict(q=256, k=256, v=256, q_win=256, N=2, C=16, W=4, Hq=4, Hkv=2, D=64, B=4, scale=0.0,
+             out=256, scores=256, kept=256, pk=256, pv=256, pool_rows=20, slot=256, table=256,
+             err=0, ws=256, ws_bytes=1 << 20, stream=0)
+    a.update(over)
+    return lib.pfd_chunk_prefill_batch(a["q"], a["k"], a["v"], a["q_win"], L, a["N"], a["C"],
+                                       a["W"], a["Hq"], a["Hkv"], a["D"], a["B"], a["scale"],
+                                       a["out"], a["scores"], a["kept"], a["pk"], a["pv"],
+                                       a["pool_rows"], a["slot"], a["table"], a["err"] or None,
+                                       a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("L,over,status", [
+    (0, {}, 1), (2, dict(N=0), 1), (2, dict(B=17), 1), (2, dict(D=96), 2), (2, dict(slot=0), 1),
+    (2, dict(table=0), 1), (2, dict(q_win=0), 1), (2, dict(ws_bytes=0), 1), (2, dict(q=12), 1),
+])
+def test_prefill_batch_host_checks(lib, L, over, status):
+    """The batched prefill refuses bad arguments on the host, before any
+    launch, with the same codes as the single-request call."""
+    assert _prefill_batch_status(lib, L, **over) == status
+
+
 def test_prefill_workspace_sizes(lib):
     small = lib.pfd_chunk_prefill_workspace(2, 16, 4, 4, 2, 64, 4)
     none = lib.pfd_chunk_prefill_workspace(2, 16, 0, 4, 2, 64, 4)
