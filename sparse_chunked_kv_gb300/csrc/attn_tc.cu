@@ -569,6 +569,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         const bool with_pv = it.kind != kWindow && it.kind != kMass;
         const int nx = it.has_b ? 2 : 1;
         bool ofree_done[2] = {items_done == 0, items_done == 0};
+        bool ofull_sent[2] = {false, false};
         auto wait_ofree = [&](int x) -> bool {
           if (ofree_done[x]) return true;
           ofree_done[x] = true;
@@ -671,6 +672,12 @@ attention_kernel(const __grid_constant__ AttnParams p) {
               if (with_pv) {
                 if (j == 0 && !wait_ofree(x)) { ok = false; break; }
                 issue_pv(x, ng, vs, j == 0);
+                if (last) {
+                  // O_x is final once this PV completes: its epilogue need
+                  // not wait for the other tile's last PV.
+                  mma_commit(&sh.o_full[x]);
+                  ofull_sent[x] = true;
+                }
               }
               if (!last) {
                 if (x == 0 && !mbar_wait(&sh.ring_full[ks_next], (ring_ctr / kRing) & 1)) {
@@ -696,9 +703,11 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         for (int x = 0; ok && x < 2; ++x)
           if (!wait_ofree(x)) ok = false;
         if (!ok) break;
-        // O_x of this item is final once every MMA issued so far completes.
-        mma_commit(&sh.o_full[0]);
-        mma_commit(&sh.o_full[1]);
+        // O_x of this item is final once every MMA issued so far completes
+        // (one o_full phase per tile and item, committed early above after
+        // the tile's last PV).
+        for (int x = 0; x < 2; ++x)
+          if (!ofull_sent[x]) mma_commit(&sh.o_full[x]);
         mma_commit(&sh.q_empty);
         ++items_done;
       }
