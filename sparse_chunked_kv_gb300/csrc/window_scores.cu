@@ -24,20 +24,22 @@
 // halves in TMEM so the tensor core computes one half while the warps
 // exponentiate the other.
 //   warp 0      TMA loads and the single-thread MMA issuer;
-//   warps 1..8  two warps per TMEM lane quarter (one thread per key row), each
-//               taking alternate 32-column pieces of every half.
+//   warps 1..16 four warps per TMEM lane quarter (one thread per key row), each
+//               taking every fourth 32-column piece of every half; their four
+//               partial sums are added in a fixed order.
 #include "pfd_internal.cuh"
 #include "sm103_ptx.cuh"
 
 namespace pfd {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
+constexpr int kSubs = kConsumerWarps / 4;        // consumer warps per lane quarter
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr uint32_t kPanelBytes = 128u * 128u;   // a 128-row, 64-column K panel
 constexpr int kMaxWindowRows = 512;
-constexpr uint32_t kConsumerBarrier = 1;         // named barrier of warps 1..8
+constexpr uint32_t kConsumerBarrier = 1;         // named barrier of warps 1..16
 
 // Rows [row0, row0 + nrows) of the concatenated chunks, starting in chunk c0.
 struct Tile {
@@ -70,7 +72,7 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
   __shared__ uint32_t tmem_base;
   __shared__ int failed;
   __shared__ __align__(16) float b_sh[2][2][kMaxWindowRows];   // [item parity][chunk of tile][column]
-  __shared__ float red[2][128];                                // second warp's partial per key row
+  __shared__ float red[2][kSubs - 1][128];   // partials of warps sub = 1.. per key row
 
   grid_dependency_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -194,7 +196,7 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
     }
   } else {
     const int quarter = warp & 3;
-    const int sub = (warp - 1) >> 2;   // 0 for warps 1..4, 1 for warps 5..8
+    const int sub = (warp - 1) >> 2;   // 0 for warps 1..4, 1 for warps 5..8, ...
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
@@ -225,7 +227,7 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
         if (ok && !mbar_wait_warp(&s_full[hf], k & 1)) ok = false;
         tc_fence_after_sync();
         if (ok) {
-          for (int pc = sub; pc < pieces; pc += 2) {
+          for (int pc = sub; pc < pieces; pc += kSubs) {
             const int c0 = hf * half + pc * 32;
             uint32_t s[32];
             tmem_ld32(lane_base + c0, s);
@@ -252,12 +254,14 @@ window_score_kernel(const __grid_constant__ WinScoreParams p) {
       f2_unpack(acc2, a0, a1);
       const float acc = a0 + a1;
       if (i_next < n_items) cp_async_wait_all();
-      if (sub == 1) red[k & 1][row] = acc;
+      if (sub > 0) red[k & 1][sub - 1][row] = acc;
       named_barrier_sync(kConsumerBarrier, kConsumers);
       if (sub == 0 && row < t.nrows && c_row < p.n_chunks) {
         const int tt = static_cast<int>(r - static_cast<long long>(c_row) * p.chunk_rows);
-        p.part_scores[((layer_chunk0 + c_row) * p.Hkv + g) * p.chunk_rows + tt] =
-            acc + red[k & 1][row];
+        float total = acc;
+#pragma unroll
+        for (int u = 0; u < kSubs - 1; ++u) total += red[k & 1][u][row];
+        p.part_scores[((layer_chunk0 + c_row) * p.Hkv + g) * p.chunk_rows + tt] = total;
       }
     }
     if (!ok) atomicOr(&failed, 2);
