@@ -19,11 +19,17 @@
 namespace pfd {
 namespace {
 
-constexpr int kTopBThreads = 1024;
-constexpr int kMaxPerThread = 8;   // C <= 8192
+// Threads of a top-B CTA: 256 for chunks of up to 2048 tokens (more CTAs
+// resident per SM, more copy splits per chunk), 1024 up to 8192.
+constexpr int kTopBThreadsSmall = 256;
+constexpr int kTopBThreadsLarge = 1024;
+constexpr int kMaxPerThread = 8;   // C <= 8 * threads
 
-// Block-wide exclusive prefix sum of one value per thread (1024 threads).
+// Block-wide exclusive prefix sum of one value per thread (kThreads threads,
+// at most 32 warps).
+template <int kThreads>
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
+  constexpr int kWarps = kThreads / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
 #pragma unroll
@@ -34,14 +40,14 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int& 
   if (lane == 31) warp_sums[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = warp_sums[lane];
+    int w = lane < kWarps ? warp_sums[lane] : 0;
     int wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xFFFFFFFFu, wi, o);
       if (lane >= o) wi += y;
     }
-    warp_sums[lane] = wi - w;       // exclusive warp offsets
+    if (lane < kWarps) warp_sums[lane] = wi - w;   // exclusive warp offsets
     if (lane == 31) warp_sums[32] = wi;
   }
   __syncthreads();
@@ -54,6 +60,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int& 
 // 4. Chunk table and the copy of BOS + kept rows (kept_src, slot order) into
 // chunk j's pool slot; CTA `part` of copy_splits copies its share of the rows.
 // Per-head ranking (head >= 0): only KV head `head`'s columns of the rows.
+template <int kThreads>
 __device__ __forceinline__ void copy_kept_rows(const TopBParams& p, int j, int head, int part,
                                                int rows, const int* kept_src, int tid) {
   const int B = p.n_keep;
@@ -79,7 +86,7 @@ __device__ __forceinline__ void copy_kept_rows(const TopBParams& p, int j, int h
   const int units = head < 0 ? row_units : p.D / 8;   // units copied per row
   const int u0 = head < 0 ? 0 : head * (p.D / 8);     // first unit copied
   const long long chunk_row0 = static_cast<long long>(j) * rows;
-  for (int idx = tid; idx < (r1 - r0) * units; idx += kTopBThreads) {
+  for (int idx = tid; idx < (r1 - r0) * units; idx += kThreads) {
     const int r = r0 + idx / units, u = u0 + idx % units;
     const long long src = (chunk_row0 + kept_src[r]) * row_units + u;
     const long long dst = (pool0 + slot + r) * row_units + u;
@@ -88,7 +95,8 @@ __device__ __forceinline__ void copy_kept_rows(const TopBParams& p, int j, int h
   }
 }
 
-__global__ void __launch_bounds__(kTopBThreads)
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads)
 topb_compact_kernel(const TopBParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t hist[256];
@@ -111,7 +119,7 @@ topb_compact_kernel(const TopBParams p) {
 
   // 1. Scores: fixed-order sum of the Hkv partial column sums (per-head
   // ranking: that head's partial alone).
-  for (int t = tid; t < rows; t += kTopBThreads) {
+  for (int t = tid; t < rows; t += kThreads) {
     float s = 0.0f;
     if (p.part_scores != nullptr) {
       if (head >= 0) {
@@ -128,7 +136,7 @@ topb_compact_kernel(const TopBParams p) {
   __syncthreads();
 
   // 2. Threshold key T (the B-th largest) and how many keys equal to T to keep.
-  const int per = (C + kTopBThreads - 1) / kTopBThreads;
+  const int per = (C + kThreads - 1) / kThreads;
   const int i0 = tid * per;
   uint32_t key[kMaxPerThread];
 #pragma unroll
@@ -198,7 +206,7 @@ topb_compact_kernel(const TopBParams p) {
 #pragma unroll
     for (int u = 0; u < kMaxPerThread; ++u)
       if (u < per && i0 + u < C && key[u] == thr) ++n_eq;
-    eq_base = block_exclusive_scan(n_eq, warp_sums, total);
+    eq_base = block_exclusive_scan<kThreads>(n_eq, warp_sums, total);
   }
   uint32_t kept_mask = 0u;
   int n_kept = 0, eq_seen = 0;
@@ -216,7 +224,7 @@ topb_compact_kernel(const TopBParams p) {
       ++n_kept;
     }
   }
-  int pos = block_exclusive_scan(n_kept, warp_sums, total);
+  int pos = block_exclusive_scan<kThreads>(n_kept, warp_sums, total);
 #pragma unroll
   for (int u = 0; u < kMaxPerThread; ++u) {
     if (kept_mask & (1u << u)) {
@@ -227,7 +235,7 @@ topb_compact_kernel(const TopBParams p) {
   }
   __syncthreads();
 
-  copy_kept_rows(p, j, head, part, rows, kept_src, tid);
+  copy_kept_rows<kThreads>(p, j, head, part, rows, kept_src, tid);
 }
 
 constexpr int kSelectThreads = 1024;
@@ -276,27 +284,34 @@ select_kernel(const float* __restrict__ s_i, const float* __restrict__ s_p,
 
 // Launches (n_chunks x copy_splits) CTAs, with copy_splits chosen here from
 // the kernel's occupancy so that the grid is about one resident wave.
-cudaError_t launch_topb_compact(const TopBParams& params, cudaStream_t stream) {
-  TopBParams p = params;
-  int dev = 0, sm_count = 1;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sm_count = 1;
+template <int kThreads>
+cudaError_t launch_topb_compact_t(TopBParams p, int sm_count, cudaStream_t stream) {
   const int rows = p.chunk_size + 1;
   const size_t smem = static_cast<size_t>((rows * 4 + 15) & ~15) + static_cast<size_t>(p.n_keep + 1) * 4;
-  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(topb_compact_kernel), static_cast<int>(smem));
+  const void* fn = reinterpret_cast<const void*>(topb_compact_kernel<kThreads>);
+  cudaError_t err = ensure_smem_limit(fn, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   // Every CTA of a chunk redoes the selection and copies a share of its rows
   // (at least 16 rows each): as many CTAs per chunk as one resident wave holds.
   int per_sm = 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topb_compact_kernel, kTopBThreads,
-                                                    smem) != cudaSuccess || per_sm < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topb_compact_kernel<kThreads>,
+                                                    kThreads, smem) != cudaSuccess || per_sm < 1)
     per_sm = 1;
   const int wave = std::max(sm_count, 1) * per_sm;
   const int units = p.n_chunks * (p.per_head ? p.Hkv : 1);   // rankings
   p.copy_splits = std::max(1, std::min(wave / std::max(units, 1), std::max(1, (p.n_keep + 1) / 16)));
   dim3 grid(units, p.copy_splits);
-  return launch_pdl(topb_compact_kernel, grid, dim3(kTopBThreads), smem, stream, p);
+  return launch_pdl(topb_compact_kernel<kThreads>, grid, dim3(kThreads), smem, stream, p);
+}
+
+cudaError_t launch_topb_compact(const TopBParams& params, cudaStream_t stream) {
+  int dev = 0, sm_count = 1;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sm_count = 1;
+  if (params.chunk_size <= kMaxPerThread * kTopBThreadsSmall)
+    return launch_topb_compact_t<kTopBThreadsSmall>(params, sm_count, stream);
+  return launch_topb_compact_t<kTopBThreadsLarge>(params, sm_count, stream);
 }
 
 cudaError_t launch_select(const float* s_i, const float* s_p, const int32_t* cu_n,
