@@ -88,7 +88,9 @@ struct TileMeta {
   int32_t ngroups;     // 0 only for the single tile of an empty item
   int32_t last;        // 1 on the last tile of an item
   int32_t fix_v;       // 1 when a group is ragged and unshifted: its V rows
-                       // past the segment must be zeroed before PV
+                       // past the segment must be zeroed before PV.  Chunk-mass
+                       // items (no PV): the segment (chunk of the item) of
+                       // group g in bits [4g, 4g + 4)
 };
 
 struct Shared {
@@ -149,10 +151,12 @@ __device__ __forceinline__ bool resolve_item(const AttnParams& p, int idx, Item&
     it.ta = 2 * (local % pairs);
     const int rest = local / pairs;
     it.g = rest % p.Hkv;
-    it.chunk = p.mass_n0[b] + rest / p.Hkv;   // table index
+    // the item's chunks: table entries [k0, k1), at most mass_chunks
+    it.k0 = p.mass_n0[b] + (rest / p.Hkv) * p.mass_chunks;
+    it.k1 = min(it.k0 + p.mass_chunks, p.mass_n0[b + 1]);
+    it.chunk = it.k0;
     it.q_map = 0;
     it.split = 0;
-    it.k0 = it.k1 = 0;
     const int lq0 = p.cu_lq[b], lq1 = p.cu_lq[b + 1];
     if (lq0 < 0 || lq1 < lq0 || lq1 > p.total_lq) return false;   // reported by the producer
     it.q_row0 = lq0;
@@ -264,13 +268,14 @@ __device__ __forceinline__ int load_segments(const AttnParams& p, const Item& it
   int nseg;
   __syncwarp();
   if (it.kind == kMass) {
-    nseg = 1;
-    if (lane == 0) {
-      const pfd_chunk_entry e = p.table[it.chunk];
+    // one segment per chunk of the item, in table order
+    nseg = it.k1 - it.k0;
+    for (int i = lane; i < nseg; i += 32) {
+      const pfd_chunk_entry e = p.table[it.k0 + i];
       const bool bad = e.row < 0 || e.len < 0 || static_cast<long long>(e.row) + e.len > p.pool_rows;
       if (bad) raise_dev_err(p.dev_err, PFD_DEVERR_TABLE);
-      seg_row[0] = bad ? 0 : e.row;
-      seg_len[0] = bad ? 0 : e.len;
+      seg_row[i] = bad ? 0 : e.row;
+      seg_len[i] = bad ? 0 : e.len;
     }
   } else if (it.kind != kDecode) {
     nseg = 1;
@@ -330,8 +335,10 @@ struct RowState {
 
 // kPrefill: a prefill launch (chunk and window items, with the analytic BOS
 // key); else a decode launch, compiled without that code.  kMassMode: a
-// chunk-mass launch (decode-shaped, mass items only).
-template <int D, bool kPrefill, bool kMassMode>
+// chunk-mass launch (decode-shaped, mass items only); kMassMulti: its items
+// hold several chunks each, with per-chunk sums (one chunk per item needs
+// only the row sum).
+template <int D, bool kPrefill, bool kMassMode, bool kMassMulti>
 __global__ void __launch_bounds__(kThreads, 1)
 attention_kernel(const __grid_constant__ AttnParams p) {
   using L = Layout<D>;
@@ -455,6 +462,14 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         const uint32_t nv_lo = __shfl_sync(0xFFFFFFFFu, packed, 0);
         const uint32_t nv_hi = __shfl_sync(0xFFFFFFFFu, packed, 4);
         const bool fix_v = __any_sync(0xFFFFFFFFu, lane < ng && code < kGroupRows);
+        uint32_t seg4 = 0;
+        if constexpr (kMassMulti) {
+          seg4 = lane < ng ? static_cast<uint32_t>(lseg & 0xF) << (4 * lane) : 0u;
+          seg4 |= __shfl_xor_sync(0xFFFFFFFFu, seg4, 1);
+          seg4 |= __shfl_xor_sync(0xFFFFFFFFu, seg4, 2);
+          seg4 |= __shfl_xor_sync(0xFFFFFFFFu, seg4, 4);
+          seg4 = __shfl_sync(0xFFFFFFFFu, seg4, 0);
+        }
         // Runs: group k continues group k-1's run when it is the next 16 rows
         // of the same tensor.  A lane that starts a run loads the whole run,
         // one box per set bit of its length (16..128 rows).
@@ -478,7 +493,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
           m.nvalid_hi = nv_hi;
           m.ngroups = ng;
           m.last = (j == tiles_to_publish - 1) ? 1 : 0;
-          m.fix_v = fix_v ? 1 : 0;
+          m.fix_v = kMassMode ? static_cast<int32_t>(seg4) : (fix_v ? 1 : 0);
           mbar_arrive(&sh.meta_full[ms]);
         }
         ++tile_ctr;
@@ -732,6 +747,11 @@ attention_kernel(const __grid_constant__ AttnParams p) {
       const bool with_pv = it.kind != kWindow && it.kind != kMass;
       const bool active = x == 0 || it.has_b;
       float m_used = -INFINITY, l_sum = 0.0f;
+      // Chunk-mass items: this row's probability mass in each of the item's
+      // chunks (segments), accumulated group by group.
+      float seg_mass[kMassChunks];
+#pragma unroll
+      for (int c = 0; c < kMassChunks; ++c) seg_mass[c] = 0.0f;
       if constexpr (kMassMode) {
         // Mass items: every probability is taken at the step's normaliser,
         // p = 2^(s * scale - lse * log2(e)), so the row's reference is its
@@ -887,6 +907,8 @@ attention_kernel(const __grid_constant__ AttnParams p) {
             const float neg_m = -m_used;
             const uint64_t scale2 = f2_pack(scale, scale), neg_m2 = f2_pack(neg_m, neg_m);
             uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+            uint64_t gsum2[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f),
+                                 f2_pack(0.f, 0.f)};   // mass items: per 16-key group
             uint32_t packed[32];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
@@ -897,10 +919,29 @@ attention_kernel(const __grid_constant__ AttnParams p) {
                                scale2, neg_m2), xb0, xb1);
               const float a0 = ex2_approx(xa0), a1 = ex2_approx(xa1);
               const float b0 = ex2_approx(xb0), b1 = ex2_approx(xb1);
-              sum2[0] = f2_add(sum2[0], f2_pack(a0, a1));
-              sum2[1] = f2_add(sum2[1], f2_pack(b0, b1));
-              packed[i >> 1] = pack_bf16x2(a0, a1);
-              packed[16 + (i >> 1)] = pack_bf16x2(b0, b1);
+              if constexpr (kMassMulti) {
+                gsum2[i >> 4] = f2_add(gsum2[i >> 4], f2_pack(a0, a1));
+                gsum2[2 + (i >> 4)] = f2_add(gsum2[2 + (i >> 4)], f2_pack(b0, b1));
+              } else {
+                sum2[0] = f2_add(sum2[0], f2_pack(a0, a1));
+                sum2[1] = f2_add(sum2[1], f2_pack(b0, b1));
+                packed[i >> 1] = pack_bf16x2(a0, a1);
+                packed[16 + (i >> 1)] = pack_bf16x2(b0, b1);
+              }
+            }
+            if constexpr (kMassMulti) {
+              // Each group's sum goes to its chunk (segment) of the item.
+#pragma unroll
+              for (int gq = 0; gq < 4; ++gq) {
+                float g0, g1;
+                f2_unpack(gsum2[gq], g0, g1);
+                const float gs = g0 + g1;
+                const uint32_t seg =
+                    (static_cast<uint32_t>(meta.fix_v) >> (4 * (half * 4 + gq))) & 0xFu;
+#pragma unroll
+                for (int c = 0; c < kMassChunks; ++c)
+                  seg_mass[c] += seg == static_cast<uint32_t>(c) ? gs : 0.0f;
+              }
             }
             if (with_pv) tmem_st32(lane_base + s_col + half * 32, packed);
             float sum[4];
@@ -941,15 +982,32 @@ attention_kernel(const __grid_constant__ AttnParams p) {
         m_used = m_new;
       }
       if constexpr (kMassMode) {
-        // This warp's rows' mass over the chunk: one partial per (item, query
-        // tile, warp), summed per chunk in a fixed order by the mass-sum
-        // kernel.
+        // This warp's rows' mass over each chunk of the item (its row sum
+        // when the item holds one chunk): one partial per (item, chunk,
+        // query tile, warp), summed per chunk in a fixed order by the
+        // mass-sum kernel.
         const int t_local = row / G;
         const int t = (it.ta + x) * p.Tq + t_local;
-        float v = (active && row < q_rows && t < it.n_t) ? l_sum : 0.0f;
+        const bool row_in = active && row < q_rows && t < it.n_t;
+        if constexpr (kMassMulti) {
+          const int nchunks = it.k1 - it.k0;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-        if (lane == 0) p.mass_part[static_cast<long long>(idx) * 8 + x * 4 + quarter] = v;
+          for (int c = 0; c < kMassChunks; ++c) {
+            if (c < nchunks) {
+              float v = row_in ? seg_mass[c] : 0.0f;
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+              if (lane == 0)
+                p.mass_part[(static_cast<long long>(idx) * p.mass_chunks + c) * 8 + x * 4 +
+                            quarter] = v;
+            }
+          }
+        } else {
+          float v = row_in ? l_sum : 0.0f;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+          if (lane == 0) p.mass_part[static_cast<long long>(idx) * 8 + x * 4 + quarter] = v;
+        }
       }
       if (!kMassMode && active) {
         const int t_local = row / G;
@@ -1080,23 +1138,27 @@ size_t attention_smem_bytes(int D, bool prefill) {
   return 1024 + (prefill ? Layout<128>::kTotalPrefill : Layout<128>::kTotalDecode);
 }
 
-template <int D, bool kPrefill, bool kMassMode>
+template <int D, bool kPrefill, bool kMassMode, bool kMassMulti = false>
 cudaError_t launch_attention_t(const AttnParams& p, int grid, size_t smem, cudaStream_t stream) {
   const cudaError_t err = ensure_smem_limit(
-      reinterpret_cast<const void*>(attention_kernel<D, kPrefill, kMassMode>),
+      reinterpret_cast<const void*>(attention_kernel<D, kPrefill, kMassMode, kMassMulti>),
       static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  return launch_pdl(attention_kernel<D, kPrefill, kMassMode>, dim3(grid), dim3(kThreads), smem,
-                    stream, p);
+  return launch_pdl(attention_kernel<D, kPrefill, kMassMode, kMassMulti>, dim3(grid),
+                    dim3(kThreads), smem, stream, p);
 }
 
 cudaError_t launch_attention(const AttnParams& p, int grid, cudaStream_t stream) {
   if (grid <= 0 || p.n_items <= 0) return cudaSuccess;
   const bool prefill = p.mode == kModePrefill;
   const size_t smem = attention_smem_bytes(p.D, prefill);
-  if (p.mode == kModeMass)
+  if (p.mode == kModeMass) {
+    if (p.mass_chunks > 1)
+      return p.D == 64 ? launch_attention_t<64, false, true, true>(p, grid, smem, stream)
+                       : launch_attention_t<128, false, true, true>(p, grid, smem, stream);
     return p.D == 64 ? launch_attention_t<64, false, true>(p, grid, smem, stream)
                      : launch_attention_t<128, false, true>(p, grid, smem, stream);
+  }
   if (p.D == 64)
     return prefill ? launch_attention_t<64, true, false>(p, grid, smem, stream)
                    : launch_attention_t<64, false, false>(p, grid, smem, stream);

@@ -251,6 +251,7 @@ struct MassSumParams {
   const float* part;
   float* mass;
   int batch, Hkv;
+  int chunks_per_item;                 // consecutive chunks of one item
   int chunk_base[kMaxMassBatch + 1];   // prefix of the sequences' chunk counts
   int n0[kMaxMassBatch];
   int item0[kMaxMassBatch];
@@ -267,10 +268,18 @@ __global__ void __launch_bounds__(128) mass_sum_kernel(const __grid_constant__ M
   int b = 0;
   while (b + 1 < p.batch && p.chunk_base[b + 1] <= i) ++b;
   const int c = i - p.chunk_base[b];
-  const int n_vals = p.Hkv * p.pairs[b] * 8;
-  const float* src = p.part + (static_cast<long long>(p.item0[b]) + static_cast<long long>(c) * p.Hkv * p.pairs[b]) * 8;
+  // Chunk c of sequence b is chunk s of chunk group cg; the items of that
+  // group (KV head x pair of query tiles) each hold 8 partials for it.
+  const int M = p.chunks_per_item;
+  const int cg = c / M, s = c % M;
+  const int n_items = p.Hkv * p.pairs[b];
+  const float* src = p.part +
+                     (static_cast<long long>(p.item0[b]) + static_cast<long long>(cg) * n_items) *
+                         M * 8 +
+                     s * 8;
   float acc = 0.0f;
-  for (int k = lane; k < n_vals; k += 32) acc += src[k];
+  for (int k = lane; k < n_items * 8; k += 32)
+    acc += src[static_cast<long long>(k >> 3) * M * 8 + (k & 7)];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
   if (lane == 0) p.mass[p.n0[b] + c] = acc * p.inv_rows[b];
@@ -286,11 +295,11 @@ cudaError_t launch_mass_sum(const AttnParams& ap, const int32_t* cu_lq_host, int
   p.mass = mass;
   p.batch = ap.mass_batch;
   p.Hkv = ap.Hkv;
+  p.chunks_per_item = ap.mass_chunks;
   p.chunk_base[0] = 0;
   for (int b = 0; b < ap.mass_batch; ++b) {
-    const int n_b = (ap.mass_pairs[b] > 0 && ap.Hkv > 0)
-                        ? (ap.mass_item0[b + 1] - ap.mass_item0[b]) / (ap.Hkv * ap.mass_pairs[b])
-                        : 0;
+    // a sequence without query rows has no items, and its chunks no mass
+    const int n_b = ap.mass_pairs[b] > 0 ? ap.mass_n0[b + 1] - ap.mass_n0[b] : 0;
     p.chunk_base[b + 1] = p.chunk_base[b] + n_b;
     p.n0[b] = ap.mass_n0[b];
     p.item0[b] = ap.mass_item0[b];

@@ -659,7 +659,9 @@ struct MassPlan {
   int batch = 0;
   int item0[kMaxMassBatch + 1];
   int n0[kMaxMassBatch];
+  int n1[kMaxMassBatch];
   int pairs[kMaxMassBatch];
+  int chunks_per_item = 1;
   long long items = 0;
   int chunks = 0;
 };
@@ -671,14 +673,31 @@ bool mass_plan(int batch, const int32_t* cu_lq_host, const int32_t* cu_n_host, i
   if (cu_lq_host[0] != 0 || cu_n_host[0] != 0) return false;
   const int Tq = kBlockM / (Hq / Hkv);
   mp->batch = batch;
-  long long items = 0;
   for (int b = 0; b < batch; ++b) {
     const int lq = cu_lq_host[b + 1] - cu_lq_host[b], n = cu_n_host[b + 1] - cu_n_host[b];
     if (lq < 0 || n < 0) return false;
-    mp->item0[b] = static_cast<int>(items);
     mp->n0[b] = cu_n_host[b];
+    mp->n1[b] = cu_n_host[b + 1];
     mp->pairs[b] = (ceil_div(lq, Tq) + 1) / 2;
-    items += static_cast<long long>(n) * Hkv * mp->pairs[b];
+  }
+  // One item per (group of M consecutive chunks, KV head, pair of query
+  // tiles): the largest M <= kMassChunks that still leaves kMassMinItems
+  // items (short items are mostly start and end; too few leave SMs idle).
+  // The choice depends only on the shapes, so the workspace size does too.
+  constexpr long long kMassMinItems = 512;
+  auto items_for = [&](int M) {
+    long long items = 0;
+    for (int b = 0; b < batch; ++b)
+      items += static_cast<long long>(ceil_div(mp->n1[b] - mp->n0[b], M)) * Hkv * mp->pairs[b];
+    return items;
+  };
+  int M = kMassChunks;
+  while (M > 1 && items_for(M) < kMassMinItems) M >>= 1;
+  mp->chunks_per_item = M;
+  long long items = 0;
+  for (int b = 0; b < batch; ++b) {
+    mp->item0[b] = static_cast<int>(items);
+    items += static_cast<long long>(ceil_div(mp->n1[b] - mp->n0[b], M)) * Hkv * mp->pairs[b];
     if (items >= (1ll << 31)) return false;
   }
   mp->item0[batch] = static_cast<int>(items);
@@ -695,7 +714,7 @@ size_t pfd_chunk_mass_workspace(int batch, const int32_t* cu_lq_host, const int3
                                 int Hq, int Hkv) {
   MassPlan mp;
   if (!mass_plan(batch, cu_lq_host, cu_n_host, Hq, Hkv, &mp)) return 0;
-  return align256(static_cast<size_t>(mp.items) * 8 * sizeof(float));
+  return align256(static_cast<size_t>(mp.items) * mp.chunks_per_item * 8 * sizeof(float));
 }
 
 pfd_status pfd_chunk_mass(const pfd_bf16* q, const int32_t* cu_lq, const int32_t* cu_lq_host,
@@ -713,7 +732,8 @@ pfd_status pfd_chunk_mass(const pfd_bf16* q, const int32_t* cu_lq, const int32_t
     return PFD_ERR_INVALID_ARG;
   if (pool_rows >= (1ll << 31)) return PFD_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(pool_k)) return PFD_ERR_INVALID_ARG;
-  const size_t need = align256(static_cast<size_t>(mp.items) * 8 * sizeof(float));
+  const size_t need =
+      align256(static_cast<size_t>(mp.items) * mp.chunks_per_item * 8 * sizeof(float));
   if (workspace_bytes < need || (need > 0 && workspace == nullptr) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return PFD_ERR_INVALID_ARG;
@@ -749,12 +769,14 @@ pfd_status pfd_chunk_mass(const pfd_bf16* q, const int32_t* cu_lq, const int32_t
   ap.scale_log2 = scale * kLog2e;
   ap.mass_lse = lse;
   ap.mass_part = static_cast<float*>(workspace);
+  ap.mass_chunks = mp.chunks_per_item;
   ap.mass_batch = batch;
   for (int b = 0; b <= batch; ++b) ap.mass_item0[b] = mp.item0[b];
   for (int b = 0; b < batch; ++b) {
     ap.mass_n0[b] = mp.n0[b];
     ap.mass_pairs[b] = mp.pairs[b];
   }
+  ap.mass_n0[batch] = mp.n1[batch - 1];
   ap.n_items = static_cast<int>(mp.items);
   const int grid = static_cast<int>(std::min<long long>(mp.items, device_sm_count()));
   pfd_status s = from_cuda(launch_attention(ap, grid, st));

@@ -33,6 +33,7 @@ constexpr int kMaxSegments = 512;   // selected chunks per sequence + the live b
 
 enum AttnMode : int { kModePrefill = 0, kModeDecode = 1, kModeMass = 2 };
 constexpr int kMaxMassBatch = 64;   // sequences of one chunk-mass call
+constexpr int kMassChunks = 8;      // most consecutive chunks of one chunk-mass item
 
 struct AttnParams {
   // Query tensors addressed by TMA: index 0 = prefill chunk rows or decode
@@ -89,13 +90,16 @@ struct AttnParams {
   int out_v8;           // out is 32-byte aligned: whole-sector (32-byte) stores
 
   // chunk mass (kModeMass): items of sequence b are mass_item0[b] ..
-  // mass_item0[b+1]-1, item = (chunk c * Hkv + g) * mass_pairs[b] + pair, the
-  // chunk being table entry mass_n0[b] + c
+  // mass_item0[b+1]-1, item = (chunk group cg * Hkv + g) * mass_pairs[b] +
+  // pair; chunk group cg holds table entries mass_n0[b] + cg * mass_chunks ..
+  // (at most mass_chunks <= kMassChunks of them, ending before mass_n0[b + 1])
   const float* mass_lse;   // [total_lq, Hq] the step's decode log-sum-exp (natural log)
-  float* mass_part;        // [n_items, 8] partial sums (two query tiles x four warps)
+  float* mass_part;        // [n_items, mass_chunks, 8] partial sums per chunk of the item
+                           // (two query tiles x four warps)
+  int mass_chunks;
   int mass_batch;
   int mass_item0[kMaxMassBatch + 1];
-  int mass_n0[kMaxMassBatch];
+  int mass_n0[kMaxMassBatch + 1];
   int mass_pairs[kMaxMassBatch];
 };
 

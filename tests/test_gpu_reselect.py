@@ -96,6 +96,10 @@ CASES = {
     "small_d64": [wl.scaled(wl.TINY, n_chunks=6, chunk_size=100, n_keep=30, n_select=3,
                             n_win=8, n_resp=20)],
     "128k": [wl.CTX_128K],
+    # many small chunks: several chunks per mass item (four, the last group
+    # partial) on the D = 64 kernel, with ragged slots of 7 rows
+    "d64_many": [wl.scaled(wl.TINY, n_chunks=1102, chunk_size=24, n_keep=6, n_select=4,
+                           n_win=8, n_resp=20)],
     "mix3": [wl.scaled(c, n_chunks=32768 // c.chunk_size // 4, n_select=max(1, c.n_select // 2))
              for c in wl.mix_configs()[:3]],
 }
