@@ -117,9 +117,14 @@ struct Item {
   int k0, k1;         // decode: selected-chunk range in sel
 };
 
-// Work item `idx`; returns false when it holds no query rows.
+// Work item `idx`; returns false when it holds no query rows.  The decode
+// and chunk-mass instantiations compile only their own mode's branch (their
+// mode is fixed); the prefill instantiation dispatches on p.mode, which
+// measured faster for it.
+template <bool kPrefill, bool kMassMode>
 __device__ __forceinline__ bool resolve_item(const AttnParams& p, int idx, Item& it) {
-  if (p.mode == kModePrefill) {
+  constexpr bool kDecodeOnly = !kPrefill && !kMassMode;
+  if (kPrefill && p.mode == kModePrefill) {
     int pairs;
     if (idx < p.n_chunk_items) {
       it.kind = kChunk;
@@ -141,7 +146,7 @@ __device__ __forceinline__ bool resolve_item(const AttnParams& p, int idx, Item&
                                   : static_cast<long long>(it.chunk / p.layer_chunks) * p.n_win;
     it.split = 0;
     it.k0 = it.k1 = 0;
-  } else if (p.mode == kModeMass) {
+  } else if (!kDecodeOnly && (kMassMode || p.mode == kModeMass)) {
     // sequence b of the item (mass_item0 is non-decreasing, b < 64)
     int b = 0;
     while (b + 1 < p.mass_batch && p.mass_item0[b + 1] <= idx) ++b;
@@ -186,9 +191,10 @@ __device__ __forceinline__ bool resolve_item(const AttnParams& p, int idx, Item&
   return it.ta * p.Tq < it.n_t;
 }
 
+template <bool kPrefill, bool kMassMode>
 __device__ __forceinline__ bool item_shape_error(const AttnParams& p, int idx) {
-  if (p.mode == kModePrefill) return false;
-  if (p.mode == kModeMass) {
+  if (kPrefill && p.mode == kModePrefill) return false;
+  if (!(!kPrefill && !kMassMode) && (kMassMode || p.mode == kModeMass)) {
     int b = 0;
     while (b + 1 < p.mass_batch && p.mass_item0[b + 1] <= idx) ++b;
     const int lq0 = p.cu_lq[b], lq1 = p.cu_lq[b + 1];
@@ -263,11 +269,13 @@ __device__ __forceinline__ int groups_of(int len) { return (len + kGroupRows - 1
 // memory; run by the whole producer warp.  Decode: the selected chunks' slots
 // through the table, then (unless the call leaves it out) the live block,
 // the last segment, read from tensor 1.
+template <bool kPrefill, bool kMassMode>
 __device__ __forceinline__ int load_segments(const AttnParams& p, const Item& it, int32_t* seg_row,
                                              int32_t* seg_len, int32_t* seg_g0, int lane) {
   int nseg;
   __syncwarp();
-  if (it.kind == kMass) {
+  constexpr bool kDecodeOnly = !kPrefill && !kMassMode;
+  if (!kDecodeOnly && (kMassMode || it.kind == kMass)) {
     // one segment per chunk of the item, in table order
     nseg = it.k1 - it.k0;
     for (int i = lane; i < nseg; i += 32) {
@@ -277,7 +285,7 @@ __device__ __forceinline__ int load_segments(const AttnParams& p, const Item& it
       seg_row[i] = bad ? 0 : e.row;
       seg_len[i] = bad ? 0 : e.len;
     }
-  } else if (it.kind != kDecode) {
+  } else if (!kDecodeOnly && !kMassMode && it.kind != kDecode) {
     nseg = 1;
     if (lane == 0) {
       seg_row[0] = it.chunk * p.chunk_rows + 1;   // the content rows; BOS enters analytically
@@ -410,12 +418,13 @@ attention_kernel(const __grid_constant__ AttnParams p) {
     bool ok = true;
     for (int kk = 0, idx; ok && (idx = nth_item<kPrefill>(p, kk)) >= 0; ++kk) {
       Item it;
-      if (!resolve_item(p, idx, it)) {
-        if (lane == 0 && item_shape_error(p, idx)) raise_dev_err(p.dev_err, PFD_DEVERR_SHAPE);
+      if (!resolve_item<kPrefill, kMassMode>(p, idx, it)) {
+        if (lane == 0 && item_shape_error<kPrefill, kMassMode>(p, idx))
+          raise_dev_err(p.dev_err, PFD_DEVERR_SHAPE);
         continue;
       }
       const bool with_pv = it.kind != kWindow && it.kind != kMass;
-      const int nseg = load_segments(p, it, seg_row, seg_len, seg_g0, lane);
+      const int nseg = load_segments<kPrefill, kMassMode>(p, it, seg_row, seg_len, seg_g0, lane);
       const long long total = seg_g0[nseg];
       const int n_splits = it.kind == kDecode ? p.n_splits : 1;
       const int g_lo = static_cast<int>(total * it.split / n_splits);
@@ -541,7 +550,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
       const uint32_t q_bytes = static_cast<uint32_t>(q_rows) * D * 2;
       for (int kk = 0, idx; ok && (idx = nth_item<kPrefill>(p, kk)) >= 0; ++kk) {
         Item it;
-        if (!resolve_item(p, idx, it)) continue;
+        if (!resolve_item<kPrefill, kMassMode>(p, idx, it)) continue;
         // The Q buffers are free once every MMA of the previous item has
         // completed (q_empty), its last QK included.  Its first PV was issued
         // only after the epilogue two items back had released O (o_free), so
@@ -580,7 +589,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
       const uint64_t desc_ring_v = sw128_desc(s_base + L::kRing0, kPanelBytes, 1024);
       for (int kk = 0, idx; ok && (idx = nth_item<kPrefill>(p, kk)) >= 0; ++kk) {
         Item it;
-        if (!resolve_item(p, idx, it)) continue;
+        if (!resolve_item<kPrefill, kMassMode>(p, idx, it)) continue;
         const bool with_pv = it.kind != kWindow && it.kind != kMass;
         const int nx = it.has_b ? 2 : 1;
         bool ofree_done[2] = {items_done == 0, items_done == 0};
@@ -743,7 +752,7 @@ attention_kernel(const __grid_constant__ AttnParams p) {
     bool ok = true;
     for (int kk = 0, idx; ok && (idx = nth_item<kPrefill>(p, kk)) >= 0; ++kk) {
       Item it;
-      if (!resolve_item(p, idx, it)) continue;
+      if (!resolve_item<kPrefill, kMassMode>(p, idx, it)) continue;
       const bool with_pv = it.kind != kWindow && it.kind != kMass;
       const bool active = x == 0 || it.has_b;
       float m_used = -INFINITY, l_sum = 0.0f;
