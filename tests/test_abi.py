@@ -140,6 +140,25 @@ def test_decode_host_checks_and_plan(lib):
     assert ws2 >= 2 * 320 * 28 * (2 * 4 + 128 * 2)   # fp32 (m, l) and bf16 O per row and split
 
 
+def test_chunk_mass_items_per_call(lib):
+    """pfd_chunk_mass groups up to 8 consecutive chunks per item, the most
+    that still leaves 512 items: its workspace holds 8 partials per (item,
+    chunk of the item), so the size shows the choice."""
+    def ws(n_chunks, lq, hq=28, hkv=4):
+        return lib.pfd_chunk_mass_workspace(1, (ctypes.c_int32 * 2)(0, lq),
+                                            (ctypes.c_int32 * 2)(0, n_chunks), hq, hkv)
+    align = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    # 128K-like: 512 chunks, 576 live rows (16 pairs of 18-token tiles)
+    assert ws(512, 576) == align(512 // 8 * 4 * 16 * 8 * 8 * 4)
+    # 8K-like: 16 chunks, 320 rows (9 pairs): 2 chunks per item would give
+    # 8 * 4 * 9 = 288 items (< 512), so one chunk per item (576 items)
+    assert ws(16, 320) == align(16 * 4 * 9 * 1 * 8 * 4)
+    # 130 chunks, 9 pairs: 2 per item gives 65 * 36 = 2340 items; 4 per item
+    # 33 * 36 = 1188; 8 per item 17 * 36 = 612 >= 512
+    assert ws(130, 320) == align(17 * 36 * 8 * 8 * 4)
+    assert ws(0, 320) == 0
+
+
 def test_partial_and_merge_host_checks(lib):
     """pfd_decode_partial needs part_lse and self_keys in {0, 1};
     pfd_lse_merge checks its counts, head dim and alignment on the host."""
