@@ -38,6 +38,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GB300 data-sheet figures (HBM3e 7.9 TB/s, dense bf16 2.25 PFLOP/s): a second
+# denominator beside the measured one, for context only.
+NOMINAL_PEAKS = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 WORKLOADS = ["tiny", "8k", "32k", "128k", "mix"]
 
 
@@ -908,11 +911,14 @@ def roofline_fracs(cfgs, dec_ms_per_call, pre_ms, peaks):
     pflops, pbytes = total(prefill_flops, cfgs), total(prefill_bytes, cfgs)
     pre_s = pre_ms * 1e-3
     t_hbm, t_tc = pbytes / (hbm * 1e9), pflops / (burst * 1e12)
+    t_nominal = max(pbytes / (NOMINAL_PEAKS["hbm_gbs"] * 1e9),
+                    pflops / (NOMINAL_PEAKS["bf16_tflops"] * 1e12))
     return dict(decode_us=dec_ms_per_call * 1e3, decode_tflops=dec_tflops,
                 decode_frac=dec_tflops / burst, decode_frac_sustained=dec_tflops / sustained,
+                decode_frac_nominal=dec_tflops / NOMINAL_PEAKS["bf16_tflops"],
                 prefill_us=pre_ms * 1e3, prefill_tflops=pflops / pre_s / 1e12,
                 prefill_gbs=pbytes / pre_s / 1e9, prefill_bound="tensor" if t_tc >= t_hbm else "hbm",
-                prefill_frac=max(t_hbm, t_tc) / pre_s)
+                prefill_frac=max(t_hbm, t_tc) / pre_s, prefill_frac_nominal=t_nominal / pre_s)
 
 
 def run_profile(args, cfgs, device):
@@ -1000,11 +1006,14 @@ def main():
                      "frac": fr["decode_frac"],
                      "frac_of_sustained": fr["decode_frac_sustained"],
                      "sustained_peak": sustained,
+                     "frac_of_nominal": fr["decode_frac_nominal"],
+                     "nominal_peak": NOMINAL_PEAKS["bf16_tflops"],
                      "traffic": recorded_traffic(f"decode_attention_{args.config}.md")},
         "prefill_roofline": {"bound": fr["prefill_bound"], "achieved_gbs": fr["prefill_gbs"],
                              "hbm_peak_gbs": hbm, "achieved_tflops": fr["prefill_tflops"],
                              "tensor_peak_tflops": burst, "frac": fr["prefill_frac"],
-                             "peak_kind": f"{peak_kind} (HBM copy; bf16 burst)"},
+                             "peak_kind": f"{peak_kind} (HBM copy; bf16 burst)",
+                             "frac_of_nominal": fr["prefill_frac_nominal"]},
         "clocks": res["clocks"],
         "gpu_launches": res["launches"],
         "wall_s_timed_region": res["wall"],
@@ -1016,9 +1025,11 @@ def main():
             line["per_config"][name] = {
                 "decode_us_per_step": f2["decode_us"], "decode_tflops": f2["decode_tflops"],
                 "decode_frac": f2["decode_frac"], "decode_frac_sustained": f2["decode_frac_sustained"],
+                "decode_frac_nominal": f2["decode_frac_nominal"],
                 "decode_splits": o["n_splits"], "prefill_us": f2["prefill_us"],
                 "prefill_tflops": f2["prefill_tflops"], "prefill_gbs": f2["prefill_gbs"],
                 "prefill_bound": f2["prefill_bound"], "prefill_frac": f2["prefill_frac"],
+                "prefill_frac_nominal": f2["prefill_frac_nominal"],
                 "timing": "median of 5 graph replays after 3 warm-ups, L2 flushed between"}
     if next_rows:
         line["next_rows"] = {}

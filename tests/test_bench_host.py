@@ -58,3 +58,67 @@ def test_job_groups_same_shaped_sequences():
             used[r:r + c.n_keep + 1] += 1
         base += c.pool_rows
     assert int(used.max()) == 1
+
+
+# Algorithmic sizes of each workload, worked out by hand from its shapes
+# before the bench existed: prefill GFLOP, prefill MB, decode GFLOP per
+# step, decode MB per step, to 2-4 significant digits.
+WORKLOAD_SIZES = {
+    "tiny": (1.15, 5.6, 0.025, 0.23),
+    "8k": (64.1, 143, 6.18, 7.4),
+    "32k": (497, 572, 20.3, 13.7),
+    "128k": (545, 2292, 72.9, 26.4),
+    "mix": (5780, 4443, 87.5, 76),
+}
+
+
+def test_cost_model_matches_oracle_counts_and_table():
+    """The work the bench divides by is the method's: its flop counts equal
+    twice the oracle's counted multiply-adds for the same shapes, and every
+    figure agrees with the hand-worked sizes to their printed precision."""
+    import math
+
+    import bench
+    from oracle import pfd_oracle as orc
+    for name, (pg, pmb, dg, dmb) in WORKLOAD_SIZES.items():
+        cfgs = bench.job_configs(name)
+        for c in cfgs:
+            assert bench.prefill_flops(c) == 2 * orc.prefill_macs(
+                c.n_chunks, c.chunk_size, c.n_win, c.n_q_heads, c.head_dim)
+            kept = c.n_select * (c.n_keep + 1)
+            assert bench.decode_flops(c) == 2 * orc.decode_step_macs(
+                c.n_live, kept, c.n_q_heads, c.head_dim)
+        got = (bench.total(bench.prefill_flops, cfgs) / 1e9,
+               bench.total(bench.prefill_bytes, cfgs) / 1e6,
+               bench.total(bench.decode_flops, cfgs) / 1e9,
+               bench.total(bench.decode_bytes, cfgs) / 1e6)
+        for g, want in zip(got, (pg, pmb, dg, dmb)):
+            # printed to 2-3 significant digits
+            digits = max(2, len(str(want).replace(".", "").lstrip("0")))
+            assert math.isclose(g, want, rel_tol=0.6 * 10.0 ** (1 - digits)), (name, g, want)
+
+
+def test_roofline_fractions():
+    """Decode against the bf16 burst, sustained and nominal peaks; prefill
+    against the slower of its HBM and tensor times, measured and nominal."""
+    import math
+
+    import bench
+    cfgs = bench.job_configs("mix")
+    peaks = {"hbm_gbs": 6691.8, "bf16_tflops": 1910.6, "bf16_tflops_sustained": 1723.9}
+    fr = bench.roofline_fracs(cfgs, 0.090, 5.08, peaks)
+    tflops = bench.total(bench.decode_flops, cfgs) / 90e-6 / 1e12
+    assert math.isclose(fr["decode_tflops"], tflops)
+    assert math.isclose(fr["decode_frac"], tflops / 1910.6)
+    assert math.isclose(fr["decode_frac_sustained"], tflops / 1723.9)
+    assert math.isclose(fr["decode_frac_nominal"], tflops / 2250.0)
+    assert fr["prefill_bound"] == "tensor"
+    t_tc = bench.total(bench.prefill_flops, cfgs) / 1910.6e12
+    assert math.isclose(fr["prefill_frac"], t_tc / 5.08e-3)
+    assert math.isclose(fr["prefill_frac_nominal"],
+                        bench.total(bench.prefill_flops, cfgs) / 2250e12 / 5.08e-3)
+    # the 128K prefill moves more bytes than its flops take at the peak
+    fr = bench.roofline_fracs(bench.job_configs("128k"), 0.0839, 1.104, peaks)
+    assert fr["prefill_bound"] == "hbm"
+    t_hbm = bench.total(bench.prefill_bytes, bench.job_configs("128k")) / 6691.8e9
+    assert math.isclose(fr["prefill_frac"], t_hbm / 1.104e-3)
