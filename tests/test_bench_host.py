@@ -122,3 +122,61 @@ def test_roofline_fractions():
     assert fr["prefill_bound"] == "hbm"
     t_hbm = bench.total(bench.prefill_bytes, bench.job_configs("128k")) / 6691.8e9
     assert math.isclose(fr["prefill_frac"], t_hbm / 1.104e-3)
+
+
+def test_bench_line_carries_the_contract_keys(monkeypatch, capsys):
+    """bench.main's one JSON line, with the GPU timings faked: every key the
+    benchmark contract names is present and follows from the timings."""
+    import json
+    import math
+    import sys
+
+    import bench
+    peaks = {"hbm_gbs": 6691.8, "bf16_tflops": 1910.6, "bf16_tflops_sustained": 1723.9}
+    clocks = {"sm_mhz": 2070, "sm_max_mhz": 2070, "reasons": [], "samples": 11}
+    fake = dict(pre_ms=5.08, dec_ms=64 * 0.090, step_ms=5.08 + 64 * 0.090, wall=0.3,
+                clocks=clocks, launches=74 * 20, n_splits=1,
+                e2e=dict(dec_ms=64 * 0.144, dec_h2d=64 * 23_592_960, dec_d2h=64 * 18_350_080,
+                         pre_ms=60.0, pre_h2d=1_000_000))
+
+    def workload(name, rank, device, reps=5):
+        cfgs = bench.job_configs(name)
+        return dict(cfgs=cfgs, pre_ms=1.0, dec_ms=cfgs[0].n_steps * 0.05, n_splits=4,
+                    T=cfgs[0].n_steps)
+
+    monkeypatch.setattr(bench, "run_gpu", lambda args, cfgs, rank, world, device: dict(fake))
+    monkeypatch.setattr(bench, "time_workload", workload)
+    monkeypatch.setattr(bench, "time_scoring_head",
+                        lambda device: {"us": 238.1, "gbs": 6539.0, "bound": "hbm"})
+    monkeypatch.setattr(bench, "time_next_rows",
+                        lambda device: {"layers": {"us": 360.0, "tflops": 712.0, "bound": "tensor"}})
+    monkeypatch.setattr(bench, "load_peaks", lambda: (dict(peaks), "measured"))
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--no-cpu-baseline"])
+    for var in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(var, raising=False)
+    bench.main()
+    lines = capsys.readouterr().out.strip().splitlines()
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "clocks", "gpu_launches", "e2e"):
+        assert key in line, key
+    assert line["n_gpus"] == 1 and line["higher_is_better"] is True
+    assert line["scaling"] == "weak" and line["vs_baseline"] is None
+    assert line["config"]["workload"].startswith("mix")
+    cfgs = bench.job_configs("mix")
+    tflops = bench.total(bench.decode_flops, cfgs) / 90e-6 / 1e12
+    assert math.isclose(line["value"], tflops)
+    roof = line["roofline"]
+    assert {"bound", "achieved", "peak", "unit", "frac", "traffic"} <= set(roof)
+    assert roof["bound"] == "tensor" and roof["unit"] == "TFLOP/s" and roof["peak"] == 1910.6
+    assert math.isclose(roof["frac"], roof["achieved"] / roof["peak"])
+    assert math.isclose(roof["frac_of_nominal"], tflops / 2250.0)
+    e2e = line["e2e"]
+    assert {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"} <= set(e2e)
+    assert math.isclose(e2e["value"], bench.total(bench.decode_flops, cfgs) / 144e-6 / 1e12)
+    assert line["gpu_launches"] == 74 * 20 and line["clocks"] == clocks
+    assert set(line["per_config"]) == {"8k", "32k", "128k"}
+    assert math.isclose(line["next_rows"]["scoring_head"]["frac"], 6539.0 / 6691.8)
+    assert math.isclose(line["next_rows"]["layers"]["frac"], 712.0 / 1910.6)
