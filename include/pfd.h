@@ -281,8 +281,9 @@ pfd_status pfd_select_chunks_batched(const float* s_I, const float* s_P, const i
 
 /*
  * Number of KV splits pfd_decode_attention uses for these sizes when
- * n_splits == 0 (a plan that depends only on the arguments and the device's
- * SM count).  cu_lq_host, cu_k_host: [batch+1] int32 host memory.
+ * n_splits == 0 (a plan that depends only on the arguments and the current
+ * device's SM count; with no usable device, 152 SMs, a GB300's count, are
+ * assumed).  cu_lq_host, cu_k_host: [batch+1] int32 host memory.
  */
 int pfd_decode_plan_splits(int batch, const int32_t* cu_lq_host, const int32_t* cu_k_host,
                            int Hq, int Hkv, int D, int max_chunk_len);

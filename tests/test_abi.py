@@ -184,3 +184,28 @@ def test_partial_and_merge_host_checks(lib):
     with_self = _abi.pfd_decode_partial_workspace(1, [0, 320], [0, 4], 28, 4, 128, 257, 1, 0)
     assert with_self == _abi.pfd_decode_workspace(1, [0, 320], [0, 4], 28, 4, 128, 257, 0)
     assert _abi.pfd_decode_partial_workspace(1, [0, 320], [0, 4], 28, 4, 128, 257, 0, 1) == 0
+
+
+def test_decode_split_plan_of_the_bench_workloads(lib):
+    """The automatic split counts of the benchmark's decode calls on a
+    152-SM GB300 (the count the planner assumes with no device): the batched
+    mix has enough (sequence, KV head, query-tile pair) items to fill the GPU
+    unsplit; the single requests split their keys 4 or 7 ways."""
+    import torch
+
+    import bench
+    if torch.cuda.is_available():
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        if sms != 152:
+            pytest.skip(f"plan stated for 152 SMs, device has {sms}")
+    want = {"tiny": 1, "8k": 4, "32k": 4, "128k": 7, "mix": 1}
+    for name, splits in want.items():
+        cfgs = bench.job_configs(name)
+        cu_lq, cu_k = [0], [0]
+        for c in cfgs:
+            cu_lq.append(cu_lq[-1] + c.n_live)
+            cu_k.append(cu_k[-1] + c.n_select)
+        c0 = cfgs[0]
+        got = _abi.pfd_decode_plan_splits(len(cfgs), cu_lq, cu_k, c0.n_q_heads, c0.n_kv_heads,
+                                          c0.head_dim, max(c.n_keep + 1 for c in cfgs))
+        assert got == splits, (name, got)
