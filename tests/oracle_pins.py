@@ -523,6 +523,69 @@ def check_loglik_closed_forms(orc):
     assert np.max(np.abs(orc.chunk_loglik(shifted, np.array([0, 1, 0]))[1] - rows)) < 1e-12
 
 
+def check_hand_worked_pipeline(orc):
+    """A two-chunk example worked out by hand, end to end: prefill, ranking,
+    compaction, selection and one decode step, with keys whose logits are
+    logs of small integers so every probability is an exact fraction.
+
+    One query head, one KV head, D = 2, scale 1; every query is (1, 0), so a
+    key's logit is its first coordinate.
+      chunk 0 rows (BOS, t1, t2, t3): logits ln 6, 0, ln 2, ln 3 -> p = (6, 1, 2, 3) / 12
+      chunk 1 rows: all logits 0 -> p = 1/4 each
+    """
+    ln = math.log
+    rows = 4
+    k = np.zeros((2 * rows, 1, 2))
+    k[0:4, 0, 0] = [ln(6), 0.0, ln(2), ln(3)]
+    k[:, 0, 1] = [5.0, -3.0, 7.0, 1.0, 2.0, 9.0, -4.0, 6.0]        # never reaches a logit
+    v = np.zeros((2 * rows, 1, 2))
+    v[0:4, 0] = [[12, 0], [24, -12], [0, 12], [12, 12]]
+    v[4:8, 0] = [[4, 0], [0, 4], [4, 4], [0, 0]]
+    q = np.zeros((2 * rows, 1, 2))
+    q[:, 0, 0] = 1.0
+    q_win = np.zeros((2, 1, 2))
+    q_win[:, 0, 0] = 1.0
+
+    # chunk attention: each chunk's rows see only that chunk's four keys
+    out = orc.chunk_attention(q, k, v, 2, 3, 1.0)
+    assert np.allclose(out[0:4, 0], [11.0, 4.0], rtol=0, atol=1e-12), "chunk 0 output != (11, 4)"
+    assert np.allclose(out[4:8, 0], [2.0, 2.0], rtol=0, atol=1e-12), "chunk 1 output != (2, 2)"
+
+    # window scores: two identical window rows, so twice each probability
+    scores = orc.window_scores(q_win, k, 2, 3, 1.0)
+    assert np.allclose(scores, [[1.0, 1 / 6, 1 / 3, 1 / 2], [0.5, 0.5, 0.5, 0.5]],
+                       rtol=0, atol=1e-12), "window scores"
+
+    # top-2 of the content tokens: BOS (the largest score of chunk 0) is not
+    # ranked; chunk 1's four-way tie keeps the lowest indices
+    kept = orc.top_b(scores, 2)
+    assert kept.tolist() == [[1, 2], [0, 1]], f"kept {kept.tolist()}"
+
+    # slots at rows 5 and 0 of a 9-row pool: BOS then the kept rows
+    pool_k = np.full((9, 1, 2), np.nan)
+    pool_v = np.full((9, 1, 2), np.nan)
+    table = orc.compact(k, v, kept, np.array([5, 0]), 3, pool_k, pool_v)
+    assert table.tolist() == [[5, 3], [0, 3]]
+    assert np.array_equal(pool_v[5:8, 0], [[12, 0], [0, 12], [12, 12]])
+    assert np.array_equal(pool_v[0:3, 0], [[4, 0], [0, 4], [4, 4]])
+    assert np.isnan(pool_v[3:5]).all() and np.isnan(pool_v[8]).all(), "rows outside the slots"
+
+    # s = s_I + s_P = (0.5, -1.5): chunk 0 first
+    sel, s = orc.select_chunks(np.array([-1.0, -2.0]), np.array([1.5, 0.5]), 2)
+    assert sel.tolist() == [0, 1] and s.tolist() == [0.5, -1.5]
+
+    # decode, one live row with key logit 0 and value (0, 24): weights
+    # (6, 2, 3 | 1, 1, 1 | 1) / 15 over chunk 0's slot, chunk 1's slot, itself
+    k_self = np.array([[[0.0, 8.0]]])
+    v_self = np.array([[[0.0, 24.0]]])
+    dec, lse = orc.decode_attention(q[:1], k_self, v_self, pool_k, pool_v, table, sel, 1.0)
+    assert np.allclose(dec[0, 0], [116 / 15, 92 / 15], rtol=0, atol=1e-12), f"decode {dec[0, 0]}"
+    assert abs(lse[0, 0] - ln(15)) < 1e-12, "decode lse != ln 15"
+    # chunk 1 alone: weights (1, 1, 1 | 1) / 4
+    dec1, lse1 = orc.decode_attention(q[:1], k_self, v_self, pool_k, pool_v, table, sel[1:], 1.0)
+    assert np.allclose(dec1[0, 0], [2.0, 8.0], rtol=0, atol=1e-12) and abs(lse1[0, 0] - ln(4)) < 1e-12
+
+
 ALL_CHECKS = [
     check_chunk_attention, check_scores_vs_sdpa, check_scores_brute_force, check_scores_invariants,
     check_scores_single_row, check_top_b, check_select, check_split_equals_concat,
@@ -530,4 +593,5 @@ ALL_CHECKS = [
     check_scores_alt_readings, check_per_head_topb_and_compact, check_layers_are_independent,
     check_chunk_mass, check_reselect,
     check_decode_vs_sdpa, check_dense_equivalence, check_compact, check_cost_model,
+    check_hand_worked_pipeline,
 ]

@@ -157,6 +157,28 @@ def _reselect_single_rounding(s, mass, lam, n_select):
     return np.array(order[:n_select], np.int32), s2
 
 
+def _compact_without_bos(k, v, kept, slot_row, c, pool_k, pool_v):
+    rows = c + 1
+    n_chunks, n_keep = kept.shape
+    table = np.empty((n_chunks, 2), dtype=np.int32)
+    for j in range(n_chunks):
+        src = [j * rows + 1 + int(t) for t in kept[j]]
+        base = int(slot_row[j])
+        pool_k[base:base + n_keep] = k[src]
+        pool_v[base:base + n_keep] = v[src]
+        table[j] = (base, n_keep)
+    return table
+
+
+def _scores_without_bos_key(q_win, k, n, c, scale, counter=None):
+    rows = c + 1
+    keep = np.ones(k.shape[0], dtype=bool)
+    keep[::rows] = False
+    s = np.zeros((n, rows))
+    s[:, 1:] = orc.window_scores(q_win, k[keep], n, c - 1, scale)
+    return s
+
+
 MUTANTS = {
     "cross_chunk_attention": (Mutant(chunk_attention=_chunk_attention_global), pins.check_chunk_attention),
     "gqa_mapping": (Mutant(chunk_attention=_chunk_attention_bad_gqa), pins.check_chunk_attention),
@@ -182,6 +204,9 @@ MUTANTS = {
     "mass_without_normaliser": (Mutant(chunk_mass=_mass_without_normaliser), pins.check_chunk_mass),
     "reselect_single_rounding": (Mutant(reselect_chunks=_reselect_single_rounding),
                                  pins.check_reselect),
+    "compact_without_bos": (Mutant(compact=_compact_without_bos), pins.check_hand_worked_pipeline),
+    "scores_without_bos_key": (Mutant(window_scores=_scores_without_bos_key),
+                               pins.check_hand_worked_pipeline),
 }
 
 
