@@ -525,8 +525,9 @@ def check_loglik_closed_forms(orc):
 
 def check_hand_worked_pipeline(orc):
     """A two-chunk example worked out by hand, end to end: prefill, ranking,
-    compaction, selection and one decode step, with keys whose logits are
-    logs of small integers so every probability is an exact fraction.
+    compaction, selection, one decode step, chunk masses and reselection,
+    with keys whose logits are logs of small integers so every probability
+    is an exact fraction.
 
     One query head, one KV head, D = 2, scale 1; every query is (1, 0), so a
     key's logit is its first coordinate.
@@ -584,6 +585,17 @@ def check_hand_worked_pipeline(orc):
     # chunk 1 alone: weights (1, 1, 1 | 1) / 4
     dec1, lse1 = orc.decode_attention(q[:1], k_self, v_self, pool_k, pool_v, table, sel[1:], 1.0)
     assert np.allclose(dec1[0, 0], [2.0, 8.0], rtol=0, atol=1e-12) and abs(lse1[0, 0] - ln(4)) < 1e-12
+
+    # attention mass at the step's lse: 11/15 on chunk 0, 3/15 on chunk 1
+    # (the live row keeps the last 1/15)
+    mass = orc.chunk_mass(q[:1], pool_k, table, [0, 1], lse, 1.0)
+    assert np.allclose(mass, [11 / 15, 3 / 15], rtol=0, atol=1e-12), f"mass {mass}"
+    # reselecting one chunk from s = (-1.5, 0.5): chunk 0 overtakes chunk 1
+    # once lam * (11/15 - 3/15) > 2, that is lam > 3.75
+    for lam, want in ((0.0, 1), (3.5, 1), (4.0, 0)):
+        sel2, s2 = orc.reselect_chunks(np.array([-1.5, 0.5]), mass, lam, 1)
+        assert sel2.tolist() == [want], (lam, sel2.tolist())
+        assert np.allclose(s2, [-1.5 + lam * 11 / 15, 0.5 + lam / 5], rtol=0, atol=1e-6)
 
 
 ALL_CHECKS = [
