@@ -557,6 +557,14 @@ def check_hand_worked_pipeline(orc):
     assert np.allclose(scores, [[1.0, 1 / 6, 1 / 3, 1 / 2], [0.5, 0.5, 0.5, 0.5]],
                        rtol=0, atol=1e-12), "window scores"
 
+    # with the window's own keys (logits 0 and ln 2, e^x summing to 3) in the
+    # denominator: chunk 0's row sums 12 + 3 = 15, chunk 1's 4 + 3 = 7
+    k_win = np.zeros((2, 1, 2))
+    k_win[:, 0, 0] = [0.0, ln(2)]
+    alt = orc.window_scores_alt(q_win, k, 2, 3, 1.0, k_win=k_win)
+    assert np.allclose(alt, [[12 / 15, 2 / 15, 4 / 15, 6 / 15], [2 / 7] * 4], rtol=0, atol=1e-12), (
+        "scores with the window keys in the denominator")
+
     # top-2 of the content tokens: BOS (the largest score of chunk 0) is not
     # ranked; chunk 1's four-way tie keeps the lowest indices
     kept = orc.top_b(scores, 2)
