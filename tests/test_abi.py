@@ -43,6 +43,52 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(_abi.SIGNATURES) == set(declared_symbols())
 
 
+def declared_prototypes():
+    """{name: (return type, [parameter types])} of every prototype in the
+    header, with comments removed and parameter names dropped."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    protos = {}
+    for ret, name, params in re.findall(
+            r"([A-Za-z_][\w ]*?\**)\s*\b(pfd_[a-z_]+)\s*\(([^;{]*?)\)\s*;", text):
+        kinds = []
+        for prm in params.split(","):
+            prm = " ".join(prm.split())
+            if not prm or prm == "void":
+                continue
+            kinds.append(re.sub(r"\s*\b\w+$", "", prm) if not prm.endswith("*") else prm)
+        protos[name] = (" ".join(ret.split()), kinds)
+    return protos
+
+
+def _ctype_of(c_type):
+    """The ctypes type a C parameter or return type must be marshalled as."""
+    if "*" in c_type:
+        return ctypes.c_char_p if c_type.replace(" ", "") == "constchar*" else ctypes.c_void_p
+    base = c_type.replace("const ", "").strip()
+    return {"pfd_stream_t": ctypes.c_void_p, "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t,
+            "float": ctypes.c_float, "int32_t": ctypes.c_int32, "int": ctypes.c_int,
+            "pfd_status": ctypes.c_int}[base]
+
+
+def test_binding_signatures_match_the_header():
+    """Every ctypes signature has the header's parameter count and, position
+    by position, a type of the same width and kind, so no argument is
+    marshalled into the wrong register or truncated."""
+    protos = declared_prototypes()
+    assert set(protos) == set(_abi.SIGNATURES)
+    for name, (ret, params) in protos.items():
+        res, args = _abi.SIGNATURES[name]
+        assert len(args) == len(params), (name, len(args), len(params))
+        assert ctypes.sizeof(res) == ctypes.sizeof(_ctype_of(ret)), (name, ret)
+        for i, (got, c_type) in enumerate(zip(args, params)):
+            want = _ctype_of(c_type)
+            assert ctypes.sizeof(got) == ctypes.sizeof(want), (name, i, c_type)
+            assert (got is ctypes.c_float) == (want is ctypes.c_float), (name, i, c_type)
+            assert (got in (ctypes.c_void_p, ctypes.c_char_p)) == (
+                want in (ctypes.c_void_p, ctypes.c_char_p)), (name, i, c_type)
+
+
 def test_version_and_status_strings(lib):
     assert _abi.pfd_abi_version() == 2
     assert _abi.pfd_status_string(0) == "PFD_OK"
