@@ -53,6 +53,40 @@ def test_prefill_parity(name, cfg):
     P.check_pool(cfg, req, res)
 
 
+# The largest sizes the prefill accepts: C = 8192 content tokens per chunk,
+# and W * G = 512 window rows per KV group (W = 128 at G = 4, W = 256 at G = 2).
+MAX_CASES = [
+    ("c8192_wg512", wl.scaled(wl.TINY, n_chunks=2, chunk_size=8192, n_keep=2049, n_win=128)),
+    ("w256_g2", wl.scaled(wl.TINY, n_q_heads=4, n_kv_heads=2, n_chunks=2, chunk_size=300,
+                          n_keep=101, n_win=256)),
+]
+
+
+@pytest.mark.parametrize("name,cfg", MAX_CASES, ids=[c[0] for c in MAX_CASES])
+def test_prefill_maximum_sizes(name, cfg):
+    """Every score, kept set and pool slot; the output at each chunk's BOS,
+    first and last rows and 64 seeded rows (the oracle's full output at
+    C = 8192 would take it minutes)."""
+    req = wl.make_request(cfg, 0)
+    res = P.run_prefill(cfg, req)
+    assert int(res["dev_err"][0]) == 0
+    span = cfg.chunk_size + 1
+    gen = np.random.default_rng(7)
+    rows = sorted({int(r) for j in range(cfg.n_chunks)
+                   for r in [j * span, j * span + 1, (j + 1) * span - 1,
+                             *(j * span + gen.integers(0, span, 64))]})
+    o_ref = orc.chunk_attention_rows(f64(req["q"]), f64(req["k"]), f64(req["v"]), cfg.chunk_size,
+                                     rows, cfg.sm_scale)
+    P.assert_close_out(res["out"][rows].double().numpy(), o_ref, "prefill out, sampled rows")
+    s_ref = orc.window_scores(f64(req["q_win"]), f64(req["k"]), cfg.n_chunks, cfg.chunk_size,
+                              cfg.sm_scale)
+    s_gpu = res["scores"].double().numpy()
+    tol = P.score_tol(s_ref, cfg.n_win, cfg.n_q_heads)
+    assert (np.abs(s_gpu - s_ref) <= tol).all(), f"scores: max diff {np.abs(s_gpu - s_ref).max()}"
+    P.check_kept(res["kept_idx"].numpy(), s_ref, cfg.n_keep)
+    P.check_pool(cfg, req, res)
+
+
 def test_prefill_by_chunk_ranges_matches_one_call():
     """Chunks are independent up to selection: calling the prefill once per
     range of chunks (as a caller overlapping input copies would) gives the
