@@ -255,3 +255,89 @@ def test_decode_split_plan_of_the_bench_workloads(lib):
         got = _abi.pfd_decode_plan_splits(len(cfgs), cu_lq, cu_k, c0.n_q_heads, c0.n_kv_heads,
                                           c0.head_dim, max(c.n_keep + 1 for c in cfgs))
         assert got == splits, (name, got)
+
+
+def test_scoring_head_mass_and_reselect_host_checks(lib):
+    """Every call here is refused on the host (no call reaches a kernel)."""
+    i32 = ctypes.c_int32
+    # pfd_chunk_loglik(logits, labels, N, R, V, row_ll, score, dev_err, stream)
+    assert lib.pfd_chunk_loglik(None, 256, 2, 3, 50, 256, 256, None, None) == 1
+    assert lib.pfd_chunk_loglik(256, 256, 0, 3, 50, 256, 256, None, None) == 1
+    assert lib.pfd_chunk_loglik(256, 256, 2, 0, 50, 256, 256, None, None) == 1
+    assert lib.pfd_chunk_loglik(256, 256, 2, 3, 0, 256, 256, None, None) == 1
+    assert lib.pfd_chunk_loglik(256, 256, 65536, 32768, 50, 256, 256, None, None) == 2
+    assert lib.pfd_chunk_loglik(256, 256, 2, 3, 1 << 31, 256, 256, None, None) == 2
+
+    # pfd_chunk_mass(q, cu_lq, cu_lq_host, pool_k, pool_rows, table, table_len, cu_n_host,
+    #                lse, batch, Hq, Hkv, D, sm_scale, mass, dev_err, ws, ws_bytes, stream)
+    def mass(**over):
+        a = dict(q=256, cu_lq=256, lq_host=(i32 * 2)(0, 320), pk=256, pool_rows=100, table=256,
+                 table_len=16, n_host=(i32 * 2)(0, 16), lse=256, batch=1, Hq=28, Hkv=4, D=128,
+                 mass=256, ws=256, ws_bytes=1 << 20)
+        a.update(over)
+        return lib.pfd_chunk_mass(a["q"], a["cu_lq"], a["lq_host"], a["pk"], a["pool_rows"],
+                                  a["table"], a["table_len"], a["n_host"], a["lse"], a["batch"],
+                                  a["Hq"], a["Hkv"], a["D"], 0.0, a["mass"], None, a["ws"],
+                                  a["ws_bytes"], None)
+    assert mass(q=None) == 1
+    assert mass(lse=None) == 1
+    assert mass(D=96) == 2
+    assert mass(batch=65, lq_host=(i32 * 66)(*range(0, 66)), n_host=(i32 * 66)(*range(66))) == 2
+    assert mass(batch=0) == 1
+    assert mass(Hq=27) == 1
+    assert mass(n_host=(i32 * 2)(0, 17)) == 1          # more chunks than table entries
+    assert mass(lq_host=(i32 * 2)(1, 320)) == 1        # offsets must start at 0
+    assert mass(q=264) == 1                             # 8-byte aligned only
+    assert mass(ws_bytes=0) == 1
+    assert mass(ws=272) == 1                            # workspace must be 256-byte aligned
+    assert mass(pool_rows=1 << 31) == 2
+
+    # pfd_reselect_chunks(s, mass, lambda, cu_n, cu_k, batch, max_n, sel, s_out, stream)
+    assert lib.pfd_reselect_chunks(None, 256, 1.0, 256, 256, 1, 8, 256, None, None) == 1
+    assert lib.pfd_reselect_chunks(256, 256, 1.0, 256, 256, 0, 8, 256, None, None) == 1
+    assert lib.pfd_reselect_chunks(256, 256, 1.0, 256, 256, 1, 0, 256, None, None) == 1
+    assert lib.pfd_reselect_chunks(256, 256, -0.5, 256, 256, 1, 8, 256, None, None) == 1
+    assert lib.pfd_reselect_chunks(256, 256, float("nan"), 256, 256, 1, 8, 256, None, None) == 1
+    assert lib.pfd_reselect_chunks(256, 256, 1.0, 256, 256, 1, 16385, 256, None, None) == 2
+    assert lib.pfd_select_chunks_batched(8, 8, 8, 8, 1, 16385, 8, None, None) == 2
+
+
+def test_prefill_variant_host_checks(lib):
+    """pfd_chunk_prefill_ex and pfd_chunk_prefill_layers refuse bad
+    arguments on the host."""
+    def ex(per_kv_head=0, C=16, k_win=256, N=2):
+        return lib.pfd_chunk_prefill_ex(256, 256, 256, 256, k_win, N, C, 4, 4, 2, 64, 4, 0.0,
+                                        per_kv_head, 256, 256, 256, 256, 256, 10, 256, 256, None,
+                                        256, 1 << 20, None)
+    assert ex(per_kv_head=2) == 1
+    assert ex(per_kv_head=-1) == 1
+    assert ex(C=9000) == 2
+    assert ex(N=0) == 1
+
+    def layers(L=2, N=2, C=16, B=4, D=64):
+        return lib.pfd_chunk_prefill_layers(256, 256, 256, 256, L, N, C, 4, 4, 2, D, B, 0.0, 256,
+                                            256, 256, 256, 256, 10, 256, 256, None, 256, 1 << 20,
+                                            None)
+    assert layers(L=0) == 1
+    assert layers(B=17) == 1
+    assert layers(D=96) == 2
+    assert layers(L=1 << 15, N=1 << 10) == 2             # more than 2^24 chunks in one call
+    assert lib.pfd_chunk_prefill_layers_workspace(0, 2, 16, 4, 4, 2, 64, 4) == 0
+    one = lib.pfd_chunk_prefill_workspace(6, 16, 4, 4, 2, 64, 4)
+    assert lib.pfd_chunk_prefill_layers_workspace(3, 2, 16, 4, 4, 2, 64, 4) == one
+
+
+def test_static_scratch_host_checks(lib):
+    """The static-scratch decode refuses, before it looks up its buffer, a
+    missing batch, a negative split count and an explicit split count whose
+    partials exceed the buffer."""
+    i32 = ctypes.c_int32
+
+    def call(batch=1, n_splits=0, lq=320, k=4):
+        return lib.pfd_decode_attention_static_scratch(
+            256, 256, 256, 256, (i32 * 2)(0, lq), 256, 256, 100, 256, 16, 256, 256,
+            (i32 * 2)(0, k), batch, 28, 4, 128, 257, 0.0, n_splits, 256, None, None, None)
+    assert call(batch=0) == 1
+    assert call(n_splits=-1) == 1
+    # 64 splits of 8192 live rows x 28 heads: far above the 32 MiB buffer
+    assert call(n_splits=64, lq=8192, k=64) == 2
