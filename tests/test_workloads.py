@@ -3,7 +3,6 @@ import json
 import os
 
 import numpy as np
-import pytest
 import torch
 
 from sparse_chunked_kv_gb300 import workloads as wl
