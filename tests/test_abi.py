@@ -341,3 +341,37 @@ def test_static_scratch_host_checks(lib):
     assert call(n_splits=-1) == 1
     # 64 splits of 8192 live rows x 28 heads: far above the 32 MiB buffer
     assert call(n_splits=64, lq=8192, k=64) == 2
+
+
+C_CONSUMER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "pfd.h"
+
+int main(void) {
+  if (pfd_abi_version() != 2) return 1;
+  if (strcmp(pfd_status_string(PFD_ERR_UNSUPPORTED), "PFD_ERR_UNSUPPORTED") != 0) return 2;
+  /* host-side checks only: null inputs are refused before any launch */
+  if (pfd_select_chunks(NULL, NULL, 4, 2, NULL, NULL, NULL) != PFD_ERR_INVALID_ARG) return 3;
+  if (pfd_chunk_prefill_workspace(16, 512, 64, 28, 4, 128, 256) == 0) return 4;
+  printf("ok\n");
+  return 0;
+}
+"""
+
+
+def test_header_serves_a_plain_c_program(lib, tmp_path):
+    """include/pfd.h compiles as strict C11 and C++17, and a C program links
+    against libpfd.so and calls it with no torch or CUDA headers involved."""
+    src = tmp_path / "consumer.c"
+    src.write_text(C_CONSUMER)
+    inc = os.path.join(entry.ROOT, "include")
+    libdir = os.path.dirname(_abi.LIB_PATH)
+    flags = ["-Wall", "-Wextra", "-Werror", "-pedantic", "-I" + inc]
+    subprocess.run(["g++", "-std=c++17", *flags, "-x", "c++", "-fsyntax-only", str(src)],
+                   check=True)
+    exe = tmp_path / "consumer"
+    subprocess.run(["gcc", "-std=c11", *flags, str(src), "-L" + libdir, "-lpfd",
+                    "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], stdout=subprocess.PIPE, text=True)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", (out.returncode, out.stdout)
