@@ -399,7 +399,9 @@ pfd_status pfd_lse_merge(const pfd_bf16* part_o, const float* part_lse, int n_pa
  *   cu_lq        [batch+1] int32 device; cu_lq_host, cu_n_host [batch+1] host
  *   pool_k       [pool_rows, Hkv, D] bf16; table [table_len]
  *   lse          [total_lq, Hq] fp32 device
- *   mass         [table_len] fp32 device (written for the listed chunks)
+ *   mass         [table_len] fp32 device (written for the listed chunks; a
+ *                sequence with no live rows, Lq_b = 0, has no mass and its
+ *                entries are left as they were)
  *   workspace    >= pfd_chunk_mass_workspace(...) bytes
  * batch <= 64.  QK on the tensor cores over every chunk's slot (no PV);
  * fixed-order sums, so repeated calls give the same bits.
