@@ -426,6 +426,10 @@ def check_layers_are_independent(orc, seed=18):
         s1 = orc.window_scores(q_win[l], k[l], n, c, 0.3)
         assert np.max(np.abs(res[l]["scores"] - s1)) < 1e-12
         assert np.array_equal(res[l]["kept"], orc.top_b(s1, b))
+        for j in range(n):                      # layer l's pool holds layer l's own rows
+            src = [j * (c + 1)] + [j * (c + 1) + 1 + int(t) for t in res[l]["kept"][j]]
+            assert np.array_equal(res[l]["pool_k"][slot[j]:slot[j] + b + 1], k[l, src])
+            assert np.array_equal(res[l]["pool_v"][slot[j]:slot[j] + b + 1], v[l, src])
         for key in ("out", "scores", "kept", "pool_k", "pool_v", "table"):
             assert np.array_equal(res[l][key], rev[n_layers - 1 - l][key])
 

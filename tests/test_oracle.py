@@ -179,6 +179,18 @@ def _scores_without_bos_key(q_win, k, n, c, scale, counter=None):
     return s
 
 
+def _layers_share_window_rows(q, k, v, q_win, n, c, b, slot, pool_rows, scale):
+    return orc.chunk_prefill_layers(q, k, v, np.repeat(q_win[:1], q_win.shape[0], axis=0), n, c, b,
+                                    slot, pool_rows, scale)
+
+
+def _layers_share_one_pool(q, k, v, q_win, n, c, b, slot, pool_rows, scale):
+    layers = orc.chunk_prefill_layers(q, k, v, q_win, n, c, b, slot, pool_rows, scale)
+    for lay in layers:                      # every layer compacted into layer 0's pool
+        lay["pool_k"], lay["pool_v"] = layers[0]["pool_k"], layers[0]["pool_v"]
+    return layers
+
+
 MUTANTS = {
     "cross_chunk_attention": (Mutant(chunk_attention=_chunk_attention_global), pins.check_chunk_attention),
     "gqa_mapping": (Mutant(chunk_attention=_chunk_attention_bad_gqa), pins.check_chunk_attention),
@@ -205,6 +217,10 @@ MUTANTS = {
     "reselect_single_rounding": (Mutant(reselect_chunks=_reselect_single_rounding),
                                  pins.check_reselect),
     "compact_without_bos": (Mutant(compact=_compact_without_bos), pins.check_hand_worked_pipeline),
+    "layers_share_window_rows": (Mutant(chunk_prefill_layers=_layers_share_window_rows),
+                                 pins.check_layers_are_independent),
+    "layers_share_one_pool": (Mutant(chunk_prefill_layers=_layers_share_one_pool),
+                              pins.check_layers_are_independent),
     "scores_without_bos_key": (Mutant(window_scores=_scores_without_bos_key),
                                pins.check_hand_worked_pipeline),
 }
