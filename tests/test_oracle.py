@@ -191,6 +191,25 @@ def _layers_share_one_pool(q, k, v, q_win, n, c, b, slot, pool_rows, scale):
     return layers
 
 
+def _select_tie_high_index(s_i, s_p, n_select):
+    s = np.asarray(s_i, np.float32) + np.asarray(s_p, np.float32)
+    order = sorted(range(len(s)), key=lambda j: (-float(s[j]), -j))
+    return np.array(order[:n_select], np.int32), s
+
+
+def _mass_rows_only(q, pool_k, table, chunks, lse, scale):
+    # averaged over the live rows but summed over the heads
+    return orc.chunk_mass(q, pool_k, table, chunks, lse, scale) * q.shape[1]
+
+
+def _scores_alt_wrong_group(q_win, k, n, c, scale, per_kv_head=False, k_win=None):
+    # query head h read against KV head h % Hkv instead of h // G
+    hq, hkv = q_win.shape[1], k.shape[1]
+    perm = [h2 for g in range(hkv) for h2 in range(g, hq, hkv)]
+    return orc.window_scores_alt(q_win[:, perm], k, n, c, scale, per_kv_head=per_kv_head,
+                                 k_win=k_win)
+
+
 MUTANTS = {
     "cross_chunk_attention": (Mutant(chunk_attention=_chunk_attention_global), pins.check_chunk_attention),
     "gqa_mapping": (Mutant(chunk_attention=_chunk_attention_bad_gqa), pins.check_chunk_attention),
@@ -217,6 +236,10 @@ MUTANTS = {
     "reselect_single_rounding": (Mutant(reselect_chunks=_reselect_single_rounding),
                                  pins.check_reselect),
     "compact_without_bos": (Mutant(compact=_compact_without_bos), pins.check_hand_worked_pipeline),
+    "select_tie_high_index": (Mutant(select_chunks=_select_tie_high_index), pins.check_select),
+    "mass_summed_over_heads": (Mutant(chunk_mass=_mass_rows_only), pins.check_chunk_mass),
+    "alt_scores_wrong_kv_group": (Mutant(window_scores_alt=_scores_alt_wrong_group),
+                                  pins.check_scores_alt_readings),
     "layers_share_window_rows": (Mutant(chunk_prefill_layers=_layers_share_window_rows),
                                  pins.check_layers_are_independent),
     "layers_share_one_pool": (Mutant(chunk_prefill_layers=_layers_share_one_pool),
